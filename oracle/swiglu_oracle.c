@@ -1,0 +1,206 @@
+/*
+ * Plain CPU oracle for the fused SwiGLU up-projection.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may call, link or load
+ * this file: only the tests, the smoke check and the bench's CPU-baseline leg
+ * use it. It shares no code, header or constant with the CUDA library.
+ *
+ * What it computes ("Tile-Level Activation Overlap for Efficient LLM
+ * Inference", Section 1 Introduction, the gated-MLP definition; restated in
+ * the technical summary's problem statement): for every output row m and
+ * column n,
+ *
+ *     Gate[m,n] = sum_k A[m,k] * W1[k,n]
+ *     Up[m,n]   = sum_k A[m,k] * W2[k,n]
+ *     Y[m,n]    = SiLU(Gate[m,n]) * Up[m,n],   SiLU(x) = x / (1 + e^-x)
+ *
+ * A [M,K], W1 [K,N], W2 [K,N] and Y [M,N] are row-major arrays of BF16 bit
+ * patterns. Every BF16 x BF16 product is exact in binary64, the K-term sums
+ * run in binary64 in increasing k, SiLU and the final product are evaluated
+ * in binary64, and the result is rounded ONCE to BF16 with
+ * round-to-nearest-even, straight from the double (going through binary32
+ * first could round twice).
+ *
+ * The loops are the definition written out: no blocking, no reordering of
+ * the k sum, no fusion beyond the definition. Rows are split across threads;
+ * each output element is computed by exactly one thread in the fixed order
+ * above, so the result does not depend on the thread count.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* BF16 bit pattern -> binary64. A BF16 value is the upper half of a binary32
+ * pattern, so the conversion is exact. */
+double oracle_bf16_to_double(uint16_t b)
+{
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* binary64 -> BF16 bit pattern, round to nearest, ties to even.
+ * BF16: 1 sign bit, 8 exponent bits (bias 127), 7 stored significand bits.
+ * For |x| in [2^E, 2^(E+1)) with E >= -126 the spacing of BF16 values is
+ * 2^(E-7); below 2^-126 (subnormals) it is fixed at 2^-133. Dividing |x| by
+ * the spacing is an exact power-of-two scaling, nearbyint() rounds the
+ * quotient to the nearest integer with ties to even (default rounding mode),
+ * and multiplying back is exact. Results at or above 2^128 overflow to
+ * infinity. */
+uint16_t oracle_double_to_bf16(double x)
+{
+    if (isnan(x))
+        return (uint16_t)0x7FC0;
+    uint16_t sign = signbit(x) ? (uint16_t)0x8000 : (uint16_t)0;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80);
+    int e;
+    (void)frexp(a, &e);          /* a = f * 2^e with f in [0.5, 1) */
+    int E = e - 1;               /* a in [2^E, 2^(E+1)) */
+    if (E < -126)
+        E = -126;
+    double spacing = ldexp(1.0, E - 7);
+    double r = nearbyint(a / spacing);
+    double v = r * spacing;
+    if (v >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80);
+    float f = (float)v;          /* v is a BF16 value: exact in binary32 */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)(sign | (uint16_t)(bits >> 16));
+}
+
+/* SiLU (Swish with beta = 1): x * sigmoid(x) = x / (1 + e^-x). For x far
+ * below zero e^-x overflows to +inf and the quotient is -0, the limit. */
+double oracle_silu(double x)
+{
+    return x / (1.0 + exp(-x));
+}
+
+typedef struct {
+    const uint16_t *A, *W1, *W2;
+    int64_t M, N, K;
+    const int64_t *rows;   /* NULL: rows 0..nrows-1 */
+    int64_t nrows;
+    uint16_t *Y;           /* [nrows, N] bf16 bits, may be NULL */
+    double *Yd;            /* [nrows, N] unrounded SiLU(g)*u, may be NULL */
+    double *G, *U;         /* [nrows, N], may be NULL */
+    int64_t r_begin, r_end;
+    int status;
+} job_t;
+
+static void *run_rows(void *arg)
+{
+    job_t *j = (job_t *)arg;
+    const int64_t N = j->N, K = j->K;
+    double *g = (double *)malloc((size_t)N * sizeof(double));
+    double *u = (double *)malloc((size_t)N * sizeof(double));
+    if (!g || !u) {
+        free(g);
+        free(u);
+        j->status = 1;
+        return NULL;
+    }
+    for (int64_t r = j->r_begin; r < j->r_end; ++r) {
+        const int64_t m = j->rows ? j->rows[r] : r;
+        const uint16_t *a_row = j->A + m * K;
+        for (int64_t n = 0; n < N; ++n) {
+            g[n] = 0.0;
+            u[n] = 0.0;
+        }
+        /* Gate = A x W1 and Up = A x W2, summed over k in increasing order. */
+        for (int64_t k = 0; k < K; ++k) {
+            const double a = oracle_bf16_to_double(a_row[k]);
+            const uint16_t *w1 = j->W1 + k * N;
+            const uint16_t *w2 = j->W2 + k * N;
+            for (int64_t n = 0; n < N; ++n) {
+                g[n] += a * oracle_bf16_to_double(w1[n]);
+                u[n] += a * oracle_bf16_to_double(w2[n]);
+            }
+        }
+        /* Y = SiLU(Gate) (.) Up, rounded once to BF16. */
+        for (int64_t n = 0; n < N; ++n) {
+            const double y = oracle_silu(g[n]) * u[n];
+            if (j->Y)
+                j->Y[r * N + n] = oracle_double_to_bf16(y);
+            if (j->Yd)
+                j->Yd[r * N + n] = y;
+            if (j->G)
+                j->G[r * N + n] = g[n];
+            if (j->U)
+                j->U[r * N + n] = u[n];
+        }
+    }
+    free(g);
+    free(u);
+    return NULL;
+}
+
+/*
+ * Computes the rows listed in `rows` (or rows 0..nrows-1 when rows is NULL)
+ * of Y = SiLU(A x W1) (.) (A x W2). Outputs are indexed by position in the
+ * row list. Any of Y, Yd, G, U may be NULL. nthreads <= 0 uses every online
+ * core. Returns 0 on success, 1 on bad arguments or allocation failure.
+ */
+int oracle_swiglu_up(const uint16_t *A, const uint16_t *W1, const uint16_t *W2,
+                     int64_t M, int64_t N, int64_t K,
+                     const int64_t *rows, int64_t nrows,
+                     uint16_t *Y, double *Yd, double *G, double *U,
+                     int nthreads)
+{
+    if (!A || !W1 || !W2 || M < 0 || N < 0 || K < 0 || nrows < 0)
+        return 1;
+    if (!rows && nrows > M)
+        return 1;
+    for (int64_t r = 0; rows && r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= M)
+            return 1;
+    if (nrows == 0 || N == 0)
+        return 0;
+    if (nthreads <= 0) {
+        long c = sysconf(_SC_NPROCESSORS_ONLN);
+        nthreads = c > 0 ? (int)c : 1;
+    }
+    if (nthreads > nrows)
+        nthreads = (int)nrows;
+
+    job_t *jobs = (job_t *)calloc((size_t)nthreads, sizeof(job_t));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    char *created = (char *)calloc((size_t)nthreads, 1);
+    if (!jobs || !tids || !created) {
+        free(jobs);
+        free(tids);
+        free(created);
+        return 1;
+    }
+    int status = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        job_t *j = &jobs[t];
+        j->A = A; j->W1 = W1; j->W2 = W2;
+        j->M = M; j->N = N; j->K = K;
+        j->rows = rows; j->nrows = nrows;
+        j->Y = Y; j->Yd = Yd; j->G = G; j->U = U;
+        j->r_begin = nrows * t / nthreads;
+        j->r_end = nrows * (t + 1) / nthreads;
+        if (pthread_create(&tids[t], NULL, run_rows, j) == 0)
+            created[t] = 1;
+        else
+            run_rows(j);   /* no thread available: run it here */
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        if (created[t])
+            pthread_join(tids[t], NULL);
+        status |= jobs[t].status;
+    }
+    free(jobs);
+    free(tids);
+    free(created);
+    return status;
+}

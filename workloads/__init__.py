@@ -1,0 +1,139 @@
+"""Seeded synthetic inputs shaped like the Qwen-2.5 gated-MLP up-projections.
+
+Shared by the oracle-side tests and the CUDA-side tests and bench: this module
+only draws random numbers and rounds them to BF16 bit patterns. It holds none
+of the method's arithmetic (no products, sums or activations).
+
+Shapes ("Tile-Level Activation Overlap for Efficient LLM Inference", Section 1
+Introduction and the technical summary's results: Qwen-2.5 0.5B to 72B MLPs,
+BF16). The pages print no batch sizes or value distributions; the token counts
+M and the distributions below are this library's workload definition:
+
+* A  ~ N(0, 1), W1 and W2 ~ N(0, 1/K) (std K^-1/2), drawn in binary32 with
+  numpy's PCG64 and rounded to BF16 (round to nearest, ties to even).
+* Seeds: A = 1000 + c, W1 = 2000 + c, W2 = 3000 + c, with c the row index of
+  the table below ("1s" reuses row 1's seeds).
+* "stress": A multiplied by 8 (an exact power of two) so that pre-activations
+  have std ~8 and SiLU saturates at both ends.
+* "outlier": round(0.01 K) columns of A, chosen by a PCG64 permutation with
+  seed 4000 + c, are multiplied by 20 in binary32 before rounding to BF16.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    c: str            # row label: "0", "1", "1s", "2" ... "11"
+    name: str
+    M: int            # tokens
+    K: int            # hidden size
+    N: int            # intermediate size
+    variant: str = "plain"   # "plain" | "stress" | "outlier"
+
+    @property
+    def seed_index(self) -> int:
+        return int(self.c.rstrip("s"))
+
+    @property
+    def flops(self) -> int:
+        """4*M*N*K: two products of 2*M*N*K multiply-adds each."""
+        return 4 * self.M * self.N * self.K
+
+    @property
+    def roofline_bytes(self) -> int:
+        """Compulsory HBM bytes: A, W1, W2 read once and Y written once, BF16."""
+        return 2 * (self.M * self.K + 2 * self.K * self.N + self.M * self.N)
+
+
+WORKLOADS = [
+    Workload("0", "qwen2.5-0.5b", 128, 896, 4864),
+    Workload("1", "qwen2.5-1.5b", 2048, 1536, 8960),
+    Workload("1s", "qwen2.5-1.5b-stress", 2048, 1536, 8960, "stress"),
+    Workload("2", "qwen2.5-7b-m1", 1, 3584, 18944),
+    Workload("3", "qwen2.5-7b-m16", 16, 3584, 18944),
+    Workload("4", "qwen2.5-7b-m128", 128, 3584, 18944),
+    Workload("5", "qwen2.5-7b-m512", 512, 3584, 18944),
+    Workload("6", "qwen2.5-7b-m2048", 2048, 3584, 18944),
+    Workload("7", "qwen2.5-7b-m8192", 8192, 3584, 18944),
+    Workload("8", "qwen2.5-32b-m64", 64, 5120, 27648, "outlier"),
+    Workload("9", "qwen2.5-32b-m4096", 4096, 5120, 27648, "outlier"),
+    Workload("10", "qwen2.5-72b-m32", 32, 8192, 29568),
+    Workload("11", "qwen2.5-72b-m8192", 8192, 8192, 29568),
+]
+
+BY_LABEL = {w.c: w for w in WORKLOADS}
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """binary32 array -> BF16 bit patterns (uint16), round to nearest even.
+
+    Inputs here are finite normals, so NaN handling is not needed; it is kept
+    anyway (quiet NaN) so that the helper is total.
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32)
+    out = np.empty(u.shape, dtype=np.uint16)
+    step = 1 << 24
+    flat_u = u.reshape(-1)
+    flat_o = out.reshape(-1)
+    for s in range(0, flat_u.size, step):
+        v = flat_u[s:s + step].astype(np.uint64)
+        r = (v + 0x7FFF + ((v >> 16) & 1)) >> 16
+        nan = (v & 0x7FFFFFFF) > 0x7F800000
+        r = np.where(nan, (v >> 16) | 0x40, r)
+        flat_o[s:s + step] = r.astype(np.uint16)
+    return out
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns -> binary32 (exact)."""
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def _normal(seed: int, shape, scale: float) -> np.ndarray:
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if scale != 1.0:
+        x *= np.float32(scale)
+    return x
+
+
+def make_A(w: Workload) -> np.ndarray:
+    c = w.seed_index
+    a = _normal(1000 + c, (w.M, w.K), 1.0)
+    if w.variant == "stress":
+        a *= np.float32(8.0)
+    elif w.variant == "outlier":
+        n_out = int(round(0.01 * w.K))
+        perm = np.random.Generator(np.random.PCG64(4000 + c)).permutation(w.K)
+        a[:, perm[:n_out]] *= np.float32(20.0)
+    return f32_to_bf16_bits(a)
+
+
+def make_W(w: Workload, which: int) -> np.ndarray:
+    """which = 1 (gate weight W1) or 2 (up weight W2); [K, N] row-major."""
+    assert which in (1, 2)
+    c = w.seed_index
+    seed = (2000 if which == 1 else 3000) + c
+    return f32_to_bf16_bits(_normal(seed, (w.K, w.N), float(w.K) ** -0.5))
+
+
+def make_inputs(w: Workload):
+    """(A [M,K], W1 [K,N], W2 [K,N]) as BF16 bit patterns (uint16)."""
+    return make_A(w), make_W(w, 1), make_W(w, 2)
+
+
+def random_case(M: int, N: int, K: int, seed: int, a_scale: float = 1.0):
+    """A small seeded case for parity tests at arbitrary (ragged) shapes."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    a = rng.standard_normal(size=(M, K), dtype=np.float32) * np.float32(a_scale)
+    s = np.float32(float(max(K, 1)) ** -0.5)
+    w1 = rng.standard_normal(size=(K, N), dtype=np.float32) * s
+    w2 = rng.standard_normal(size=(K, N), dtype=np.float32) * s
+    return f32_to_bf16_bits(a), f32_to_bf16_bits(w1), f32_to_bf16_bits(w2)

@@ -63,7 +63,7 @@ def _load():
     lib.oracle_silu.restype = ctypes.c_double
     lib.oracle_swiglu_up.argtypes = [u16p, u16p, u16p,
                                      ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
-                                     i64p, ctypes.c_int64,
+                                     i64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                      u16p, f64p, f64p, f64p, ctypes.c_int]
     lib.oracle_swiglu_up.restype = ctypes.c_int
     _lib = lib
@@ -90,12 +90,13 @@ def _ptr(a, ctype):
 
 def swiglu_up(A: np.ndarray, W1: np.ndarray, W2: np.ndarray, rows=None,
               want_unrounded: bool = False, want_gate_up: bool = False,
-              nthreads: int = 0):
+              nthreads: int = 0, cols=None):
     """Oracle Y for BF16 bit-pattern inputs (numpy uint16).
 
     A is [M, K], W1 and W2 are [K, N]. ``rows`` selects output rows (default:
-    all). Returns a dict with ``Y`` ([R, N] uint16 BF16 bits) and, on request,
-    ``Yd`` (unrounded binary64 SiLU(g)*u), ``G`` and ``U`` (binary64 sums).
+    all), ``cols`` = (n0, n1) a column range (default: all). Returns a dict
+    with ``Y`` ([R, C] uint16 BF16 bits) and, on request, ``Yd`` (unrounded
+    binary64 SiLU(g)*u), ``G`` and ``U`` (binary64 sums).
     """
     lib = _load()
     A = np.ascontiguousarray(A, dtype=np.uint16)
@@ -111,13 +112,15 @@ def swiglu_up(A: np.ndarray, W1: np.ndarray, W2: np.ndarray, rows=None,
     else:
         rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
         R = rows_arr.shape[0]
-    Y = np.empty((R, N), dtype=np.uint16)
-    Yd = np.empty((R, N), dtype=np.float64) if want_unrounded else None
-    G = np.empty((R, N), dtype=np.float64) if want_gate_up else None
-    U = np.empty((R, N), dtype=np.float64) if want_gate_up else None
+    n0, n1 = (0, N) if cols is None else (int(cols[0]), int(cols[1]))
+    C = max(0, n1 - n0)
+    Y = np.empty((R, C), dtype=np.uint16)
+    Yd = np.empty((R, C), dtype=np.float64) if want_unrounded else None
+    G = np.empty((R, C), dtype=np.float64) if want_gate_up else None
+    U = np.empty((R, C), dtype=np.float64) if want_gate_up else None
     rc = lib.oracle_swiglu_up(_ptr(A, ctypes.c_uint16), _ptr(W1, ctypes.c_uint16),
                               _ptr(W2, ctypes.c_uint16), M, N, K,
-                              _ptr(rows_arr, ctypes.c_int64), R,
+                              _ptr(rows_arr, ctypes.c_int64), R, n0, n1,
                               _ptr(Y, ctypes.c_uint16), _ptr(Yd, ctypes.c_double),
                               _ptr(G, ctypes.c_double), _ptr(U, ctypes.c_double),
                               int(nthreads))

@@ -87,11 +87,12 @@ double oracle_silu(double x)
 typedef struct {
     const uint16_t *A, *W1, *W2;
     int64_t M, N, K;
+    int64_t n0, n1;        /* output columns [n0, n1) */
     const int64_t *rows;   /* NULL: rows 0..nrows-1 */
     int64_t nrows;
-    uint16_t *Y;           /* [nrows, N] bf16 bits, may be NULL */
-    double *Yd;            /* [nrows, N] unrounded SiLU(g)*u, may be NULL */
-    double *G, *U;         /* [nrows, N], may be NULL */
+    uint16_t *Y;           /* [nrows, n1-n0] bf16 bits, may be NULL */
+    double *Yd;            /* [nrows, n1-n0] unrounded SiLU(g)*u, may be NULL */
+    double *G, *U;         /* [nrows, n1-n0], may be NULL */
     int64_t r_begin, r_end;
     int status;
 } job_t;
@@ -99,9 +100,9 @@ typedef struct {
 static void *run_rows(void *arg)
 {
     job_t *j = (job_t *)arg;
-    const int64_t N = j->N, K = j->K;
-    double *g = (double *)malloc((size_t)N * sizeof(double));
-    double *u = (double *)malloc((size_t)N * sizeof(double));
+    const int64_t N = j->N, K = j->K, n0 = j->n0, n1 = j->n1, W = n1 - n0;
+    double *g = (double *)malloc((size_t)W * sizeof(double));
+    double *u = (double *)malloc((size_t)W * sizeof(double));
     if (!g || !u) {
         free(g);
         free(u);
@@ -111,31 +112,31 @@ static void *run_rows(void *arg)
     for (int64_t r = j->r_begin; r < j->r_end; ++r) {
         const int64_t m = j->rows ? j->rows[r] : r;
         const uint16_t *a_row = j->A + m * K;
-        for (int64_t n = 0; n < N; ++n) {
-            g[n] = 0.0;
-            u[n] = 0.0;
+        for (int64_t i = 0; i < W; ++i) {
+            g[i] = 0.0;
+            u[i] = 0.0;
         }
         /* Gate = A x W1 and Up = A x W2, summed over k in increasing order. */
         for (int64_t k = 0; k < K; ++k) {
             const double a = oracle_bf16_to_double(a_row[k]);
-            const uint16_t *w1 = j->W1 + k * N;
-            const uint16_t *w2 = j->W2 + k * N;
-            for (int64_t n = 0; n < N; ++n) {
-                g[n] += a * oracle_bf16_to_double(w1[n]);
-                u[n] += a * oracle_bf16_to_double(w2[n]);
+            const uint16_t *w1 = j->W1 + k * N + n0;
+            const uint16_t *w2 = j->W2 + k * N + n0;
+            for (int64_t i = 0; i < W; ++i) {
+                g[i] += a * oracle_bf16_to_double(w1[i]);
+                u[i] += a * oracle_bf16_to_double(w2[i]);
             }
         }
         /* Y = SiLU(Gate) (.) Up, rounded once to BF16. */
-        for (int64_t n = 0; n < N; ++n) {
-            const double y = oracle_silu(g[n]) * u[n];
+        for (int64_t i = 0; i < W; ++i) {
+            const double y = oracle_silu(g[i]) * u[i];
             if (j->Y)
-                j->Y[r * N + n] = oracle_double_to_bf16(y);
+                j->Y[r * W + i] = oracle_double_to_bf16(y);
             if (j->Yd)
-                j->Yd[r * N + n] = y;
+                j->Yd[r * W + i] = y;
             if (j->G)
-                j->G[r * N + n] = g[n];
+                j->G[r * W + i] = g[i];
             if (j->U)
-                j->U[r * N + n] = u[n];
+                j->U[r * W + i] = u[i];
         }
     }
     free(g);
@@ -145,24 +146,27 @@ static void *run_rows(void *arg)
 
 /*
  * Computes the rows listed in `rows` (or rows 0..nrows-1 when rows is NULL)
- * of Y = SiLU(A x W1) (.) (A x W2). Outputs are indexed by position in the
- * row list. Any of Y, Yd, G, U may be NULL. nthreads <= 0 uses every online
- * core. Returns 0 on success, 1 on bad arguments or allocation failure.
+ * and the columns [n0, n1) of Y = SiLU(A x W1) (.) (A x W2). Outputs are
+ * [nrows, n1-n0], indexed by position in the row list and by n - n0. Any of
+ * Y, Yd, G, U may be NULL. nthreads <= 0 uses every online core. Returns 0 on
+ * success, 1 on bad arguments or allocation failure.
  */
 int oracle_swiglu_up(const uint16_t *A, const uint16_t *W1, const uint16_t *W2,
                      int64_t M, int64_t N, int64_t K,
-                     const int64_t *rows, int64_t nrows,
+                     const int64_t *rows, int64_t nrows, int64_t n0, int64_t n1,
                      uint16_t *Y, double *Yd, double *G, double *U,
                      int nthreads)
 {
     if (!A || !W1 || !W2 || M < 0 || N < 0 || K < 0 || nrows < 0)
+        return 1;
+    if (n0 < 0 || n1 > N || n0 > n1)
         return 1;
     if (!rows && nrows > M)
         return 1;
     for (int64_t r = 0; rows && r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= M)
             return 1;
-    if (nrows == 0 || N == 0)
+    if (nrows == 0 || n1 == n0)
         return 0;
     if (nthreads <= 0) {
         long c = sysconf(_SC_NPROCESSORS_ONLN);
@@ -185,6 +189,7 @@ int oracle_swiglu_up(const uint16_t *A, const uint16_t *W1, const uint16_t *W2,
         job_t *j = &jobs[t];
         j->A = A; j->W1 = W1; j->W2 = W2;
         j->M = M; j->N = N; j->K = K;
+        j->n0 = n0; j->n1 = n1;
         j->rows = rows; j->nrows = nrows;
         j->Y = Y; j->Yd = Yd; j->G = G; j->U = U;
         j->r_begin = nrows * t / nthreads;

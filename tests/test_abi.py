@@ -1,0 +1,145 @@
+"""C-ABI checks that need no GPU: the library builds, loads without a driver,
+exports every function include/swiglu.h declares, and rejects bad arguments
+on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from tests import parity
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gemm_swiglu_mlp_gb300 import build
+    build.build()
+    import gemm_swiglu_mlp_gb300 as sg
+    return sg.load_library()
+
+
+def _declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(swiglu_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("swiglu_pack_weights", "swiglu_up_forward", "swiglu_packed_weight_bytes",
+                     "swiglu_check_device_status", "swiglu_status_string",
+                     "swiglu_workspace_bytes"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import gemm_swiglu_mlp_gb300 as sg
+    for name in _declared_functions():
+        assert hasattr(lib, name), name          # dlsym succeeds
+    assert set(_declared_functions()) <= set(sg.EXPORTED_SYMBOLS)
+
+
+def test_status_strings_and_version(lib):
+    import gemm_swiglu_mlp_gb300 as sg
+    assert sg.swiglu_status_string(0) == "SWIGLU_OK"
+    assert sg.swiglu_status_string(4) == "SWIGLU_ERR_DEVICE_TIMEOUT"
+    assert sg.swiglu_status_string(77) == "SWIGLU_ERR_UNKNOWN"
+    assert sg.swiglu_version() >= 1
+
+
+def test_packed_weight_bytes(lib):
+    import gemm_swiglu_mlp_gb300 as sg
+    assert sg.swiglu_packed_weight_bytes(4864, 896) == 2 * 4864 * 896 * 2
+    assert sg.swiglu_packed_weight_bytes(136, 64) == 2 * 256 * 64 * 2    # padded to 256 columns
+    assert sg.swiglu_packed_weight_bytes(0, 64) == 0
+    assert sg.swiglu_packed_weight_bytes(8, -1) == 0
+
+
+def test_workspace_query_is_consistent(lib):
+    import gemm_swiglu_mlp_gb300 as sg
+    for M, N, K in [(1, 18944, 3584), (2048, 8960, 1536), (8192, 29568, 8192)]:
+        assert sg.swiglu_workspace_bytes(M, N, K) >= 0
+
+
+P = 0x10000          # fake, 16-byte aligned "device" addresses: never dereferenced
+Q = 0x40000000
+R = 0x80000000
+
+
+@pytest.mark.parametrize("args", [
+    (0, Q, R, 4, 8, 8), (P, 0, R, 4, 8, 8), (P, Q, 0, 4, 8, 8),       # null pointers
+    (P, Q, R, 0, 8, 8), (P, Q, R, -3, 8, 8),                          # M < 1
+    (P, Q, R, 4, 12, 8), (P, Q, R, 4, 8, 12), (P, Q, R, 4, 0, 8),     # N, K not multiples of 8
+    (P + 8, Q, R, 4, 8, 8), (P, Q + 2, R, 4, 8, 8), (P, Q, R + 4, 4, 8, 8),  # misaligned
+    (P, Q, P, 4, 8, 8),                                               # Y aliases A
+    (P, Q, R, 1 << 31, 8, 8),                                         # M too large
+])
+def test_forward_rejects_bad_arguments_on_host(lib, args):
+    A, Wp, Y, M, N, K = args
+    st = lib.swiglu_up_forward(A, Wp, Y, M, N, K, None, 0, None)
+    assert st == 1, "expected SWIGLU_ERR_INVALID_ARG"
+
+
+@pytest.mark.parametrize("args", [
+    (0, Q, R, 64, 64), (P, Q, 0, 64, 64), (P, Q, R, 60, 64), (P, Q, R, 64, 4),
+    (P + 2, Q, R, 64, 64), (P, Q, P, 64, 64),
+])
+def test_pack_rejects_bad_arguments_on_host(lib, args):
+    W1, W2, Wp, K, N = args
+    assert lib.swiglu_pack_weights(W1, W2, K, N, Wp, None) == 1
+
+
+def test_valid_call_without_gpu_reports_error_not_crash(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = lib.swiglu_up_forward(P, Q, R, 4, 8, 8, None, 0, None)
+    assert st in (2, 3)                       # UNSUPPORTED or CUDA: no device here
+
+
+def test_binding_fails_loudly_when_library_missing(tmp_path):
+    import gemm_swiglu_mlp_gb300 as sg
+    saved = sg._lib
+    sg._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="not built"):
+            sg.load_library(str(tmp_path / "missing.so"))
+    finally:
+        sg._lib = saved
+
+
+def test_pack_reference_layout_by_hand():
+    # K=2, N=3: packed has 2*128 rows; row r<3 is W1[:, r], row 128+r is W2[:, r]
+    W1 = np.arange(6, dtype=np.uint16).reshape(2, 3)
+    W2 = (100 + np.arange(6, dtype=np.uint16)).reshape(2, 3)
+    P_ = parity.pack_reference(W1, W2)
+    assert P_.shape == (256, 2)
+    assert P_[1].tolist() == [1, 4] and P_[129].tolist() == [101, 104]
+    assert not P_[3:128].any() and not P_[131:].any()
+
+
+def test_parity_criteria_by_hand():
+    import workloads
+    want = workloads.f32_to_bf16_bits(np.array([1.0, 0.0, 100.0, 1e-4], np.float32))
+    same = parity.compare(want, want)
+    assert same["mismatches"] == 0 and same["over_bound"] == 0 and same["bit_exact_frac"] == 1.0
+    # one BF16 ulp off at 100 (ulp 0.5) is within 2 ulps; 2% off is a mismatch
+    got = workloads.f32_to_bf16_bits(np.array([1.0, 0.0, 100.5, 1e-4], np.float32))
+    r = parity.compare(got, want)
+    assert r["mismatches"] == 0 and r["over_bound"] == 0
+    got = workloads.f32_to_bf16_bits(np.array([1.02, 0.0, 100.0, 1e-4], np.float32))
+    r = parity.compare(got, want)
+    assert r["mismatches"] == 1 and r["over_bound"] == 1
+    # near zero the relative test is floored: 5e-6 <= 0.01 * 1e-3 is not a mismatch,
+    # but it is one under the literal, unfloored reading
+    got = workloads.f32_to_bf16_bits(np.array([1.0, 5e-6, 100.0, 1e-4], np.float32))
+    r = parity.compare(got, want)
+    assert r["mismatches"] == 0 and r["over_bound"] == 0 and r["literal_rel_mismatches"] == 1

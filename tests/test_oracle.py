@@ -225,3 +225,13 @@ def test_workload_variants():
     a_o = workloads.bf16_bits_to_f32(workloads.make_A(o))
     big_cols = np.where(np.abs(a_o).max(axis=0) > 6.0)[0]
     assert 1 <= len(big_cols) <= 5               # round(0.01 * 500) = 5 outlier columns
+
+
+def test_column_range_matches_full(oracle_mod):
+    A, W1, W2 = workloads.random_case(9, 70, 33, 17)
+    full = oracle_mod.swiglu_up(A, W1, W2, want_gate_up=True)
+    part = oracle_mod.swiglu_up(A, W1, W2, rows=[8, 2], cols=(13, 51), want_gate_up=True)
+    assert np.array_equal(part["Y"], full["Y"][[8, 2], 13:51])
+    assert np.array_equal(part["G"], full["G"][[8, 2], 13:51])
+    with pytest.raises(RuntimeError):
+        oracle_mod.swiglu_up(A, W1, W2, cols=(10, 71))

@@ -72,22 +72,24 @@ BY_NAME = {w.name: w for w in WORKLOADS}
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """binary32 array -> BF16 bit patterns (uint16), round to nearest even.
 
-    Inputs here are finite normals, so NaN handling is not needed; it is kept
-    anyway (quiet NaN) so that the helper is total.
+    Adds 0x7FFF plus the lowest kept bit and truncates (the usual RNE trick;
+    finite inputs cannot overflow 32 bits this way). NaNs map to a quiet NaN.
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32)
+    u = x.view(np.uint32).reshape(-1)
     out = np.empty(u.shape, dtype=np.uint16)
     step = 1 << 24
-    flat_u = u.reshape(-1)
-    flat_o = out.reshape(-1)
-    for s in range(0, flat_u.size, step):
-        v = flat_u[s:s + step].astype(np.uint64)
-        r = (v + 0x7FFF + ((v >> 16) & 1)) >> 16
-        nan = (v & 0x7FFFFFFF) > 0x7F800000
-        r = np.where(nan, (v >> 16) | 0x40, r)
-        flat_o[s:s + step] = r.astype(np.uint16)
-    return out
+    for s in range(0, u.size, step):
+        v = u[s:s + step]
+        r = (v >> np.uint32(16)) & np.uint32(1)
+        r += np.uint32(0x7FFF)
+        r += v
+        r >>= np.uint32(16)
+        nan = (v & np.uint32(0x7FFFFFFF)) > np.uint32(0x7F800000)
+        if nan.any():
+            r[nan] = (v[nan] >> np.uint32(16)) | np.uint32(0x40)
+        out[s:s + step] = r
+    return out.reshape(x.shape)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:

@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused SwiGLU up-projection Y = SiLU(A x W1) (.) (A x W2).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload LABEL]
+
+One step = one call of swiglu_up_forward (the whole fused path: both GEMMs,
+the activation and the BF16 store) over one batch of M tokens. Default
+workload: the Qwen-2.5-1.5B-shaped up-projection, M=2048, K=1536, N=8960.
+Inputs are seeded synthetic data (workloads/), generated once and resident in
+HBM before the timed region. Consecutive steps rotate over several copies of
+A, the packed weights and Y whose total exceeds twice the L2 size, so no step
+finds its operands in L2.
+
+Prints one JSON line (rank 0). Under torchrun each rank runs the same
+workload on its own GPU (independent replicas, no collective on the data
+path); `value` is the FLOP total of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused SwiGLU up-proj TFLOP/s and % of GB300 BF16/HBM roofline vs M"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "1"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+REFERENCE_BUDGET_S = 120.0
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gemm_swiglu_mlp_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_label: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    only if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d.get("workloads", {}).get(workload_label)
+        if rec and d.get("kernel_source_hash") == kernel_source_hash():
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def roofline_us(w, peaks):
+    return max(w.flops / (peaks["bf16_tflops"] * 1e12), w.roofline_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
+
+
+def bound_of(w, peaks) -> str:
+    t_tc = w.flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = w.roofline_bytes / (peaks["hbm_gbs"] * 1e9)
+    return "tensor" if t_tc >= t_hbm else "hbm"
+
+
+class ClockSampler:
+    """Samples SM clock, power and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.samples = []
+        self.proc = None
+        self.t_timed = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                self.samples.append({
+                    "t": time.time(), "sm": float(parts[2]), "sm_max": float(parts[3]),
+                    "power": float(parts[4]), "hw": parts[6], "hw_thermal": parts[7],
+                    "sw_thermal": parts[8], "sw_power_cap": parts[9]})
+            except ValueError:
+                continue
+
+    def mark_timed(self, t0, t1):
+        self.t_timed = (t0, t1)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        window = "timed"
+        sel = [s for s in self.samples if self.t_timed and self.t_timed[0] <= s["t"] <= self.t_timed[1]]
+        if len(sel) < 3:
+            window = "warmup+timed"
+            sel = self.samples[1:] or self.samples
+        active = lambda v: v.lower() in ("active", "1", "yes")
+        reasons = set()
+        for s in sel:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power_cap", "sw_power_cap")):
+                if active(s[key]):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s["sm"] for s in sel),
+                "sm_max_mhz": max(s["sm_max"] for s in sel),
+                "power_w_median": statistics.median(s["power"] for s in sel),
+                "samples": len(sel), "window": window, "reasons": sorted(reasons)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a scalar over all ranks (identity for a single process)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world <= 1:
+        return
+    import torch
+    import torch.distributed as dist
+    t = torch.zeros(1, device=device)
+    dist.all_reduce(t)
+
+
+def aggregate_value(flops_per_step: float, steps: int, world: int, elapsed_max_s: float) -> float:
+    """Whole-job TFLOP/s: every rank's FLOPs over the slowest rank's time."""
+    return flops_per_step * steps * world / elapsed_max_s / 1e12
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+def oracle_sample_rate(w, A, W1, W2, rows: int, cols: int, threads: int = 0):
+    """Times the oracle on `rows` rows x `cols` columns; returns (seconds, flops)."""
+    import numpy as np
+
+    import oracle
+    rng = np.random.Generator(np.random.PCG64(77))
+    r = np.sort(rng.choice(w.M, size=min(rows, w.M), replace=False))
+    t0 = time.perf_counter()
+    oracle.swiglu_up(A, W1, W2, rows=r, cols=(0, cols), nthreads=threads)
+    dt = time.perf_counter() - t0
+    return dt, 4.0 * len(r) * cols * w.K
+
+
+def cpu_baseline(w, A, W1, W2, target_s: float = 12.0):
+    """The oracle as it stands, on every host core, on a bounded row sample."""
+    cores = len(os.sched_getaffinity(0))
+    dt, fl = oracle_sample_rate(w, A, W1, W2, rows=cores, cols=w.N)
+    rows_per_s = cores / dt
+    rows = int(min(w.M, max(cores, (target_s - dt) * rows_per_s)))
+    rows = max(cores, rows // cores * cores)
+    dt2, fl2 = oracle_sample_rate(w, A, W1, W2, rows=rows, cols=w.N)
+    return {"value": fl2 / dt2 / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d of %d rows x all %d columns (K=%d), %.1f s" % (rows, w.M, w.N, w.K, dt2)}
+
+
+def run_reference(args, w):
+    """Reference arm: the CPU oracle timed on this host's cores, one bounded
+    sample of the workload per step."""
+    import numpy as np
+
+    import workloads
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    A, W1, W2 = workloads.make_inputs(w)
+    cores = len(os.sched_getaffinity(0))
+    rows = min(cores, w.M)
+    # size the per-step column block so that warmup + steps fit the budget
+    dt, _ = oracle_sample_rate(w, A, W1, W2, rows=rows, cols=min(w.N, 256))
+    per_col = dt / min(w.N, 256)
+    budget = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)
+    cols = int(max(8, min(w.N, budget / max(per_col, 1e-9))) // 8 * 8)
+    for _ in range(args.warmup):
+        oracle_sample_rate(w, A, W1, W2, rows=rows, cols=cols)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        _, fl = oracle_sample_rate(w, A, W1, W2, rows=rows, cols=cols)
+        flops += fl
+    el = time.perf_counter() - t0
+    value = flops / el / 1e12
+    sample = "%d rows x %d columns (K=%d) of the %dx%d output per step" % (rows, cols, w.K, w.M, w.N)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / max(1, args.steps) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, None),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, l2_note):
+    c = {"workload": "%s: M=%d tokens, K=%d, N=%d, A~N(0,1), W1/W2~N(0,1/K), BF16 in/out, FP32 accumulate"
+                     % (w.name, w.M, w.K, w.N),
+         "M": w.M, "K": w.K, "N": w.N, "parallelism": "replicas"}
+    if l2_note:
+        c["l2"] = l2_note
+    return c
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gb300(args, w):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from gemm_swiglu_mlp_gb300 import build as lib_build
+    lib_build.build()
+    import gemm_swiglu_mlp_gb300 as sg
+    import workloads
+    from tests.parity import to_device_bf16
+
+    peaks, peaks_src = load_peaks()
+    A, W1, W2 = workloads.make_inputs(w)
+    A_d = to_device_bf16(A, dev)
+    Wp = sg.swiglu_pack_weights(to_device_bf16(W1, dev), to_device_bf16(W2, dev))
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_set = w.M * w.K * 2 + Wp.numel() + w.M * w.N * 2
+    R = max(2, -(-2 * l2 // per_set))
+    As = [A_d] + [A_d.clone() for _ in range(R - 1)]
+    Wps = [Wp] + [Wp.clone() for _ in range(R - 1)]
+    Ys = [torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    ws = sg.swiglu_workspace_bytes(w.M, w.N, w.K)
+    Wss = [torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev) if ws else None for _ in range(R)]
+    l2_note = "rotating %d input sets (%.0f MB total, > 2x the %.0f MB L2)" % (
+        R, R * per_set / 1e6, l2 / 1e6)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        j = i % R
+        sg.swiglu_up_forward(As[j], Wps[j], w.N, Y=Ys[j], workspace=Wss[j], stream=stream)
+
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    sg.swiglu_check_device_status(stream)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    t_begin.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    barrier(world, dev)
+    sampler.mark_timed(wall0, wall1)
+    elapsed = t_begin.elapsed_time(t_end) * 1e-3
+    launch_s = [a.elapsed_time(b) * 1e-3 for a, b in ev]
+    sg.swiglu_check_device_status(stream)
+    elapsed_max = max_over_ranks(elapsed, world, dev)
+    value = aggregate_value(w.flops, K, world, elapsed_max)
+    avg_launch = sum(launch_s) / len(launch_s)
+
+    # ---- end to end through the public API: pinned host A in, Y back out, every step
+    Ke = min(K, 2000)
+    A_h = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Y_h = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step(i):
+        j = i % R
+        As[j].copy_(A_h, non_blocking=True)
+        sg.swiglu_up_forward(As[j], Wps[j], w.N, Y=Ys[j], workspace=Wss[j], stream=stream)
+        Y_h.copy_(Ys[j], non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(Ke):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    sampler.stop()
+    e_el = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world, dev)
+    e2e_value = aggregate_value(w.flops, Ke, world, e_el)
+    sg.swiglu_check_device_status(stream)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    bound = bound_of(w, peaks)
+    if bound == "tensor":
+        achieved = w.flops / avg_launch / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": "%s burst bf16" % peaks_src,
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
+    else:
+        achieved = w.roofline_bytes / avg_launch / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": "%s copy bandwidth" % peaks_src}
+    roof["traffic"] = recorded_traffic(w.c)
+    roof["algorithmic_per_launch"] = w.flops if bound == "tensor" else w.roofline_bytes
+    roof["avg_launch_us"] = avg_launch * 1e6
+    roof["frac_of_roofline_time"] = roofline_us(w, peaks) * 1e-6 / avg_launch
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": elapsed_max / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, l2_note), "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": w.M * w.K * 2,
+                "d2h_bytes_per_step": w.M * w.N * 2, "steps": Ke},
+        "gpu_launches": K, "clocks": sampler.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, A, W1, W2)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=500)
+    p.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                   help="workload label (workloads.WORKLOADS), default 1 = Qwen-2.5-1.5B M=2048")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    import workloads
+    w = workloads.BY_LABEL[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gb300(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,189 @@
+"""Python binding of the GB300 fused SwiGLU up-projection C ABI (include/swiglu.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libswiglu_gb300.so. PyTorch supplies device memory and the current
+stream; there is no CPU or PyTorch fallback, and the functions raise if the
+library has not been built (``python -m gemm_swiglu_mlp_gb300.build``).
+
+The names follow the C ABI:
+
+    swiglu_packed_weight_bytes(N, K) -> int
+    swiglu_pack_weights(W1, W2, Wpacked=None) -> Wpacked (uint8 tensor)
+    swiglu_workspace_bytes(M, N, K) -> int
+    swiglu_up_forward(A, Wpacked, N, Y=None, workspace=None) -> Y
+    swiglu_check_device_status() -> raw status word (raises on timeout)
+    swiglu_status_string(status) -> str
+
+Y = SiLU(A x W1) (.) (A x W2) ("Tile-Level Activation Overlap for Efficient
+LLM Inference", Section 1 Introduction), BF16 in and out, FP32 accumulation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH
+
+__all__ = [
+    "SwigluError", "load_library", "swiglu_version", "swiglu_status_string",
+    "swiglu_packed_weight_bytes", "swiglu_pack_weights", "swiglu_workspace_bytes",
+    "swiglu_up_forward", "swiglu_check_device_status", "EXPORTED_SYMBOLS",
+]
+
+SWIGLU_OK = 0
+SWIGLU_ERR_INVALID_ARG = 1
+SWIGLU_ERR_UNSUPPORTED = 2
+SWIGLU_ERR_CUDA = 3
+SWIGLU_ERR_DEVICE_TIMEOUT = 4
+
+EXPORTED_SYMBOLS = (
+    "swiglu_version", "swiglu_status_string", "swiglu_packed_weight_bytes",
+    "swiglu_pack_weights", "swiglu_workspace_bytes", "swiglu_up_forward",
+    "swiglu_check_device_status",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SwigluError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s" % (what, _status_name(status)))
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libswiglu_gb300.so (no fallback: raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                "libswiglu_gb300.so is not built (%s); run "
+                "`python -m gemm_swiglu_mlp_gb300.build`" % path)
+        lib = ctypes.CDLL(path)
+        vp, i64, sz, u32p = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.POINTER(ctypes.c_uint32)
+        lib.swiglu_version.argtypes = []
+        lib.swiglu_version.restype = ctypes.c_int
+        lib.swiglu_status_string.argtypes = [ctypes.c_int]
+        lib.swiglu_status_string.restype = ctypes.c_char_p
+        lib.swiglu_packed_weight_bytes.argtypes = [i64, i64]
+        lib.swiglu_packed_weight_bytes.restype = sz
+        lib.swiglu_pack_weights.argtypes = [vp, vp, i64, i64, vp, vp]
+        lib.swiglu_pack_weights.restype = ctypes.c_int
+        lib.swiglu_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.swiglu_workspace_bytes.restype = sz
+        lib.swiglu_up_forward.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+        lib.swiglu_up_forward.restype = ctypes.c_int
+        lib.swiglu_check_device_status.argtypes = [vp, u32p]
+        lib.swiglu_check_device_status.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return load_library().swiglu_status_string(int(status)).decode()
+    except Exception:  # library missing: still give a readable message
+        return "status %d" % status
+
+
+def _check(status: int, what: str):
+    if status != SWIGLU_OK:
+        raise SwigluError(status, what)
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _require_bf16_cuda(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != torch.bfloat16:
+        raise TypeError("%s must be bfloat16, got %s" % (name, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def swiglu_version() -> int:
+    return load_library().swiglu_version()
+
+
+def swiglu_status_string(status: int) -> str:
+    return load_library().swiglu_status_string(int(status)).decode()
+
+
+def swiglu_packed_weight_bytes(N: int, K: int) -> int:
+    return int(load_library().swiglu_packed_weight_bytes(int(N), int(K)))
+
+
+def swiglu_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().swiglu_workspace_bytes(int(M), int(N), int(K)))
+
+
+def swiglu_pack_weights(W1: torch.Tensor, W2: torch.Tensor, Wpacked: torch.Tensor = None,
+                        stream=None) -> torch.Tensor:
+    """Pack W1, W2 ([K, N] BF16 each) into the library's fused weight operand."""
+    lib = load_library()
+    _require_bf16_cuda(W1, "W1")
+    _require_bf16_cuda(W2, "W2")
+    if W1.dim() != 2 or W1.shape != W2.shape:
+        raise ValueError("W1 and W2 must both be [K, N]")
+    K, N = W1.shape
+    nbytes = swiglu_packed_weight_bytes(N, K)
+    if Wpacked is None:
+        Wpacked = torch.empty(nbytes, dtype=torch.uint8, device=W1.device)
+    elif Wpacked.numel() * Wpacked.element_size() < nbytes or not Wpacked.is_contiguous():
+        raise ValueError("Wpacked must be contiguous with at least %d bytes" % nbytes)
+    with torch.cuda.device(W1.device):
+        _check(lib.swiglu_pack_weights(W1.data_ptr(), W2.data_ptr(), K, N, Wpacked.data_ptr(),
+                                       _stream_handle(stream)), "swiglu_pack_weights")
+    return Wpacked
+
+
+def swiglu_up_forward(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: torch.Tensor = None,
+                      workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Y[M, N] = SiLU(A x W1) (.) (A x W2) from A [M, K] BF16 and packed weights."""
+    lib = load_library()
+    _require_bf16_cuda(A, "A")
+    if A.dim() != 2:
+        raise ValueError("A must be [M, K]")
+    M, K = A.shape
+    N = int(N)
+    need = swiglu_packed_weight_bytes(N, K)
+    if not Wpacked.is_cuda or Wpacked.numel() * Wpacked.element_size() < need:
+        raise ValueError("Wpacked must be a CUDA buffer of at least %d bytes" % need)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _require_bf16_cuda(Y, "Y")
+        if tuple(Y.shape) != (M, N):
+            raise ValueError("Y must be [%d, %d]" % (M, N))
+    ws_need = swiglu_workspace_bytes(M, N, K)
+    ws_ptr, ws_bytes = None, 0
+    if ws_need:
+        if workspace is None:
+            workspace = torch.zeros(ws_need, dtype=torch.uint8, device=A.device)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    with torch.cuda.device(A.device):
+        _check(lib.swiglu_up_forward(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(), M, N, K,
+                                     ws_ptr, ws_bytes, _stream_handle(stream)),
+               "swiglu_up_forward")
+    return Y
+
+
+def swiglu_check_device_status(stream=None) -> int:
+    """Synchronize the stream and read/clear the device status word."""
+    lib = load_library()
+    raw = ctypes.c_uint32(0)
+    st = lib.swiglu_check_device_status(_stream_handle(stream), ctypes.byref(raw))
+    if st == SWIGLU_ERR_DEVICE_TIMEOUT:
+        raise SwigluError(st, "device status word 0x%x" % raw.value)
+    _check(st, "swiglu_check_device_status")
+    return raw.value

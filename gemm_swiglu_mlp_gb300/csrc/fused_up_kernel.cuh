@@ -1,0 +1,347 @@
+// Fused SwiGLU up-projection kernel for sm_103a (tcgen05 / TMEM / TMA).
+//
+// Computes Y = SiLU(A x W1) (.) (A x W2) ("Tile-Level Activation Overlap for
+// Efficient LLM Inference", Section 1 Introduction) without writing Gate or
+// Up to global memory (same paper, Abstract). Design, per persistent CTA:
+//
+//   warp 0        TMA producer: for each k-block loads one A tile [128 x 64]
+//                 and one packed weight tile [256 x 64] (128 Gate rows then
+//                 128 Up rows of the same output columns) into a STAGES-deep
+//                 shared-memory ring. Each A tile feeds both products.
+//   warp 1        MMA issuer: one tcgen05.mma (M=128, N=256, K=16) per K
+//                 step puts Gate in TMEM columns [0,128) and Up in [128,256)
+//                 of one accumulator stage; two stages (512 columns) let the
+//                 next tile's MMAs run while the epilogue drains this one.
+//   warps 2..5    epilogue: tcgen05.ld Gate and Up for 32 rows each,
+//                 y = SiLU(g) * u in FP32, round to BF16, stage in 128-byte
+//                 swizzled shared memory, TMA store (clipped at M and N).
+//
+// This replaces the pages' two SM90 designs (technical summary, "Kernel-1"
+// and "Kernel-2"): the packed operand plays the role of Kernel-2's fused
+// weight matrix (one GEMM feeds both accumulators from one A tile), the
+// paired accumulators sit in TMEM instead of registers, and the activation
+// overlaps the next tile's MMA (Kernel-2's compute/store overlap) rather
+// than the Up-tile load (Kernel-1).
+//
+// Every wait is bounded (sm103_ptx.cuh). A role that gives up sets a bit in
+// the device status word and the shared abort flag; the others leave their
+// loops, in-flight TMA loads and MMAs are drained with bounded waits, and
+// TMEM is released before the CTA exits.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "sm103_ptx.cuh"
+
+namespace swiglu {
+
+// Device status word, read and cleared by swiglu_check_device_status. The
+// library is one translation unit (no relocatable device code), so the
+// definition lives here.
+__device__ unsigned int g_status_word = 0;
+
+enum : unsigned int {
+    kStatusProducerTimeout = 1u,
+    kStatusMmaTimeout = 2u,
+    kStatusEpilogueTimeout = 4u,
+    kStatusDrainTimeout = 8u,
+};
+
+// Persistent tile order: tiles are visited in groups of `group_m` row-tiles;
+// inside a group the row-tile index runs fastest, so the CTAs working at the
+// same time share a few weight blocks and a bounded slab of A in L2.
+struct TileOrder {
+    int m_tiles;
+    int n_tiles;
+    int group_m;
+    __device__ __forceinline__ void coords(int t, int &mb, int &nb) const {
+        const int per_group = group_m * n_tiles;
+        const int g = t / per_group;
+        const int first_m = g * group_m;
+        const int gm = min(group_m, m_tiles - first_m);
+        const int idx = t - g * per_group;
+        nb = idx / gm;
+        mb = first_m + idx % gm;
+    }
+};
+
+struct FusedArgs {
+    int M, N, K;
+    int k_blocks;
+    int num_tiles;
+    TileOrder order;
+};
+
+template <int STAGES>
+struct FusedCfg {
+    static constexpr int BM = 128;                // token rows per tile = UMMA M
+    static constexpr int BN = 128;                // output columns per tile
+    static constexpr int BK = 64;                 // K per stage: 128-byte rows
+    static constexpr int UMMA_N = 2 * BN;         // Gate | Up
+    static constexpr int UMMA_K = 16;
+    static constexpr int A_BYTES = BM * BK * 2;   // 16 KB
+    static constexpr int B_BYTES = UMMA_N * BK * 2;  // 32 KB
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int Y_HALF_BYTES = 32 * 64 * 2;      // 32 rows x 64 cols, 4 KB
+    static constexpr int Y_WARP_BYTES = 2 * Y_HALF_BYTES;  // 32 rows x 128 cols
+    static constexpr int TMEM_COLS = 2 * UMMA_N;          // two accumulator stages
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_Y = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_BAR = OFF_Y + EPI_WARPS * Y_WARP_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull x2, tempty x2, drain
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + 1 KB alignment slack
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static_assert(TMEM_COLS == 512, "two 256-column accumulator stages fill TMEM");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ float silu_mul(uint32_t gbits, uint32_t ubits) {
+    const float g = __uint_as_float(gbits);
+    const float u = __uint_as_float(ubits);
+    // SiLU(g) = g / (1 + e^-g); for g << 0 the denominator is +inf and the
+    // quotient 0, the limit.
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Bounded wait that ignores the abort flag (used while draining).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const int never = 0;
+    return mbar_wait(bar, parity, &never);
+}
+
+template <int STAGES>
+__global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
+    fused_up_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmY, const FusedArgs args) {
+    using C = FusedCfg<STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const uint32_t sbase = smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    auto full_bar = [&](int s) { return sbase + C::OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sbase + C::OFF_BAR + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return sbase + C::OFF_BAR + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return sbase + C::OFF_BAR + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t drain_bar = sbase + C::OFF_BAR + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), C::EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmY);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    // Producer bookkeeping kept for the drain after an abort: which stages
+    // received a load, and the parity of the phase of the last one.
+    uint32_t issued_mask = 0, last_parity = 0;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+                int mb, nb;
+                args.order.coords(t, mb, nb);
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
+                    tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
+                                kb * C::BK, mb * C::BM);
+                    tma_load_2d(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, full_bar(stage),
+                                kb * C::BK, nb * C::UMMA_N);
+                    issued_mask |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok && !*abort_flag) {
+                atomicOr(&g_status_word, kStatusProducerTimeout);
+                *abort_flag = 1;
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(C::BM, C::UMMA_N);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::UMMA_N);
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a_desc = smem_desc_k128(sbase + C::OFF_A + stage * C::A_BYTES);
+                    const uint64_t b_desc = smem_desc_k128(sbase + C::OFF_B + stage * C::B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < C::BK / C::UMMA_K; ++k) {
+                        // +32 bytes along K per step inside the 128-byte swizzle row
+                        umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
+                                  (kb | k) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull_bar(acc));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (!ok && !*abort_flag) {
+                atomicOr(&g_status_word, kStatusMmaTimeout);
+                *abort_flag = 1;
+            }
+        }
+    } else {
+        // Epilogue warps 2..5. tcgen05.ld lets warp w touch TMEM lanes
+        // [32*(w%4), 32*(w%4)+32): those are the tile rows it owns.
+        const int quad = warp & 3;
+        const uint32_t ybuf = sbase + C::OFF_Y + (warp - 2) * C::Y_WARP_BYTES;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+            int mb, nb;
+            args.order.coords(t, mb, nb);
+            ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            const int row0 = mb * C::BM + 32 * quad;
+            const bool rows_live = row0 < args.M;
+            if (rows_live) {
+                if (lane == 0) bulk_wait_group_read0();  // last store has read ybuf
+                __syncwarp();
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) +
+                                       static_cast<uint32_t>(acc * C::UMMA_N);
+#pragma unroll 1
+                for (int c = 0; c < C::BN; c += 32) {
+                    uint32_t g[32], u[32];
+                    tmem_ld_32x32b_x32(tbase + c, g);
+                    tmem_ld_32x32b_x32(tbase + C::BN + c, u);
+                    tmem_ld_wait();
+                    reg_fence32(g);
+                    reg_fence32(u);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 8 * j + 2 * e;
+                            w[e] = pack_bf16x2(silu_mul(g[i], u[i]), silu_mul(g[i + 1], u[i + 1]));
+                        }
+                        // 128-byte swizzle: 16-byte chunk index XOR (row % 8)
+                        const int col = c + 8 * j;
+                        const int half = col >> 6;
+                        const int chunk = (col & 63) >> 3;
+                        const uint32_t addr = ybuf + half * C::Y_HALF_BYTES + lane * 128 +
+                                              (static_cast<uint32_t>(chunk ^ (lane & 7)) << 4);
+                        st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (rows_live) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int x0 = nb * C::BN;
+                    tma_store_2d(&tmY, ybuf, x0, row0);
+                    if (x0 + 64 < args.N) tma_store_2d(&tmY, ybuf + C::Y_HALF_BYTES, x0 + 64, row0);
+                    bulk_commit_group();
+                }
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (lane == 0) {
+            bulk_wait_group0();
+            if (!ok && !*abort_flag) {
+                atomicOr(&g_status_word, kStatusEpilogueTimeout);
+                *abort_flag = 1;
+            }
+        }
+    }
+
+    // ---- teardown: every role has left its loop.
+    __syncthreads();
+    if (*abort_flag) {
+        if (warp == 0 && lane == 0) {
+            // let every TMA load already issued land before shared memory goes
+            for (int s = 0; s < STAGES; ++s)
+                if ((issued_mask >> s) & 1u)
+                    if (!mbar_wait_drain(full_bar(s), (last_parity >> s) & 1u))
+                        atomicOr(&g_status_word, kStatusDrainTimeout);
+        }
+        if (warp == 1 && lane == 0) {
+            // all MMAs issued by this thread complete before TMEM is freed
+            umma_commit(drain_bar);
+            if (!mbar_wait_drain(drain_bar, 0)) atomicOr(&g_status_word, kStatusDrainTimeout);
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace swiglu

@@ -1,0 +1,120 @@
+/*
+ * swiglu.h - C ABI of the GB300 (sm_103a) fused SwiGLU up-projection library.
+ *
+ * The library computes the gated-MLP up-projection with its activation,
+ *
+ *     Y[m,n] = SiLU(Gate[m,n]) * Up[m,n],  Gate = A x W1,  Up = A x W2,
+ *     SiLU(x) = x / (1 + e^-x),
+ *
+ * ("Tile-Level Activation Overlap for Efficient LLM Inference", Section 1
+ * Introduction, the gated-MLP definition) in one kernel per call: Gate and
+ * Up are accumulated in FP32 in tensor memory and never written to global
+ * memory (same paper, Abstract: the activation is fused into the GEMM at tile
+ * level). Inputs and output are BF16; accumulation is FP32; the FP32 result
+ * SiLU(g)*u is rounded once to BF16 (round to nearest even).
+ *
+ * Conventions for every entry point
+ *   - Pointers marked "device" are CUDA device pointers on the current device
+ *     (cudaSetDevice / torch's current device). The caller allocates and owns
+ *     every buffer; the library keeps no per-call allocation. It caches, per
+ *     device and for the life of the process, a few host-side values (SM
+ *     count, kernel attributes) and one 4-byte device status word.
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream. Every call is asynchronous on `stream` and never synchronizes,
+ *     except swiglu_check_device_status.
+ *   - Return value: a swiglu_status. Arguments are validated on the host
+ *     before anything is launched; a rejected call launches nothing. No C++
+ *     exception crosses this boundary.
+ *   - BF16 arrays are passed as raw 16-bit patterns (uint16_t storage).
+ */
+#ifndef SWIGLU_GB300_H
+#define SWIGLU_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SWIGLU_OK = 0,
+    SWIGLU_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad size */
+    SWIGLU_ERR_UNSUPPORTED = 2,     /* valid but not supported (no sm_103a device, sizes over limits) */
+    SWIGLU_ERR_CUDA = 3,            /* a CUDA runtime/driver call or a launch failed */
+    SWIGLU_ERR_DEVICE_TIMEOUT = 4   /* a kernel gave up on a bounded wait (see check_device_status) */
+} swiglu_status;
+
+/* Library ABI version, (major << 16) | minor. */
+int swiglu_version(void);
+
+/* Human-readable name of a swiglu_status value (static string, never NULL). */
+const char *swiglu_status_string(int status);
+
+/*
+ * Size in bytes of the packed weight operand for an N x K pair (W1, W2).
+ *
+ * Packed layout (this library's own; the pages' Kernel-2 interleaves W1 and
+ * W2 column by column into one K x 2N operand, technical summary
+ * "Kernel-2", and this is the same idea in the blocked, K-major form the
+ * tensor cores consume): a row-major [2*Np, K] BF16 matrix, Np = N rounded up
+ * to a multiple of 128. Rows come in blocks of 256: rows 256j..256j+127 hold
+ * W1[:, 128j..128j+127] transposed (Gate), rows 256j+128..256j+255 hold
+ * W2[:, 128j..128j+127] transposed (Up). Rows for columns n >= N are zero.
+ * Returns 0 if N <= 0 or K <= 0.
+ */
+size_t swiglu_packed_weight_bytes(int64_t N, int64_t K);
+
+/*
+ * Packs W1 and W2 (device, BF16, [K, N] row-major each) into Wpacked
+ * (device, swiglu_packed_weight_bytes(N, K) bytes, layout above). A pure
+ * permutation plus zero padding: bit-exact. One-time per weight set; runs as
+ * one kernel on `stream`.
+ * Requirements: K > 0, N > 0, N % 8 == 0, K % 8 == 0; all pointers non-null
+ * and 16-byte aligned; Wpacked must not overlap W1 or W2.
+ * Errors: SWIGLU_ERR_INVALID_ARG (arguments), SWIGLU_ERR_CUDA (launch).
+ */
+int swiglu_pack_weights(const void *W1, const void *W2, int64_t K, int64_t N,
+                        void *Wpacked, void *stream);
+
+/*
+ * Bytes of device workspace that swiglu_up_forward needs for (M, N, K).
+ * 0 means none: pass workspace = NULL, workspace_bytes = 0.
+ */
+size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Y = SiLU(A x W1) (.) (A x W2) in one fused kernel.
+ *   A        device, BF16, [M, K] row-major (row stride K elements)
+ *   Wpacked  device, output of swiglu_pack_weights for this (N, K)
+ *   Y        device, BF16, [M, N] row-major; fully overwritten
+ *   workspace, workspace_bytes: device scratch of at least
+ *            swiglu_workspace_bytes(M, N, K) bytes (may be NULL when that is 0)
+ * Requirements: M >= 1, N >= 8, K >= 8, N % 8 == 0, K % 8 == 0 (16-byte row
+ * strides), M, N, K < 2^31; A, Wpacked, Y 16-byte aligned; Y must not overlap
+ * A, Wpacked or the workspace. M, N and K need not be multiples of any tile
+ * size. The schedule (tile shape, CTA count) is chosen from M, N, K and the
+ * device's SM count; the result is bit-identical from run to run.
+ * Errors: SWIGLU_ERR_INVALID_ARG, SWIGLU_ERR_UNSUPPORTED (device is not
+ * sm_103 / sm_100-family with tcgen05), SWIGLU_ERR_CUDA (tensor-map encode
+ * or launch failure). Device-side timeouts are reported later by
+ * swiglu_check_device_status.
+ */
+int swiglu_up_forward(const void *A, const void *Wpacked, void *Y,
+                      int64_t M, int64_t N, int64_t K,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the current device's status
+ * word. Every wait inside the kernels is bounded (about a second); a kernel
+ * that gives up sets a bit in the word, releases its tensor memory and
+ * exits instead of hanging. Returns SWIGLU_OK, SWIGLU_ERR_DEVICE_TIMEOUT
+ * (and writes the raw word to *raw_word if non-NULL), or SWIGLU_ERR_CUDA.
+ */
+int swiglu_check_device_status(void *stream, uint32_t *raw_word);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIGLU_GB300_H */

@@ -1,0 +1,140 @@
+// Work schedule of one fused launch over a persistent grid (host + device).
+//
+// Tiles are 128 token rows x 128 output columns (one UMMA N=256 covers their
+// Gate and Up columns). With T tiles, kb k-blocks per tile and G persistent
+// CTAs:
+//   * data-parallel part: tiles [0, dp_tiles) run whole, round robin; dp_tiles
+//     is a multiple of G, so every CTA gets the same number of them;
+//   * stream-K part: the k-block iterations of tiles [dp_tiles, T) form one
+//     space of sk_iters = (T - dp_tiles) * kb iterations, cut into G
+//     contiguous ranges whose lengths differ by at most one. A tile whose
+//     iterations span several CTAs' ranges is summed through a workspace
+//     (fused_up_kernel.cuh, split epilogue).
+// The stream-K part absorbs the last partial wave of tiles (and, for decode
+// shapes with fewer tiles than SMs, all of them), so every CTA does the same
+// amount of MMA work up to one k-block.
+#pragma once
+
+#include <cstdint>
+
+namespace swiglu {
+
+// Persistent tile order: tiles are visited in groups of `group_m` row-tiles;
+// inside a group the row-tile index runs fastest, so the CTAs working at the
+// same time share a few weight blocks and a bounded slab of A in L2.
+struct TileOrder {
+    int m_tiles;
+    int n_tiles;
+    int group_m;
+    __host__ __device__ __forceinline__ void coords(int t, int &mb, int &nb) const {
+        const int per_group = group_m * n_tiles;
+        const int g = t / per_group;
+        const int first_m = g * group_m;
+        const int gm = (group_m < m_tiles - first_m) ? group_m : (m_tiles - first_m);
+        const int idx = t - g * per_group;
+        nb = idx / gm;
+        mb = first_m + idx % gm;
+    }
+};
+
+struct WorkSched {
+    int num_tiles;
+    int k_blocks;
+    int grid;
+    int dp_tiles;        // multiple of grid
+    long long sk_iters;  // (num_tiles - dp_tiles) * k_blocks; >= grid when > 0
+    TileOrder order;
+
+    // first stream-K iteration of CTA c (c = grid gives sk_iters)
+    __host__ __device__ __forceinline__ long long sk_begin(int c) const {
+        return sk_iters * c / grid;
+    }
+    // the CTA whose stream-K range holds iteration x
+    __host__ __device__ __forceinline__ int sk_owner(long long x) const {
+        return static_cast<int>(((x + 1) * grid - 1) / sk_iters);
+    }
+    // workspace slot (0: first stream-K tile of the CTA, 1: its last) that
+    // CTA c uses for stream-K tile s
+    __host__ __device__ __forceinline__ int sk_slot(int c, long long s) const {
+        return (sk_begin(c) / k_blocks == s) ? 0 : 1;
+    }
+};
+
+struct Unit {
+    int tile;  // linear tile index in TileOrder
+    int kb0;   // k-block range [kb0, kb1)
+    int kb1;
+    int sk;    // stream-K tile index (tile - dp_tiles), or -1 for a data-parallel tile
+};
+
+// A CTA's units in execution order: its data-parallel tiles, then the pieces
+// of its stream-K range (one unit per tile it touches).
+struct UnitIter {
+    int k_blocks, grid, dp_tiles;
+    int dp_next;
+    long long x, x_end;
+
+    __host__ __device__ __forceinline__ void init(const WorkSched &s, int cta) {
+        k_blocks = s.k_blocks;
+        grid = s.grid;
+        dp_tiles = s.dp_tiles;
+        dp_next = cta;
+        x = s.sk_begin(cta);
+        x_end = s.sk_begin(cta + 1);
+    }
+    __host__ __device__ __forceinline__ bool next(Unit &u) {
+        if (dp_next < dp_tiles) {
+            u.tile = dp_next;
+            u.kb0 = 0;
+            u.kb1 = k_blocks;
+            u.sk = -1;
+            dp_next += grid;
+            return true;
+        }
+        if (x >= x_end) return false;
+        const long long st = x / k_blocks;
+        const int k0 = static_cast<int>(x - st * k_blocks);
+        const long long left = x_end - x;
+        const int k1 = (k0 + left < k_blocks) ? static_cast<int>(k0 + left) : k_blocks;
+        u.tile = dp_tiles + static_cast<int>(st);
+        u.kb0 = k0;
+        u.kb1 = k1;
+        u.sk = static_cast<int>(st);
+        x += k1 - k0;
+        return true;
+    }
+};
+
+// Host-side choice of grid and split. `min_sk_iters` keeps every CTA's
+// stream-K share at a few k-blocks so tiles are not cut into slivers.
+inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_count,
+                               int group_m, int min_sk_iters = 4) {
+    WorkSched s{};
+    s.num_tiles = m_tiles * n_tiles;
+    s.k_blocks = k_blocks;
+    s.order.m_tiles = m_tiles;
+    s.order.n_tiles = n_tiles;
+    s.order.group_m = group_m < m_tiles ? group_m : m_tiles;
+    const long long total = static_cast<long long>(s.num_tiles) * k_blocks;
+    long long g = sm_count;
+    if (s.num_tiles % sm_count == 0) {
+        // whole waves: plain data-parallel, no workspace
+        s.grid = sm_count;
+        s.dp_tiles = s.num_tiles;
+        s.sk_iters = 0;
+        return s;
+    }
+    const long long max_grid = total / (min_sk_iters > 0 ? min_sk_iters : 1);
+    if (g > max_grid) g = max_grid > 0 ? max_grid : 1;
+    s.grid = static_cast<int>(g);
+    const int full_waves = s.num_tiles / s.grid;
+    // keep one full wave plus the remainder in the stream-K part
+    s.dp_tiles = (full_waves >= 2 ? full_waves - 1 : 0) * s.grid;
+    s.sk_iters = static_cast<long long>(s.num_tiles - s.dp_tiles) * k_blocks;
+    if (s.sk_iters < s.grid) {  // tiny problem: one iteration per CTA at most
+        s.grid = static_cast<int>(s.sk_iters);
+    }
+    return s;
+}
+
+}  // namespace swiglu

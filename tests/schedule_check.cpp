@@ -1,0 +1,100 @@
+// Host-side check of the fused kernel's work schedule (schedule.cuh), compiled
+// with g++ by tests/test_schedule.py. For each (m_tiles, n_tiles, k_blocks,
+// sm_count) given on stdin it verifies that:
+//   * the units of all CTAs cover every (tile, k-block) exactly once;
+//   * data-parallel tiles are whole and evenly spread (same count per CTA);
+//   * for every stream-K tile, the contributor range [sk_owner(first),
+//     sk_owner(last)] is exactly the set of CTAs that produced units for it,
+//     each contributor has one unit for it, and units arrive in k order;
+//   * workspace slots (2*c + sk_slot) of split tiles never collide;
+//   * per-CTA MMA work differs by at most max(1 k-block, 1 whole tile split);
+// and prints one summary line per case. Exit code 1 on any violation.
+#define __host__
+#define __device__
+#define __forceinline__ inline
+#include <cstdio>
+#include <cstdlib>
+#include <map>
+#include <set>
+#include <vector>
+
+#include "../gemm_swiglu_mlp_gb300/csrc/schedule.cuh"
+
+using namespace swiglu;
+
+static int fail(const char *what, int a, int b) {
+    std::printf("FAIL %s (%d, %d)\n", what, a, b);
+    return 1;
+}
+
+int main() {
+    int mt, nt, kb, sms, min_iters;
+    int bad = 0;
+    while (std::scanf("%d %d %d %d %d", &mt, &nt, &kb, &sms, &min_iters) == 5) {
+        const WorkSched s = plan_schedule(mt, nt, kb, sms, 16, min_iters);
+        const int T = mt * nt;
+        if (s.grid < 1 || s.grid > sms) { bad |= fail("grid", s.grid, sms); continue; }
+        if (s.dp_tiles % s.grid != 0) { bad |= fail("dp multiple", s.dp_tiles, s.grid); continue; }
+        if (s.sk_iters != (long long)(T - s.dp_tiles) * kb) { bad |= fail("sk_iters", T, s.dp_tiles); continue; }
+        if (s.sk_iters > 0 && s.sk_iters < s.grid) { bad |= fail("sk < grid", (int)s.sk_iters, s.grid); continue; }
+        std::vector<int> cover((size_t)T * kb, 0);
+        std::map<int, std::vector<std::pair<int, int>>> contrib;  // sk tile -> (cta, kb0)
+        std::vector<long long> work(s.grid, 0);
+        std::set<long long> coords_seen;
+        for (int c = 0; c < s.grid; ++c) {
+            UnitIter it;
+            it.init(s, c);
+            Unit u;
+            int n_dp = 0;
+            while (it.next(u)) {
+                if (u.tile < 0 || u.tile >= T || u.kb0 < 0 || u.kb1 > kb || u.kb0 >= u.kb1) {
+                    bad |= fail("unit range", u.tile, u.kb0);
+                    break;
+                }
+                for (int k = u.kb0; k < u.kb1; ++k) cover[(size_t)u.tile * kb + k]++;
+                work[c] += u.kb1 - u.kb0;
+                if (u.sk < 0) {
+                    ++n_dp;
+                    if (u.kb0 != 0 || u.kb1 != kb) bad |= fail("dp not whole", u.tile, c);
+                } else {
+                    if (u.sk != u.tile - s.dp_tiles) bad |= fail("sk index", u.sk, u.tile);
+                    contrib[u.sk].push_back({c, u.kb0});
+                }
+                int mb, nb;
+                s.order.coords(u.tile, mb, nb);
+                if (mb < 0 || mb >= mt || nb < 0 || nb >= nt) bad |= fail("coords", mb, nb);
+                coords_seen.insert((long long)mb * nt + nb);
+            }
+            if (n_dp != s.dp_tiles / s.grid) bad |= fail("dp per cta", n_dp, c);
+        }
+        for (size_t i = 0; i < cover.size(); ++i)
+            if (cover[i] != 1) { bad |= fail("coverage", (int)(i / kb), cover[i]); break; }
+        if ((int)coords_seen.size() != T) bad |= fail("tile order not a bijection", (int)coords_seen.size(), T);
+        std::set<int> slots_used;
+        int split_tiles = 0, max_contrib = 0;
+        for (auto &kv : contrib) {
+            const long long st = kv.first;
+            const int lo = s.sk_owner(st * kb), hi = s.sk_owner(st * kb + kb - 1);
+            const auto &v = kv.second;
+            if ((int)v.size() != hi - lo + 1) { bad |= fail("contributor count", (int)v.size(), hi - lo + 1); continue; }
+            for (int i = 0; i < (int)v.size(); ++i) {
+                if (v[i].first != lo + i) bad |= fail("contributor order", v[i].first, lo + i);
+                if (i > 0 && v[i].second <= v[i - 1].second) bad |= fail("k order", v[i].second, v[i - 1].second);
+            }
+            if (hi > lo) {
+                ++split_tiles;
+                for (int c = lo; c <= hi; ++c) {
+                    const int slot = 2 * c + s.sk_slot(c, st);
+                    if (!slots_used.insert(slot).second) bad |= fail("slot collision", slot, (int)st);
+                }
+            }
+            if (hi - lo + 1 > max_contrib) max_contrib = hi - lo + 1;
+        }
+        long long wmin = work[0], wmax = work[0];
+        for (long long w : work) { wmin = w < wmin ? w : wmin; wmax = w > wmax ? w : wmax; }
+        if (wmax - wmin > 1) bad |= fail("imbalance", (int)wmin, (int)wmax);
+        std::printf("mt=%d nt=%d kb=%d sms=%d grid=%d dp=%d sk_iters=%lld split=%d max_contrib=%d work=[%lld,%lld]\n",
+                    mt, nt, kb, sms, s.grid, s.dp_tiles, s.sk_iters, split_tiles, max_contrib, wmin, wmax);
+    }
+    return bad;
+}

@@ -1,0 +1,42 @@
+"""Host-side checks of the persistent / stream-K work schedule (no GPU):
+compiles tests/schedule_check.cpp against schedule.cuh with g++ and runs it
+over every workload shape and a sweep of small and ragged shapes."""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import workloads
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def checker(tmp_path_factory):
+    exe = str(tmp_path_factory.mktemp("sched") / "schedule_check")
+    subprocess.run(["g++", "-O1", "-std=c++17", "-Wall", os.path.join(HERE, "schedule_check.cpp"),
+                    "-o", exe], check=True)
+    return exe
+
+
+def _cases():
+    cases = []
+    for w in workloads.WORKLOADS:
+        mt, nt, kb = -(-w.M // 128), -(-w.N // 128), -(-w.K // 64)
+        for sms in (152, 148, 132):
+            cases.append((mt, nt, kb, sms, 8))
+    rng = np.random.Generator(np.random.PCG64(3))
+    for _ in range(300):
+        cases.append((int(rng.integers(1, 40)), int(rng.integers(1, 40)), int(rng.integers(1, 30)),
+                      int(rng.integers(1, 200)), int(rng.integers(1, 10))))
+    cases += [(1, 1, 1, 152, 8), (1, 1, 200, 152, 8), (1, 152, 3, 152, 8), (2, 152, 5, 152, 8),
+              (1, 153, 7, 152, 1), (64, 231, 128, 152, 8)]
+    return cases
+
+
+def test_schedule_covers_every_iteration_once_and_balances(checker):
+    inp = "\n".join(" ".join(map(str, c)) for c in _cases()) + "\n"
+    r = subprocess.run([checker], input=inp, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout[-3000:]
+    assert r.stdout.count("\n") == len(_cases())

@@ -404,11 +404,15 @@ def main(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD,
                    help="workload label (workloads.WORKLOADS), default 1 = Qwen-2.5-1.5B M=2048")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--variant", choices=("auto", "1sm", "2sm"), default="auto",
+                   help="fused kernel: auto (2-SM pairs for M >= 256), or force one (ablation)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     import workloads
     w = workloads.BY_LABEL[args.workload]
+    if args.variant != "auto":
+        os.environ["SWIGLU_FUSED_VARIANT"] = args.variant
     if args.impl == "reference":
         return run_reference(args, w)
     return run_gb300(args, w)

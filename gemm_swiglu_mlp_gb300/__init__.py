@@ -47,6 +47,7 @@ EXPORTED_SYMBOLS = (
 
 _lock = threading.Lock()
 _lib = None
+_workspaces = {}   # (device index, stream handle) -> zero-initialised uint8 tensor
 
 
 class SwigluError(RuntimeError):
@@ -165,17 +166,33 @@ def swiglu_up_forward(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: torch.T
         _require_bf16_cuda(Y, "Y")
         if tuple(Y.shape) != (M, N):
             raise ValueError("Y must be [%d, %d]" % (M, N))
-    ws_need = swiglu_workspace_bytes(M, N, K)
-    ws_ptr, ws_bytes = None, 0
-    if ws_need:
-        if workspace is None:
-            workspace = torch.zeros(ws_need, dtype=torch.uint8, device=A.device)
-        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     with torch.cuda.device(A.device):
+        ws_need = swiglu_workspace_bytes(M, N, K)
+        ws_ptr, ws_bytes = None, 0
+        if ws_need:
+            if workspace is None:
+                workspace = _default_workspace(A.device, ws_need, stream)
+            ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
         _check(lib.swiglu_up_forward(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(), M, N, K,
                                      ws_ptr, ws_bytes, _stream_handle(stream)),
                "swiglu_up_forward")
     return Y
+
+
+def _default_workspace(device, nbytes: int, stream) -> torch.Tensor:
+    """One zero-filled workspace per (device, stream), grown on demand. Calls
+    on one stream run one after another, and each completed call leaves the
+    workspace's counters at zero, so reuse across calls and shapes is safe.
+    The zero fill is ordered on the same stream as the calls that use it."""
+    dev = torch.device(device)
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    key = (dev.index, int(s.cuda_stream))
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        with torch.cuda.stream(s):
+            ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        _workspaces[key] = ws
+    return ws
 
 
 def swiglu_check_device_status(stream=None) -> int:

@@ -1,0 +1,118 @@
+// Pieces shared by the 1-SM and 2-SM fused kernels: the device status word,
+// the stream-K workspace slot shape, the argument block, and the epilogue
+// math (SiLU(g) * u in FP32 -> BF16 into 128-byte-swizzled staging).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "schedule.cuh"
+#include "sm103_ptx.cuh"
+
+namespace swiglu {
+
+// Device status word, read and cleared by swiglu_check_device_status. The
+// library is one translation unit (no relocatable device code), so the
+// definition lives here.
+__device__ unsigned int g_status_word = 0;
+
+enum : unsigned int {
+    kStatusProducerTimeout = 1u,
+    kStatusMmaTimeout = 2u,
+    kStatusEpilogueTimeout = 4u,
+    kStatusDrainTimeout = 8u,
+};
+
+// FP32 Gate|Up partial of one tile in the workspace: 256 columns (Gate
+// 0..127, Up 128..255) x slot_rows rows, column-major so that the 32 lanes of
+// a warp (32 consecutive rows) touch 128 contiguous bytes per column.
+// slot_rows = min(128, M rounded up to 32): rows past it are never live.
+constexpr int kSlotCols = 256;
+
+__host__ __device__ __forceinline__ int slot_rows_for(long long M) {
+    return M >= 128 ? 128 : static_cast<int>((M + 31) / 32 * 32);
+}
+
+struct FusedArgs {
+    int M, N, K;
+    int stage_tx_bytes;       // bytes one stage's TMA loads deliver (A box + weight tile)
+    int slot_rows;            // rows per workspace slot
+    WorkSched sched;
+    float *partials;          // 2 * grid slots of kSlotCols * slot_rows floats (stream-K only)
+    unsigned int *counters;   // one per stream-K tile, zero between launches
+};
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    // SiLU(g) = g / (1 + e^-g); for g << 0 the denominator is +inf and the
+    // quotient 0, the limit.
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Bounded wait that ignores the abort flag (used while draining).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const int never = 0;
+    return mbar_wait(bar, parity, &never);
+}
+
+// Named barrier over the four epilogue warps only.
+__device__ __forceinline__ void epilogue_bar() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// Named barrier over the four epilogue warps that also ANDs a predicate over
+// them: every epilogue thread gets the same answer, so all four warps take
+// the same branch afterwards (no warp can be left alone at a later barrier).
+__device__ __forceinline__ bool epilogue_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v))
+        : "memory");
+    return r != 0;
+}
+
+// y for 32 consecutive columns [c, c+32) of this thread's row, from FP32 Gate
+// and Up values, written as BF16 into the warp's swizzled staging buffer.
+__device__ __forceinline__ void stage_y32(uint32_t ybuf, int lane, int c, const float (&g)[32],
+                                          const float (&u)[32]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 8 * j + 2 * e;
+            w[e] = pack_bf16x2(silu_mul(g[i], u[i]), silu_mul(g[i + 1], u[i + 1]));
+        }
+        // 128-byte swizzle: 16-byte chunk index XOR (row % 8)
+        const int col = c + 8 * j;
+        const int half = col >> 6;
+        const int chunk = (col & 63) >> 3;
+        const uint32_t addr = ybuf + half * (32 * 64 * 2) + lane * 128 +
+                              (static_cast<uint32_t>(chunk ^ (lane & 7)) << 4);
+        st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+    }
+}
+
+__device__ __forceinline__ void tmem_ld_gu(uint32_t tbase, int c, float (&g)[32], float (&u)[32]) {
+    uint32_t gr[32], ur[32];
+    tmem_ld_32x32b_x32(tbase + c, gr);
+    tmem_ld_32x32b_x32(tbase + 128 + c, ur);
+    tmem_ld_wait();
+    reg_fence32(gr);
+    reg_fence32(ur);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        g[i] = __uint_as_float(gr[i]);
+        u[i] = __uint_as_float(ur[i]);
+    }
+}
+
+}  // namespace swiglu

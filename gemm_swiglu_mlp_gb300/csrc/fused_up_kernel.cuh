@@ -6,15 +6,28 @@
 //
 //   warp 0        TMA producer: for each k-block loads one A tile [128 x 64]
 //                 and one packed weight tile [256 x 64] (128 Gate rows then
-//                 128 Up rows of the same output columns) into a STAGES-deep
-//                 shared-memory ring. Each A tile feeds both products.
+//                 128 Up rows of the same output columns, one contiguous
+//                 32 KB block of the packed operand) into a STAGES-deep
+//                 shared-memory ring. Each A tile feeds both products. When
+//                 M < 128 the A box has only ceil(M/8)*8 rows: the rows past
+//                 it keep stale shared-memory data, which reaches only
+//                 accumulator rows >= M, and those are never stored.
 //   warp 1        MMA issuer: one tcgen05.mma (M=128, N=256, K=16) per K
 //                 step puts Gate in TMEM columns [0,128) and Up in [128,256)
 //                 of one accumulator stage; two stages (512 columns) let the
-//                 next tile's MMAs run while the epilogue drains this one.
+//                 next unit's MMAs run while the epilogue drains this one.
 //   warps 2..5    epilogue: tcgen05.ld Gate and Up for 32 rows each,
 //                 y = SiLU(g) * u in FP32, round to BF16, stage in 128-byte
 //                 swizzled shared memory, TMA store (clipped at M and N).
+//
+// Work is split by schedule.cuh: whole tiles first, then an even stream-K
+// split of the remaining k-block iterations. A tile cut between CTAs is
+// finished without any inter-CTA waiting: every contributor writes its FP32
+// Gate/Up partial to a workspace slot and increments the tile's counter; the
+// one that brings the counter to the number of contributors sums all
+// partials in k order (so the result does not depend on arrival order),
+// applies the activation, stores Y and resets the counter to zero. SiLU is
+// nonlinear, so partial sums are always combined BEFORE it.
 //
 // This replaces the pages' two SM90 designs (technical summary, "Kernel-1"
 // and "Kernel-2"): the packed operand plays the role of Kernel-2's fused
@@ -29,48 +42,9 @@
 // TMEM is released before the CTA exits.
 #pragma once
 
-#include <cuda_bf16.h>
-
-#include "sm103_ptx.cuh"
+#include "epilogue.cuh"
 
 namespace swiglu {
-
-// Device status word, read and cleared by swiglu_check_device_status. The
-// library is one translation unit (no relocatable device code), so the
-// definition lives here.
-__device__ unsigned int g_status_word = 0;
-
-enum : unsigned int {
-    kStatusProducerTimeout = 1u,
-    kStatusMmaTimeout = 2u,
-    kStatusEpilogueTimeout = 4u,
-    kStatusDrainTimeout = 8u,
-};
-
-// Persistent tile order: tiles are visited in groups of `group_m` row-tiles;
-// inside a group the row-tile index runs fastest, so the CTAs working at the
-// same time share a few weight blocks and a bounded slab of A in L2.
-struct TileOrder {
-    int m_tiles;
-    int n_tiles;
-    int group_m;
-    __device__ __forceinline__ void coords(int t, int &mb, int &nb) const {
-        const int per_group = group_m * n_tiles;
-        const int g = t / per_group;
-        const int first_m = g * group_m;
-        const int gm = min(group_m, m_tiles - first_m);
-        const int idx = t - g * per_group;
-        nb = idx / gm;
-        mb = first_m + idx % gm;
-    }
-};
-
-struct FusedArgs {
-    int M, N, K;
-    int k_blocks;
-    int num_tiles;
-    TileOrder order;
-};
 
 template <int STAGES>
 struct FusedCfg {
@@ -91,31 +65,13 @@ struct FusedCfg {
     static constexpr int OFF_Y = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_BAR = OFF_Y + EPI_WARPS * Y_WARP_BYTES;
     static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull x2, tempty x2, drain
-    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag, last flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + 1 KB alignment slack
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static_assert(TMEM_COLS == 512, "two 256-column accumulator stages fill TMEM");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(UMMA_N == kSlotCols, "workspace slot shape");
 };
-
-__device__ __forceinline__ float silu_mul(uint32_t gbits, uint32_t ubits) {
-    const float g = __uint_as_float(gbits);
-    const float u = __uint_as_float(ubits);
-    // SiLU(g) = g / (1 + e^-g); for g << 0 the denominator is +inf and the
-    // quotient 0, the limit.
-    return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-
-// Bounded wait that ignores the abort flag (used while draining).
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
-    const int never = 0;
-    return mbar_wait(bar, parity, &never);
-}
 
 template <int STAGES>
 __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
@@ -130,6 +86,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
 
     auto full_bar = [&](int s) { return sbase + C::OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sbase + C::OFF_BAR + 8u * (STAGES + s); };
@@ -138,6 +95,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
     const uint32_t drain_bar = sbase + C::OFF_BAR + 8u * (2 * STAGES + 4);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -150,6 +108,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
+        *last_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
@@ -163,6 +122,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    const WorkSched &sched = args.sched;
 
     // Producer bookkeeping kept for the drain after an abort: which stages
     // received a load, and the parity of the phase of the last one.
@@ -173,19 +133,22 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+            UnitIter it;
+            it.init(sched, cta);
+            Unit u;
+            while (ok && it.next(u)) {
                 int mb, nb;
-                args.order.coords(t, mb, nb);
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                sched.order.coords(u.tile, mb, nb);
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
+                    mbar_arrive_expect_tx(full_bar(stage), args.stage_tx_bytes);
                     tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
                                 kb * C::BK, mb * C::BM);
-                    tma_load_2d(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, full_bar(stage),
-                                kb * C::BK, nb * C::UMMA_N);
+                    tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, full_bar(stage), 0, 0,
+                                nb * sched.k_blocks + kb);
                     issued_mask |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -207,14 +170,17 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+            UnitIter it;
+            it.init(sched, cta);
+            Unit u;
+            while (ok && it.next(u)) {
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::UMMA_N);
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
                         ok = false;
                         break;
@@ -226,7 +192,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                     for (int k = 0; k < C::BK / C::UMMA_K; ++k) {
                         // +32 bytes along K per step inside the 128-byte swizzle row
                         umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
-                                  (kb | k) != 0 ? 1u : 0u);
+                                  (kb != u.kb0 || k != 0) ? 1u : 0u);
                     }
                     umma_commit(empty_bar(stage));
                     if (++stage == STAGES) {
@@ -250,53 +216,119 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
         // Epilogue warps 2..5. tcgen05.ld lets warp w touch TMEM lanes
         // [32*(w%4), 32*(w%4)+32): those are the tile rows it owns.
         const int quad = warp & 3;
+        const int row_in_tile = 32 * quad + lane;
         const uint32_t ybuf = sbase + C::OFF_Y + (warp - 2) * C::Y_WARP_BYTES;
+        const bool leader = (warp == 2 && lane == 0);
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+        UnitIter it;
+        it.init(sched, cta);
+        Unit u;
+        while (it.next(u)) {
             int mb, nb;
-            args.order.coords(t, mb, nb);
-            ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, abort_flag));
+            sched.order.coords(u.tile, mb, nb);
+            // Accumulator ready? The answer must be the same in all four warps:
+            // one warp could see the barrier complete while another sees the
+            // abort flag first.
+            ok = epilogue_all(mbar_wait(tfull_bar(acc), acc_phase, abort_flag));
             if (!ok) break;
             tc_fence_after();
             const int row0 = mb * C::BM + 32 * quad;
             const bool rows_live = row0 < args.M;
-            if (rows_live) {
-                if (lane == 0) bulk_wait_group_read0();  // last store has read ybuf
-                __syncwarp();
-                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) +
-                                       static_cast<uint32_t>(acc * C::UMMA_N);
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) +
+                                   static_cast<uint32_t>(acc * C::UMMA_N);
+
+            // Contributors of a stream-K tile: CTAs c_lo..c_hi, in k order.
+            int c_lo = cta, c_hi = cta;
+            if (u.sk >= 0) {
+                const long long first = static_cast<long long>(u.sk) * sched.k_blocks;
+                c_lo = sched.sk_owner(first);
+                c_hi = sched.sk_owner(first + sched.k_blocks - 1);
+            }
+            const bool split = c_hi > c_lo;
+            bool store_y = true;
+
+            if (!split) {
+                if (rows_live) {
+                    if (lane == 0) bulk_wait_group_read0();  // last store has read ybuf
+                    __syncwarp();
 #pragma unroll 1
-                for (int c = 0; c < C::BN; c += 32) {
-                    uint32_t g[32], u[32];
-                    tmem_ld_32x32b_x32(tbase + c, g);
-                    tmem_ld_32x32b_x32(tbase + C::BN + c, u);
-                    tmem_ld_wait();
-                    reg_fence32(g);
-                    reg_fence32(u);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i = 8 * j + 2 * e;
-                            w[e] = pack_bf16x2(silu_mul(g[i], u[i]), silu_mul(g[i + 1], u[i + 1]));
-                        }
-                        // 128-byte swizzle: 16-byte chunk index XOR (row % 8)
-                        const int col = c + 8 * j;
-                        const int half = col >> 6;
-                        const int chunk = (col & 63) >> 3;
-                        const uint32_t addr = ybuf + half * C::Y_HALF_BYTES + lane * 128 +
-                                              (static_cast<uint32_t>(chunk ^ (lane & 7)) << 4);
-                        st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+                    for (int c = 0; c < C::BN; c += 32) {
+                        float g[32], v[32];
+                        tmem_ld_gu(tbase, c, g, v);
+                        stage_y32(ybuf, lane, c, g, v);
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+            } else {
+                // 1) this CTA's FP32 partial -> its workspace slot
+                const size_t slot_floats = static_cast<size_t>(kSlotCols) * args.slot_rows;
+                float *slot = args.partials +
+                              static_cast<size_t>(2 * cta + sched.sk_slot(cta, u.sk)) * slot_floats;
+                if (rows_live) {
+#pragma unroll 1
+                    for (int c = 0; c < C::BN; c += 32) {
+                        float g[32], v[32];
+                        tmem_ld_gu(tbase, c, g, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            __stcg(slot + static_cast<size_t>(c + i) * args.slot_rows + row_in_tile,
+                                   g[i]);
+                            __stcg(slot + static_cast<size_t>(C::BN + c + i) * args.slot_rows +
+                                       row_in_tile,
+                                   v[i]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                // 2) publish, and find out whether this CTA completes the tile
+                __threadfence();
+                epilogue_bar();
+                if (leader) {
+                    const unsigned int prev = atomicAdd(args.counters + u.sk, 1u);
+                    *last_flag = (prev == static_cast<unsigned int>(c_hi - c_lo)) ? 1 : 0;
+                }
+                epilogue_bar();
+                store_y = *last_flag != 0;
+                if (store_y) {
+                    __threadfence();
+                    // 3) sum every contributor's partial in k order, then activate
+                    if (rows_live) {
+                        if (lane == 0) bulk_wait_group_read0();
+                        __syncwarp();
+#pragma unroll 1
+                        for (int c = 0; c < C::BN; c += 32) {
+                            float g[32], v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                g[i] = 0.0f;
+                                v[i] = 0.0f;
+                            }
+                            for (int k = c_lo; k <= c_hi; ++k) {
+                                const float *src = args.partials +
+                                    static_cast<size_t>(2 * k + sched.sk_slot(k, u.sk)) * slot_floats;
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    const float pg = __ldcg(src + static_cast<size_t>(c + i) *
+                                                                      args.slot_rows + row_in_tile);
+                                    const float pu = __ldcg(src + static_cast<size_t>(C::BN + c + i) *
+                                                                      args.slot_rows + row_in_tile);
+                                    g[i] = (k == c_lo) ? pg : g[i] + pg;
+                                    v[i] = (k == c_lo) ? pu : v[i] + pu;
+                                }
+                            }
+                            stage_y32(ybuf, lane, c, g, v);
+                        }
+                    }
+                    if (leader) args.counters[u.sk] = 0u;  // ready for the next launch
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
-            if (rows_live) {
+            if (store_y && rows_live) {
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {

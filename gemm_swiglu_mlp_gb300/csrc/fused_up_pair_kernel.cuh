@@ -1,0 +1,372 @@
+// 2-SM (CTA pair) fused SwiGLU up-projection for sm_103a.
+//
+// Same computation as fused_up_kernel.cuh ("Tile-Level Activation Overlap for
+// Efficient LLM Inference", Section 1 Introduction: Y = SiLU(A x W1) (.)
+// (A x W2), Gate and Up never written to global memory), for large M. A
+// cluster of two CTAs on two SMs works on a 256-row x 128-column tile with
+// one 2-SM UMMA (tcgen05.mma.cta_group::2, M=256, N=256):
+//
+//   * each CTA loads ITS 128 rows of A and ITS HALF of the packed weight tile
+//     (leader: the 128 Gate rows, peer: the 128 Up rows) into its own
+//     shared memory: 32 KB per k-block per SM instead of 48 KB, so the
+//     operand traffic into each SM is two thirds of the 1-SM kernel's, and
+//     six stages fit in shared memory;
+//   * the leader's single MMA thread issues the UMMA; the accumulator lands
+//     in both SMs' TMEM (each CTA holds its own 128 rows, all 256 Gate|Up
+//     columns), so each CTA's epilogue is the 1-SM epilogue unchanged;
+//   * both CTAs' TMA loads signal the leader's full barrier; the leader's
+//     commits are multicast to both CTAs' empty / accumulator-full barriers;
+//     both CTAs' epilogue warps arrive on the leader's accumulator-empty
+//     barrier.
+//
+// Work split: schedule.cuh over pairs (data-parallel pair tiles, then
+// stream-K). Split tiles are summed per CTA half through the workspace as in
+// the 1-SM kernel (slot = (2 * pair + first/last) * 2 + rank, counter =
+// 2 * stream-K tile + rank).
+//
+// Every wait is bounded. An abort sets the abort flag of both CTAs of the
+// pair; after a cluster barrier the leader drains the loads and MMAs in
+// flight (all loads of the pair complete on the leader's barriers), a second
+// cluster barrier keeps the peer alive until then, and both CTAs free TMEM.
+#pragma once
+
+#include "epilogue.cuh"
+
+namespace swiglu {
+
+template <int STAGES>
+struct PairCfg {
+    static constexpr int BM = 128;                  // rows per CTA; the pair tile has 256
+    static constexpr int BN = 128;                  // output columns per tile
+    static constexpr int BK = 64;                   // K per stage: 128-byte rows
+    static constexpr int UMMA_M = 256;
+    static constexpr int UMMA_N = 2 * BN;           // Gate | Up
+    static constexpr int UMMA_K = 16;
+    static constexpr int A_BYTES = BM * BK * 2;     // 16 KB: this CTA's A rows
+    static constexpr int B_BYTES = BN * BK * 2;     // 16 KB: this CTA's half of Gate|Up
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int Y_HALF_BYTES = 32 * 64 * 2;
+    static constexpr int Y_WARP_BYTES = 2 * Y_HALF_BYTES;
+    static constexpr int TMEM_COLS = 2 * UMMA_N;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_Y = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_BAR = OFF_Y + EPI_WARPS * Y_WARP_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull x2, tempty x2, drain
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static_assert(TMEM_COLS == 512, "two 256-column accumulator stages fill TMEM");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(UMMA_N == kSlotCols, "workspace slot shape");
+};
+
+template <int STAGES>
+__global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
+    fused_up_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmY, const FusedArgs args) {
+    using C = PairCfg<STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const uint32_t sbase = smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool is_leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+
+    auto full_bar = [&](int s) { return sbase + C::OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sbase + C::OFF_BAR + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return sbase + C::OFF_BAR + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return sbase + C::OFF_BAR + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t drain_bar = sbase + C::OFF_BAR + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);
+    // the same flag in the other CTA of the pair
+    const uint32_t peer_abort = mapa_shared(sbase + C::OFF_MISC + 4, rank ^ 1u);
+    auto set_abort_both = [&]() {
+        *abort_flag = 1;
+        st_cluster_u32(peer_abort, 1u);
+    };
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 2 * C::EPI_WARPS);  // epilogue warps of both CTAs
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmY);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const WorkSched &sched = args.sched;
+
+    uint32_t issued_mask = 0, last_parity = 0;  // leader's drain bookkeeping
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            UnitIter it;
+            it.init(sched, pair);
+            Unit u;
+            while (ok && it.next(u)) {
+                int pm, nb;
+                sched.order.coords(u.tile, pm, nb);
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    // every load of the pair completes on the LEADER's full barrier
+                    if (is_leader) mbar_arrive_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
+                    const uint32_t bar = mapa_shared(full_bar(stage), 0);
+                    tma_load_2d_pair(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, bar, kb * C::BK,
+                                     pm * C::UMMA_M + C::BM * static_cast<int>(rank));
+                    tma_load_3d_pair(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, bar, 0,
+                                     C::BN * static_cast<int>(rank), nb * sched.k_blocks + kb);
+                    issued_mask |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok && !*abort_flag) {
+                atomicOr(&g_status_word, kStatusProducerTimeout);
+                set_abort_both();
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && is_leader) {
+            constexpr uint32_t idesc = idesc_bf16_f32(C::UMMA_M, C::UMMA_N);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            UnitIter it;
+            it.init(sched, pair);
+            Unit u;
+            while (ok && it.next(u)) {
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::UMMA_N);
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a_desc = smem_desc_k128(sbase + C::OFF_A + stage * C::A_BYTES);
+                    const uint64_t b_desc = smem_desc_k128(sbase + C::OFF_B + stage * C::B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < C::BK / C::UMMA_K; ++k)
+                        umma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
+                                       (kb != u.kb0 || k != 0) ? 1u : 0u);
+                    umma_commit_pair_mc(empty_bar(stage), 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair_mc(tfull_bar(acc), 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (!ok && !*abort_flag) {
+                atomicOr(&g_status_word, kStatusMmaTimeout);
+                set_abort_both();
+            }
+        }
+    } else {
+        const int quad = warp & 3;
+        const int row_in_tile = 32 * quad + lane;  // row within this CTA's 128 rows
+        const uint32_t ybuf = sbase + C::OFF_Y + (warp - 2) * C::Y_WARP_BYTES;
+        const bool lead_thread = (warp == 2 && lane == 0);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        UnitIter it;
+        it.init(sched, pair);
+        Unit u;
+        while (it.next(u)) {
+            int pm, nb;
+            sched.order.coords(u.tile, pm, nb);
+            ok = epilogue_all(mbar_wait(tfull_bar(acc), acc_phase, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            const int row0 = pm * C::UMMA_M + C::BM * static_cast<int>(rank) + 32 * quad;
+            const bool rows_live = row0 < args.M;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) +
+                                   static_cast<uint32_t>(acc * C::UMMA_N);
+            const uint32_t tempty_leader = mapa_shared(tempty_bar(acc), 0);
+
+            int c_lo = pair, c_hi = pair;
+            if (u.sk >= 0) {
+                const long long first = static_cast<long long>(u.sk) * sched.k_blocks;
+                c_lo = sched.sk_owner(first);
+                c_hi = sched.sk_owner(first + sched.k_blocks - 1);
+            }
+            const bool split = c_hi > c_lo;
+            bool store_y = true;
+
+            if (!split) {
+                if (rows_live) {
+                    if (lane == 0) bulk_wait_group_read0();
+                    __syncwarp();
+#pragma unroll 1
+                    for (int c = 0; c < C::BN; c += 32) {
+                        float g[32], v[32];
+                        tmem_ld_gu(tbase, c, g, v);
+                        stage_y32(ybuf, lane, c, g, v);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tempty_leader);
+            } else {
+                const size_t slot_floats = static_cast<size_t>(kSlotCols) * args.slot_rows;
+                auto slot_of = [&](int p) {
+                    return args.partials +
+                           static_cast<size_t>((2 * p + sched.sk_slot(p, u.sk)) * 2 + rank) *
+                               slot_floats;
+                };
+                float *slot = slot_of(pair);
+                if (rows_live) {
+#pragma unroll 1
+                    for (int c = 0; c < C::BN; c += 32) {
+                        float g[32], v[32];
+                        tmem_ld_gu(tbase, c, g, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            __stcg(slot + static_cast<size_t>(c + i) * args.slot_rows + row_in_tile,
+                                   g[i]);
+                            __stcg(slot + static_cast<size_t>(C::BN + c + i) * args.slot_rows +
+                                       row_in_tile,
+                                   v[i]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tempty_leader);
+                __threadfence();
+                epilogue_bar();
+                unsigned int *counter = args.counters + 2 * u.sk + rank;
+                if (lead_thread) {
+                    const unsigned int prev = atomicAdd(counter, 1u);
+                    *last_flag = (prev == static_cast<unsigned int>(c_hi - c_lo)) ? 1 : 0;
+                }
+                epilogue_bar();
+                store_y = *last_flag != 0;
+                if (store_y) {
+                    __threadfence();
+                    if (rows_live) {
+                        if (lane == 0) bulk_wait_group_read0();
+                        __syncwarp();
+#pragma unroll 1
+                        for (int c = 0; c < C::BN; c += 32) {
+                            float g[32], v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                g[i] = 0.0f;
+                                v[i] = 0.0f;
+                            }
+                            for (int p = c_lo; p <= c_hi; ++p) {
+                                const float *src = slot_of(p);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    const float pg = __ldcg(src + static_cast<size_t>(c + i) *
+                                                                      args.slot_rows + row_in_tile);
+                                    const float pu = __ldcg(src + static_cast<size_t>(C::BN + c + i) *
+                                                                      args.slot_rows + row_in_tile);
+                                    g[i] = (p == c_lo) ? pg : g[i] + pg;
+                                    v[i] = (p == c_lo) ? pu : v[i] + pu;
+                                }
+                            }
+                            stage_y32(ybuf, lane, c, g, v);
+                        }
+                    }
+                    if (lead_thread) *counter = 0u;
+                }
+            }
+            if (store_y && rows_live) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int x0 = nb * C::BN;
+                    tma_store_2d(&tmY, ybuf, x0, row0);
+                    if (x0 + 64 < args.N) tma_store_2d(&tmY, ybuf + C::Y_HALF_BYTES, x0 + 64, row0);
+                    bulk_commit_group();
+                }
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (lane == 0) {
+            bulk_wait_group0();
+            if (!ok && !*abort_flag) {
+                atomicOr(&g_status_word, kStatusEpilogueTimeout);
+                set_abort_both();
+            }
+        }
+    }
+
+    // ---- teardown
+    __syncthreads();
+    cluster_sync();  // both CTAs out of their loops; abort flags final
+    if (*abort_flag && is_leader) {
+        if (warp == 0 && lane == 0) {
+            // every load of the pair completes on the leader's full barriers
+            for (int s = 0; s < STAGES; ++s)
+                if ((issued_mask >> s) & 1u)
+                    if (!mbar_wait_drain(full_bar(s), (last_parity >> s) & 1u))
+                        atomicOr(&g_status_word, kStatusDrainTimeout);
+        }
+        if (warp == 1 && lane == 0) {
+            umma_commit_pair_mc(drain_bar, 0x1);
+            if (!mbar_wait_drain(drain_bar, 0)) atomicOr(&g_status_word, kStatusDrainTimeout);
+        }
+    }
+    __syncthreads();
+    cluster_sync();  // the peer stays until the leader has drained
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace swiglu

@@ -1,11 +1,15 @@
-// Weight packing: W1, W2 [K, N] row-major BF16 -> Wpacked [2*Np, K] K-major.
+// Weight packing: W1, W2 [K, N] row-major BF16 -> Wpacked, tile-contiguous.
 //
-// Packed row p belongs to block j = p / 256; r = p % 256; rows r < 128 are
-// Gate columns n = 128j + r (W1[:, n] transposed), rows r >= 128 are Up
-// columns n = 128j + r - 128 (W2[:, n] transposed); n >= N gives a zero row.
+// Wpacked is [NB][KB][256][64] BF16 with NB = ceil(N/128), KB = ceil(K/64):
+// element (j, b, r, kk) is W1[64b + kk][128j + r] for r < 128 (Gate) and
+// W2[64b + kk][128j + r - 128] for r >= 128 (Up); zero where the column is
+// >= N or the k index is >= K. One (j, b) tile is one contiguous 32 KB block
+// holding exactly what one k-block of one output tile needs (both Gate and
+// Up rows, K-major), so each weight load is a single contiguous read.
 // This is the tensor-core-friendly form of the pages' fused weight matrix
 // (technical summary, "Kernel-2": W1 and W2 merged into one K x 2N operand so
-// one GEMM feeds Gate and Up from the same A tile). A permutation: bit-exact.
+// one GEMM feeds Gate and Up from the same A tile). A permutation plus zero
+// padding: bit-exact.
 #pragma once
 
 #include <cstdint>
@@ -14,16 +18,18 @@ namespace swiglu {
 
 constexpr int kPackTile = 64;
 
-// One CTA transposes a 64 (k) x 64 (n) tile through shared memory so that
-// both the reads (along n) and the writes (along k) are coalesced.
+// One CTA transposes a 64 (k) x 64 (n) tile through shared memory: reads
+// are coalesced along n, and the 64 packed rows it writes (64 x 128 bytes)
+// are one contiguous 8 KB run of the output.
 __global__ void __launch_bounds__(256) pack_weights_kernel(const uint16_t *__restrict__ W1,
                                                             const uint16_t *__restrict__ W2,
                                                             uint16_t *__restrict__ Wp, int K,
-                                                            int N) {
+                                                            int N, int KB) {
     __shared__ uint16_t tile[kPackTile][kPackTile + 2];
-    const int k0 = blockIdx.x * kPackTile;
-    const int p0 = blockIdx.y * kPackTile;   // first packed row of this CTA
-    const int j = p0 / 256;
+    const int b = blockIdx.x;                // k-block
+    const int k0 = b * kPackTile;
+    const int p0 = blockIdx.y * kPackTile;   // first packed row (over all 2*Np rows)
+    const int j = p0 / 256;                  // output-column block
     const int r0 = p0 % 256;                 // 64-row chunks never straddle Gate/Up halves
     const bool up = r0 >= 128;
     const int n0 = 128 * j + (r0 & 127);
@@ -35,10 +41,11 @@ __global__ void __launch_bounds__(256) pack_weights_kernel(const uint16_t *__res
         tile[kk][nn] = (k < K && n < N) ? W[static_cast<int64_t>(k) * N + n] : uint16_t(0);
     }
     __syncthreads();
+    uint16_t *__restrict__ out =
+        Wp + ((static_cast<int64_t>(j) * KB + b) * 256 + r0) * kPackTile;
     for (int i = threadIdx.x; i < kPackTile * kPackTile; i += blockDim.x) {
         const int nn = i / kPackTile, kk = i % kPackTile;
-        const int k = k0 + kk;
-        if (k < K) Wp[static_cast<int64_t>(p0 + nn) * K + k] = tile[kk][nn];
+        out[nn * kPackTile + kk] = tile[kk][nn];
     }
 }
 

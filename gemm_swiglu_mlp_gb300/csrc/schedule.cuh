@@ -3,8 +3,9 @@
 // Tiles are 128 token rows x 128 output columns (one UMMA N=256 covers their
 // Gate and Up columns). With T tiles, kb k-blocks per tile and G persistent
 // CTAs:
-//   * data-parallel part: tiles [0, dp_tiles) run whole, round robin; dp_tiles
-//     is a multiple of G, so every CTA gets the same number of them;
+//   * data-parallel part: tiles [0, dp_tiles) run whole, round robin (when a
+//     stream-K part follows, dp_tiles is a multiple of G, so every CTA gets
+//     the same number of them);
 //   * stream-K part: the k-block iterations of tiles [dp_tiles, T) form one
 //     space of sk_iters = (T - dp_tiles) * kb iterations, cut into G
 //     contiguous ranges whose lengths differ by at most one. A tile whose
@@ -41,7 +42,7 @@ struct WorkSched {
     int num_tiles;
     int k_blocks;
     int grid;
-    int dp_tiles;        // multiple of grid
+    int dp_tiles;        // a multiple of grid whenever sk_iters > 0
     long long sk_iters;  // (num_tiles - dp_tiles) * k_blocks; >= grid when > 0
     TileOrder order;
 
@@ -105,10 +106,18 @@ struct UnitIter {
     }
 };
 
-// Host-side choice of grid and split. `min_sk_iters` keeps every CTA's
-// stream-K share at a few k-blocks so tiles are not cut into slivers.
+// Host-side choice of grid and split. Whole tiles round robin (no
+// workspace) unless that leaves the grid poorly used: with W = ceil(T/G)
+// waves, the data-parallel efficiency is T / (W * G); below
+// `min_dp_efficiency` the stream-K split is used. Splitting costs a partial
+// write and a dependent read-back on the critical path at the end of the
+// kernel, more than a mostly full last wave loses (and for weight-streaming
+// shapes a short last wave loses little: its CTAs get more bandwidth each).
+// `min_sk_iters` keeps every CTA's stream-K share at a few k-blocks so tiles
+// are not cut into slivers.
 inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_count,
-                               int group_m, int min_sk_iters = 4) {
+                               int group_m, int min_sk_iters = 4,
+                               double min_dp_efficiency = 0.85) {
     WorkSched s{};
     s.num_tiles = m_tiles * n_tiles;
     s.k_blocks = k_blocks;
@@ -117,9 +126,10 @@ inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_co
     s.order.group_m = group_m < m_tiles ? group_m : m_tiles;
     const long long total = static_cast<long long>(s.num_tiles) * k_blocks;
     long long g = sm_count;
-    if (s.num_tiles % sm_count == 0) {
-        // whole waves: plain data-parallel, no workspace
-        s.grid = sm_count;
+    const int waves = (s.num_tiles + sm_count - 1) / sm_count;
+    if (static_cast<double>(s.num_tiles) >= min_dp_efficiency * waves * sm_count) {
+        // data-parallel: every tile whole, no workspace
+        s.grid = s.num_tiles < sm_count ? s.num_tiles : sm_count;
         s.dp_tiles = s.num_tiles;
         s.sk_iters = 0;
         return s;

@@ -5,10 +5,12 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
 #include "fused_up_kernel.cuh"
+#include "fused_up_pair_kernel.cuh"
 #include "pack_kernel.cuh"
 #include "swiglu.h"
 
@@ -17,12 +19,29 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kFusedStages = 4;
+constexpr int kGroupM = 16;          // row-tiles per L2 group in the tile order
+constexpr int kMinStreamKIters = 8;  // k-blocks per CTA share, at least
+constexpr int kAssumedMaxSms = 256;  // workspace sizing when no device answers
+constexpr int kPairStages = 6;
+constexpr int64_t kPairMinM = 256;   // from this many tokens on, the 2-SM kernel
 using FusedC = FusedCfg<kFusedStages>;
+using PairC = PairCfg<kPairStages>;
+
+// Which kernel serves a call: the 2-SM (CTA pair) kernel for M >= 256, the
+// 1-SM kernel below. SWIGLU_FUSED_VARIANT=1sm|2sm overrides the choice (for
+// ablations and tests); it is read on every call.
+bool use_pair_kernel(int64_t M) {
+    const char *v = std::getenv("SWIGLU_FUSED_VARIANT");
+    if (v && std::strcmp(v, "1sm") == 0) return false;
+    if (v && std::strcmp(v, "2sm") == 0) return true;
+    return M >= kPairMinM;
+}
 
 struct DeviceState {
     std::once_flag once;
     int status = SWIGLU_OK;  // result of the one-time setup
     int sm_count = 0;
+    int pair_clusters = 0;   // CTA pairs of the 2-SM kernel that can run at once
 };
 
 DeviceState g_devices[kMaxDevices];
@@ -71,11 +90,34 @@ int device_setup(int *dev_out, DeviceState **st_out) {
         }
         if (cudaFuncSetAttribute(fused_up_kernel<kFusedStages>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 FusedC::SMEM_BYTES) != cudaSuccess) {
+                                 FusedC::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PairC::SMEM_BYTES) != cudaSuccess) {
             cudaGetLastError();
             st.status = SWIGLU_ERR_CUDA;
             return;
         }
+        // how many CTA pairs fit at once (clusters must sit on SM pairs)
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(sms / 2 * 2));
+        cfg.blockDim = dim3(PairC::THREADS);
+        cfg.dynamicSmemBytes = PairC::SMEM_BYTES;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, fused_up_pair_kernel<kPairStages>, &cfg) !=
+                cudaSuccess ||
+            clusters < 1) {
+            cudaGetLastError();
+            clusters = sms / 2;
+        }
+        st.pair_clusters = std::min(clusters, sms / 2);
         st.sm_count = sms;
         st.status = SWIGLU_OK;
     });
@@ -86,11 +128,69 @@ int device_setup(int *dev_out, DeviceState **st_out) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// SM count of the current device without the sm_103 check (for sizing only).
+int current_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return kAssumedMaxSms;
+    }
+    return sms;
+}
+
+// Schedule of one call. `workers` = CTAs (1-SM kernel) or CTA pairs (2-SM
+// kernel) that run at once; a 2-SM tile has 256 rows.
+WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, bool pair) {
+    const int rows = pair ? PairC::UMMA_M : FusedC::BM;
+    const int m_tiles = static_cast<int>((M + rows - 1) / rows);
+    const int n_tiles = static_cast<int>((N + FusedC::BN - 1) / FusedC::BN);
+    const int k_blocks = static_cast<int>((K + FusedC::BK - 1) / FusedC::BK);
+    return plan_schedule(m_tiles, n_tiles, k_blocks, workers, pair ? kGroupM / 2 : kGroupM,
+                         kMinStreamKIters);
+}
+
+// Workspace layout: a counter region at offset 0 whose size depends only on
+// the device (so a counter never lands where another shape's call left
+// partial sums), then the partial slots. Every stream-K tile needs at most
+// one counter per CTA half, and there are fewer than 2 * grid stream-K
+// tiles, so 4 * sm_count counters always suffice.
+size_t counter_region_bytes(int sm_count) {
+    return (static_cast<size_t>(4) * sm_count * sizeof(unsigned int) + 255) / 256 * 256;
+}
+// Partial slots: 2 per worker (its first and last stream-K tile), and for
+// the 2-SM kernel one per CTA of the pair.
+size_t workspace_partials_bytes(const WorkSched &s, int64_t M, bool pair) {
+    return s.sk_iters > 0 ? static_cast<size_t>(2) * s.grid * (pair ? 2 : 1) * kSlotCols *
+                                slot_rows_for(M) * sizeof(float)
+                          : 0;
+}
+size_t workspace_bytes_for(const WorkSched &s, int64_t M, bool pair, int sm_count) {
+    if (s.sk_iters == 0) return 0;
+    return counter_region_bytes(sm_count) + workspace_partials_bytes(s, M, pair);
+}
+
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
     return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// Tensor map over the tile-contiguous packed weights [tiles][256][64]: a box
+// is box_rows x 64 of one tile (the whole 32 KB tile for the 1-SM kernel, the
+// Gate or the Up half for one CTA of a pair), 128-byte swizzled.
+bool encode_packed_weights(CUtensorMap *m, const void *base, uint64_t tiles, uint32_t box_rows) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {64, 256, tiles};
+    const cuuint64_t strides[2] = {64 * 2, 256 * 64 * 2};
+    const cuuint32_t box[3] = {64, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D BF16 tensor map over a row-major [rows, cols] matrix with a
@@ -131,7 +231,7 @@ const char *swiglu_status_string(int status) {
 
 size_t swiglu_packed_weight_bytes(int64_t N, int64_t K) {
     if (N <= 0 || K <= 0) return 0;
-    return static_cast<size_t>(2 * round_up(N, 128)) * static_cast<size_t>(K) * 2u;
+    return static_cast<size_t>(2 * round_up(N, 128)) * static_cast<size_t>(round_up(K, 64)) * 2u;
 }
 
 int swiglu_pack_weights(const void *W1, const void *W2, int64_t K, int64_t N, void *Wpacked,
@@ -145,50 +245,76 @@ int swiglu_pack_weights(const void *W1, const void *W2, int64_t K, int64_t N, vo
     if (overlaps(Wpacked, pbytes, W1, wbytes) || overlaps(Wpacked, pbytes, W2, wbytes))
         return SWIGLU_ERR_INVALID_ARG;
     const int64_t rows = 2 * round_up(N, 128);
+    const int64_t kblocks = (K + kPackTile - 1) / kPackTile;
     if (rows / kPackTile > 65535) return SWIGLU_ERR_UNSUPPORTED;
     int dev;
     DeviceState *st;
     const int s = device_setup(&dev, &st);
     if (s != SWIGLU_OK) return s;
-    const dim3 grid(static_cast<unsigned>((K + kPackTile - 1) / kPackTile),
-                    static_cast<unsigned>(rows / kPackTile));
+    const dim3 grid(static_cast<unsigned>(kblocks), static_cast<unsigned>(rows / kPackTile));
     pack_weights_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t *>(W1), static_cast<const uint16_t *>(W2),
-        static_cast<uint16_t *>(Wpacked), static_cast<int>(K), static_cast<int>(N));
+        static_cast<uint16_t *>(Wpacked), static_cast<int>(K), static_cast<int>(N),
+        static_cast<int>(kblocks));
     if (cudaGetLastError() != cudaSuccess) return SWIGLU_ERR_CUDA;
     return SWIGLU_OK;
 }
 
 size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    (void)M;
-    (void)N;
-    (void)K;
-    return 0;
+    if (M < 1 || N < 1 || K < 1 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
+        K >= (int64_t(1) << 31))
+        return 0;
+    const bool pair = use_pair_kernel(M);
+    int dev;
+    DeviceState *st;
+    if (device_setup(&dev, &st) == SWIGLU_OK)  // the same plan swiglu_up_forward will use
+        return workspace_bytes_for(plan_for(M, N, K, pair ? st->pair_clusters : st->sm_count, pair),
+                                   M, pair, st->sm_count);
+    const int sms = current_sm_count();         // no usable device: a size for its SM count
+    return workspace_bytes_for(plan_for(M, N, K, pair ? sms / 2 : sms, pair), M, pair, sms);
 }
 
 int swiglu_up_forward(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t N,
                       int64_t K, void *workspace, size_t workspace_bytes, void *stream) {
-    (void)workspace;
     if (!A || !Wpacked || !Y) return SWIGLU_ERR_INVALID_ARG;
     if (M < 1 || N < 8 || K < 8 || (N % 8) != 0 || (K % 8) != 0) return SWIGLU_ERR_INVALID_ARG;
     const int64_t lim = int64_t(1) << 31;
     if (M >= lim || N >= lim || K >= lim) return SWIGLU_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(Wpacked) || !aligned16(Y)) return SWIGLU_ERR_INVALID_ARG;
-    if (workspace_bytes < swiglu_workspace_bytes(M, N, K)) return SWIGLU_ERR_INVALID_ARG;
     const size_t ybytes = static_cast<size_t>(M) * N * 2;
     if (overlaps(Y, ybytes, A, static_cast<size_t>(M) * K * 2) ||
         overlaps(Y, ybytes, Wpacked, swiglu_packed_weight_bytes(N, K)))
         return SWIGLU_ERR_INVALID_ARG;
+    const int64_t tiles = ((M + FusedC::BM - 1) / FusedC::BM) * ((N + FusedC::BN - 1) / FusedC::BN);
+    if (tiles >= lim) return SWIGLU_ERR_UNSUPPORTED;
 
     int dev;
     DeviceState *st;
     const int s = device_setup(&dev, &st);
     if (s != SWIGLU_OK) return s;
 
-    const int64_t n_pad = round_up(N, 128);
+    const bool pair = use_pair_kernel(M);
+    const WorkSched sched = plan_for(M, N, K, pair ? st->pair_clusters : st->sm_count, pair);
+    const size_t ws_need = workspace_bytes_for(sched, M, pair, st->sm_count);
+    if (ws_need > 0) {
+        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+            workspace_bytes < ws_need)
+            return SWIGLU_ERR_INVALID_ARG;
+        if (overlaps(workspace, ws_need, Y, ybytes) ||
+            overlaps(workspace, ws_need, A, static_cast<size_t>(M) * K * 2) ||
+            overlaps(workspace, ws_need, Wpacked, swiglu_packed_weight_bytes(N, K)))
+            return SWIGLU_ERR_INVALID_ARG;
+    }
+
+    // A box: 128 rows, or ceil(M/8)*8 when the whole problem has fewer rows
+    // (1-SM kernel only; a pair tile always loads 128 rows per CTA)
+    const int a_rows =
+        (pair || M >= FusedC::BM) ? FusedC::BM : static_cast<int>(round_up(M, 8));
+    const uint64_t weight_tiles =
+        static_cast<uint64_t>(sched.order.n_tiles) * static_cast<uint64_t>(sched.k_blocks);
     CUtensorMap tmA, tmB, tmY;
-    if (!encode_bf16_2d(&tmA, A, K, M, FusedC::BK, FusedC::BM) ||
-        !encode_bf16_2d(&tmB, Wpacked, K, 2 * n_pad, FusedC::BK, FusedC::UMMA_N) ||
+    if (!encode_bf16_2d(&tmA, A, K, M, FusedC::BK, a_rows) ||
+        !encode_packed_weights(&tmB, Wpacked, weight_tiles, pair ? 128u : 256u) ||
         !encode_bf16_2d(&tmY, Y, N, M, 64, 32))
         return SWIGLU_ERR_CUDA;
 
@@ -196,17 +322,37 @@ int swiglu_up_forward(const void *A, const void *Wpacked, void *Y, int64_t M, in
     args.M = static_cast<int>(M);
     args.N = static_cast<int>(N);
     args.K = static_cast<int>(K);
-    args.k_blocks = static_cast<int>((K + FusedC::BK - 1) / FusedC::BK);
-    args.order.m_tiles = static_cast<int>((M + FusedC::BM - 1) / FusedC::BM);
-    args.order.n_tiles = static_cast<int>(n_pad / FusedC::BN);
-    args.order.group_m = std::min(16, args.order.m_tiles);
-    const int64_t tiles = int64_t(args.order.m_tiles) * args.order.n_tiles;
-    if (tiles >= lim) return SWIGLU_ERR_UNSUPPORTED;
-    args.num_tiles = static_cast<int>(tiles);
+    args.stage_tx_bytes = a_rows * FusedC::BK * 2 + FusedC::B_BYTES;
+    args.slot_rows = slot_rows_for(M);
+    args.sched = sched;
+    args.counters = ws_need ? static_cast<unsigned int *>(workspace) : nullptr;
+    args.partials = ws_need ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                        counter_region_bytes(st->sm_count))
+                            : nullptr;
 
-    const int grid = static_cast<int>(std::min<int64_t>(tiles, st->sm_count));
-    fused_up_kernel<kFusedStages><<<grid, FusedC::THREADS, FusedC::SMEM_BYTES,
-                                     static_cast<cudaStream_t>(stream)>>>(tmA, tmB, tmY, args);
+    cudaStream_t s_ = static_cast<cudaStream_t>(stream);
+    if (pair) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * sched.grid));
+        cfg.blockDim = dim3(PairC::THREADS);
+        cfg.dynamicSmemBytes = PairC::SMEM_BYTES;
+        cfg.stream = s_;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages>, tmA, tmB, tmY, args) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return SWIGLU_ERR_CUDA;
+        }
+        return SWIGLU_OK;
+    }
+    fused_up_kernel<kFusedStages><<<sched.grid, FusedC::THREADS, FusedC::SMEM_BYTES, s_>>>(
+        tmA, tmB, tmY, args);
     if (cudaGetLastError() != cudaSuccess) return SWIGLU_ERR_CUDA;
     return SWIGLU_OK;
 }

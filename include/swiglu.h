@@ -56,11 +56,12 @@ const char *swiglu_status_string(int status);
  *
  * Packed layout (this library's own; the pages' Kernel-2 interleaves W1 and
  * W2 column by column into one K x 2N operand, technical summary
- * "Kernel-2", and this is the same idea in the blocked, K-major form the
- * tensor cores consume): a row-major [2*Np, K] BF16 matrix, Np = N rounded up
- * to a multiple of 128. Rows come in blocks of 256: rows 256j..256j+127 hold
- * W1[:, 128j..128j+127] transposed (Gate), rows 256j+128..256j+255 hold
- * W2[:, 128j..128j+127] transposed (Up). Rows for columns n >= N are zero.
+ * "Kernel-2", and this is the same idea in the tiled, K-major form the
+ * tensor cores consume): BF16 [NB][KB][256][64], NB = ceil(N/128),
+ * KB = ceil(K/64). Tile (j, b) is one contiguous 32 KB block: its rows
+ * 0..127 are W1[64b..64b+63, 128j..128j+127] transposed (Gate), rows
+ * 128..255 the same columns of W2 (Up), each row 64 consecutive k values.
+ * Entries for columns n >= N or k >= K are zero. Size = 4 * NB*128 * KB*64.
  * Returns 0 if N <= 0 or K <= 0.
  */
 size_t swiglu_packed_weight_bytes(int64_t N, int64_t K);
@@ -78,8 +79,12 @@ int swiglu_pack_weights(const void *W1, const void *W2, int64_t K, int64_t N,
                         void *Wpacked, void *stream);
 
 /*
- * Bytes of device workspace that swiglu_up_forward needs for (M, N, K).
- * 0 means none: pass workspace = NULL, workspace_bytes = 0.
+ * Bytes of device workspace that swiglu_up_forward needs for (M, N, K) on
+ * the current device (the split of K over CTAs depends on its SM count).
+ * 0 means none: pass workspace = NULL, workspace_bytes = 0. The workspace
+ * holds FP32 Gate/Up partial tiles for tiles whose K range is split between
+ * CTAs (balancing the last wave of tiles, or all tiles when there are fewer
+ * tiles than SMs), plus one counter per such tile.
  */
 size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
@@ -89,7 +94,13 @@ size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   Wpacked  device, output of swiglu_pack_weights for this (N, K)
  *   Y        device, BF16, [M, N] row-major; fully overwritten
  *   workspace, workspace_bytes: device scratch of at least
- *            swiglu_workspace_bytes(M, N, K) bytes (may be NULL when that is 0)
+ *            swiglu_workspace_bytes(M, N, K) bytes, 256-byte aligned (may be
+ *            NULL when that is 0). It must be zero-filled before its first
+ *            use; every completed call leaves it ready for the next one
+ *            (its tile counters back at zero), whatever the shape. After a
+ *            SWIGLU_ERR_DEVICE_TIMEOUT, zero it again. Calls that run at the
+ *            same time on the GPU (different streams) need separate
+ *            workspaces.
  * Requirements: M >= 1, N >= 8, K >= 8, N % 8 == 0, K % 8 == 0 (16-byte row
  * strides), M, N, K < 2^31; A, Wpacked, Y 16-byte aligned; Y must not overlap
  * A, Wpacked or the workspace. M, N and K need not be multiples of any tile

@@ -113,13 +113,29 @@ def from_device_bf16(t) -> np.ndarray:
 
 def pack_reference(W1: np.ndarray, W2: np.ndarray) -> np.ndarray:
     """The library's packed-weight layout, written out with numpy slicing:
-    [2*Np, K], blocks of 256 rows = 128 Gate columns (W1 transposed) then 128
-    Up columns (W2 transposed); columns past N are zero rows."""
+    [NB][KB][256][64] with NB = ceil(N/128), KB = ceil(K/64); tile (j, b)
+    rows 0..127 = W1[64b:64b+64, 128j:128j+128] transposed (Gate), rows
+    128..255 = the same block of W2 (Up); zero outside N and K. Returned as
+    a flat uint16 array."""
     K, N = W1.shape
-    Np = -(-N // 128) * 128
-    P = np.zeros((2 * Np, K), dtype=np.uint16)
-    for j in range(Np // 128):
-        n0, n1 = 128 * j, min(N, 128 * j + 128)
-        P[256 * j:256 * j + (n1 - n0)] = W1[:, n0:n1].T
-        P[256 * j + 128:256 * j + 128 + (n1 - n0)] = W2[:, n0:n1].T
-    return P
+    NB, KB = -(-N // 128), -(-K // 64)
+    Np, Kp = NB * 128, KB * 64
+    w1 = np.zeros((Kp, Np), np.uint16)
+    w2 = np.zeros((Kp, Np), np.uint16)
+    w1[:K, :N] = W1
+    w2[:K, :N] = W2
+    P = np.zeros((NB, KB, 256, 64), np.uint16)
+    for j in range(NB):
+        for b in range(KB):
+            P[j, b, :128] = w1[64 * b:64 * b + 64, 128 * j:128 * j + 128].T
+            P[j, b, 128:] = w2[64 * b:64 * b + 64, 128 * j:128 * j + 128].T
+    return P.reshape(-1)
+
+
+def unpack_reference(P: np.ndarray, K: int, N: int):
+    """Inverse of pack_reference: (W1, W2) from the flat packed array."""
+    NB, KB = -(-N // 128), -(-K // 64)
+    T = P.reshape(NB, KB, 256, 64)
+    w1 = T[:, :, :128, :].transpose(1, 3, 0, 2).reshape(KB * 64, NB * 128)
+    w2 = T[:, :, 128:, :].transpose(1, 3, 0, 2).reshape(KB * 64, NB * 128)
+    return w1[:K, :N], w2[:K, :N]

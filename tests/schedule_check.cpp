@@ -2,7 +2,7 @@
 // with g++ by tests/test_schedule.py. For each (m_tiles, n_tiles, k_blocks,
 // sm_count) given on stdin it verifies that:
 //   * the units of all CTAs cover every (tile, k-block) exactly once;
-//   * data-parallel tiles are whole and evenly spread (same count per CTA);
+//   * data-parallel tiles are whole and spread round robin;
 //   * for every stream-K tile, the contributor range [sk_owner(first),
 //     sk_owner(last)] is exactly the set of CTAs that produced units for it,
 //     each contributor has one unit for it, and units arrive in k order;
@@ -34,9 +34,12 @@ int main() {
         const WorkSched s = plan_schedule(mt, nt, kb, sms, 16, min_iters);
         const int T = mt * nt;
         if (s.grid < 1 || s.grid > sms) { bad |= fail("grid", s.grid, sms); continue; }
-        if (s.dp_tiles % s.grid != 0) { bad |= fail("dp multiple", s.dp_tiles, s.grid); continue; }
+        if (s.sk_iters > 0 && s.dp_tiles % s.grid != 0) { bad |= fail("dp multiple", s.dp_tiles, s.grid); continue; }
+        if (s.sk_iters == 0 && s.dp_tiles != T) { bad |= fail("dp-only must cover all tiles", s.dp_tiles, T); continue; }
         if (s.sk_iters != (long long)(T - s.dp_tiles) * kb) { bad |= fail("sk_iters", T, s.dp_tiles); continue; }
         if (s.sk_iters > 0 && s.sk_iters < s.grid) { bad |= fail("sk < grid", (int)s.sk_iters, s.grid); continue; }
+        // the workspace counter region holds 2 counters per CTA-pair half: stream-K tiles < 2 * grid
+        if (s.sk_iters > 0 && T - s.dp_tiles >= 2 * s.grid) { bad |= fail("sk tiles >= 2*grid", T - s.dp_tiles, s.grid); continue; }
         std::vector<int> cover((size_t)T * kb, 0);
         std::map<int, std::vector<std::pair<int, int>>> contrib;  // sk tile -> (cta, kb0)
         std::vector<long long> work(s.grid, 0);
@@ -65,7 +68,8 @@ int main() {
                 if (mb < 0 || mb >= mt || nb < 0 || nb >= nt) bad |= fail("coords", mb, nb);
                 coords_seen.insert((long long)mb * nt + nb);
             }
-            if (n_dp != s.dp_tiles / s.grid) bad |= fail("dp per cta", n_dp, c);
+            const int want_dp = s.dp_tiles / s.grid + (c < s.dp_tiles % s.grid ? 1 : 0);
+            if (n_dp != want_dp) bad |= fail("dp per cta", n_dp, c);
         }
         for (size_t i = 0; i < cover.size(); ++i)
             if (cover[i] != 1) { bad |= fail("coverage", (int)(i / kb), cover[i]); break; }
@@ -92,7 +96,14 @@ int main() {
         }
         long long wmin = work[0], wmax = work[0];
         for (long long w : work) { wmin = w < wmin ? w : wmin; wmax = w > wmax ? w : wmax; }
-        if (wmax - wmin > 1) bad |= fail("imbalance", (int)wmin, (int)wmax);
+        // stream-K: balanced to one k-block; data-parallel: to one whole tile,
+        // and then only when the grid is used at least 85% (the plan's threshold)
+        if (s.sk_iters > 0 && wmax - wmin > 1) bad |= fail("imbalance", (int)wmin, (int)wmax);
+        if (s.sk_iters == 0) {
+            if (wmax - wmin > kb) bad |= fail("dp imbalance", (int)wmin, (int)wmax);
+            const int waves = (T + sms - 1) / sms;
+            if (T < 0.85 * waves * sms) bad |= fail("dp chosen below threshold", T, waves * sms);
+        }
         std::printf("mt=%d nt=%d kb=%d sms=%d grid=%d dp=%d sk_iters=%lld split=%d max_contrib=%d work=[%lld,%lld]\n",
                     mt, nt, kb, sms, s.grid, s.dp_tiles, s.sk_iters, split_tiles, max_contrib, wmin, wmax);
     }

@@ -47,6 +47,12 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(_declared_functions()) <= set(sg.EXPORTED_SYMBOLS)
 
 
+def test_binding_has_every_abi_name():
+    import gemm_swiglu_mlp_gb300 as sg
+    for name in _declared_functions():
+        assert callable(getattr(sg, name, None)), name
+
+
 def test_status_strings_and_version(lib):
     import gemm_swiglu_mlp_gb300 as sg
     assert sg.swiglu_status_string(0) == "SWIGLU_OK"
@@ -59,6 +65,7 @@ def test_packed_weight_bytes(lib):
     import gemm_swiglu_mlp_gb300 as sg
     assert sg.swiglu_packed_weight_bytes(4864, 896) == 2 * 4864 * 896 * 2
     assert sg.swiglu_packed_weight_bytes(136, 64) == 2 * 256 * 64 * 2    # padded to 256 columns
+    assert sg.swiglu_packed_weight_bytes(128, 72) == 2 * 128 * 128 * 2   # K padded to 128
     assert sg.swiglu_packed_weight_bytes(0, 64) == 0
     assert sg.swiglu_packed_weight_bytes(8, -1) == 0
 
@@ -117,13 +124,22 @@ def test_binding_fails_loudly_when_library_missing(tmp_path):
 
 
 def test_pack_reference_layout_by_hand():
-    # K=2, N=3: packed has 2*128 rows; row r<3 is W1[:, r], row 128+r is W2[:, r]
+    # K=2, N=3: one tile [256][64]; row r<3 holds W1[:, r] in its first 2
+    # entries, row 128+r holds W2[:, r]; everything else is zero padding
     W1 = np.arange(6, dtype=np.uint16).reshape(2, 3)
     W2 = (100 + np.arange(6, dtype=np.uint16)).reshape(2, 3)
-    P_ = parity.pack_reference(W1, W2)
-    assert P_.shape == (256, 2)
-    assert P_[1].tolist() == [1, 4] and P_[129].tolist() == [101, 104]
-    assert not P_[3:128].any() and not P_[131:].any()
+    P_ = parity.pack_reference(W1, W2).reshape(256, 64)
+    assert P_[1, :2].tolist() == [1, 4] and P_[129, :2].tolist() == [101, 104]
+    assert not P_[:, 2:].any() and not P_[3:128].any() and not P_[131:].any()
+    # two k-blocks and two column blocks: element W1[70, 130] sits in tile
+    # (j=1, b=1), row 2, column 6
+    K, N = 72, 136
+    A1 = np.arange(K * N, dtype=np.uint16).reshape(K, N)
+    A2 = A1 + np.uint16(1)
+    T = parity.pack_reference(A1, A2).reshape(2, 2, 256, 64)
+    assert T[1, 1, 2, 6] == A1[70, 130] and T[1, 1, 130, 6] == A2[70, 130]
+    u1, u2 = parity.unpack_reference(T.reshape(-1), K, N)
+    assert np.array_equal(u1, A1) and np.array_equal(u2, A2)
 
 
 def test_parity_criteria_by_hand():

@@ -12,7 +12,7 @@ import pytest
 
 import workloads
 from tests.parity import (compare, fp32_accumulation_bound, from_device_bf16, pack_reference,
-                          to_device_bf16)
+                          to_device_bf16, unpack_reference)
 
 torch = pytest.importorskip("torch")
 
@@ -53,19 +53,18 @@ def assert_parity(got, want, label="", accum_bound=None):
     return r
 
 
-@pytest.mark.parametrize("K,N,seed", [(8, 8, 1), (64, 128, 2), (200, 264, 3), (896, 4864, 4)])
+@pytest.mark.parametrize("K,N,seed", [(8, 8, 1), (64, 128, 2), (200, 264, 3), (896, 4864, 4),
+                                        (72, 136, 5)])
 def test_pack_is_the_documented_permutation(sg, K, N, seed):
     _, W1, W2 = workloads.random_case(1, N, K, seed)
     Wp = sg.swiglu_pack_weights(to_device_bf16(W1, "cuda"), to_device_bf16(W2, "cuda"))
     torch.cuda.synchronize()
-    got = Wp.cpu().numpy().view(np.uint16).reshape(-1, K)
+    got = Wp.cpu().numpy().view(np.uint16).reshape(-1)
     want = pack_reference(W1, W2)
-    assert np.array_equal(got, want)
+    assert got.shape == want.shape and np.array_equal(got, want)
     # unpack(pack(W)) == W
-    Np = want.shape[0] // 2
-    blocks = got.reshape(Np // 128, 2, 128, K)
-    assert np.array_equal(blocks[:, 0].reshape(Np, K)[:N].T, W1)
-    assert np.array_equal(blocks[:, 1].reshape(Np, K)[:N].T, W2)
+    u1, u2 = unpack_reference(got, K, N)
+    assert np.array_equal(u1, W1) and np.array_equal(u2, W2)
 
 
 SMALL = [
@@ -75,16 +74,24 @@ SMALL = [
     (129, 256, 128),    # one row into a second row-tile
     (300, 392, 200),    # several tiles, ragged in every dimension
     (256, 1024, 1024),  # more tiles than a single wave of row-tiles
-    (128, 4864, 896),   # the Qwen-2.5-0.5B shape, checked in full
+    (128, 4864, 896),   # the Qwen-2.5-0.5B shape, checked in full (3-way split tiles)
+    (70, 520, 1000),    # K split across 2 CTAs per tile; ragged M leaves a dead warp
+    (33, 264, 2000),    # K split across 4 CTAs per tile; 33 rows
+    (1, 136, 4096),     # one token, long K split many ways
+    (2048, 392, 520),   # data-parallel tiles plus a stream-K tail
+    (513, 136, 72),     # one row into a third 256-row pair tile
 ]
 
 
+@pytest.mark.parametrize("variant", ["1sm", "2sm"])
 @pytest.mark.parametrize("M,N,K", SMALL)
-def test_forward_small_full_compare(sg, orc, M, N, K):
+def test_forward_small_full_compare(sg, orc, monkeypatch, variant, M, N, K):
+    # both kernels on every shape: the 1-SM kernel and the 2-SM (CTA pair) one
+    monkeypatch.setenv("SWIGLU_FUSED_VARIANT", variant)
     A, W1, W2 = workloads.random_case(M, N, K, seed=M * 7 + N * 3 + K)
     got, _ = run_fused(sg, A, W1, W2)
     want = orc.swiglu_up(A, W1, W2)["Y"]
-    assert_parity(got, want, (M, N, K))
+    assert_parity(got, want, (variant, M, N, K))
 
 
 def test_forward_saturating_inputs(sg, orc):
@@ -124,13 +131,27 @@ def test_rank_one_inputs(sg, orc):
     assert np.all(diff[same_sign] <= 1), r
 
 
-def test_deterministic_bitwise(sg):
+@pytest.mark.parametrize("variant", ["1sm", "2sm"])
+def test_deterministic_bitwise(sg, monkeypatch, variant):
+    monkeypatch.setenv("SWIGLU_FUSED_VARIANT", variant)
     A, W1, W2 = workloads.random_case(300, 392, 520, seed=9)
     Wp = sg.swiglu_pack_weights(to_device_bf16(W1, "cuda"), to_device_bf16(W2, "cuda"))
     Ad = to_device_bf16(A, "cuda")
     y1 = from_device_bf16(sg.swiglu_up_forward(Ad, Wp, 392))
     y2 = from_device_bf16(sg.swiglu_up_forward(Ad, Wp, 392))
     assert np.array_equal(y1, y2)
+
+
+def test_workspace_reused_across_shapes(sg, orc, monkeypatch):
+    # the default workspace is shared by all calls on a stream: counters must
+    # come back to zero after every call, whatever the split and the kernel
+    cases = [(70, 520, 1000, 21), (33, 264, 2000, 22), (128, 4864, 896, 23), (70, 520, 1000, 24),
+             (600, 392, 2000, 25), (70, 520, 1000, 26)]
+    for M, N, K, seed in cases:
+        monkeypatch.setenv("SWIGLU_FUSED_VARIANT", "2sm" if M >= 256 else "1sm")
+        A, W1, W2 = workloads.random_case(M, N, K, seed=seed)
+        got, _ = run_fused(sg, A, W1, W2)
+        assert_parity(got, orc.swiglu_up(A, W1, W2)["Y"], (M, N, K, seed))
 
 
 def test_output_rows_outside_m_untouched(sg):

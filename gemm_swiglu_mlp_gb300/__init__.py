@@ -30,7 +30,8 @@ from .build import LIB_PATH
 __all__ = [
     "SwigluError", "load_library", "swiglu_version", "swiglu_status_string",
     "swiglu_packed_weight_bytes", "swiglu_pack_weights", "swiglu_workspace_bytes",
-    "swiglu_up_forward", "swiglu_check_device_status", "EXPORTED_SYMBOLS",
+    "swiglu_up_forward", "swiglu_up_forward_noalloc", "swiglu_check_device_status",
+    "EXPORTED_SYMBOLS",
 ]
 
 SWIGLU_OK = 0
@@ -42,7 +43,7 @@ SWIGLU_ERR_DEVICE_TIMEOUT = 4
 EXPORTED_SYMBOLS = (
     "swiglu_version", "swiglu_status_string", "swiglu_packed_weight_bytes",
     "swiglu_pack_weights", "swiglu_workspace_bytes", "swiglu_up_forward",
-    "swiglu_check_device_status",
+    "swiglu_up_forward_noalloc", "swiglu_check_device_status",
 )
 
 _lock = threading.Lock()
@@ -80,6 +81,8 @@ def load_library(path: str = LIB_PATH):
         lib.swiglu_workspace_bytes.restype = sz
         lib.swiglu_up_forward.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
         lib.swiglu_up_forward.restype = ctypes.c_int
+        lib.swiglu_up_forward_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+        lib.swiglu_up_forward_noalloc.restype = ctypes.c_int
         lib.swiglu_check_device_status.argtypes = [vp, u32p]
         lib.swiglu_check_device_status.restype = ctypes.c_int
         _lib = lib
@@ -193,6 +196,24 @@ def _default_workspace(device, nbytes: int, stream) -> torch.Tensor:
             ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         _workspaces[key] = ws
     return ws
+
+
+def swiglu_up_forward_noalloc(A: torch.Tensor, Wpacked: torch.Tensor, N: int,
+                              Y: torch.Tensor, stream=None) -> torch.Tensor:
+    """The allocation-free forward: the caller passes Y; the library uses its
+    own fixed device scratch instead of a workspace (include/swiglu.h)."""
+    lib = load_library()
+    _require_bf16_cuda(A, "A")
+    _require_bf16_cuda(Y, "Y")
+    M, K = A.shape
+    N = int(N)
+    if tuple(Y.shape) != (M, N):
+        raise ValueError("Y must be [%d, %d]" % (M, N))
+    with torch.cuda.device(A.device):
+        _check(lib.swiglu_up_forward_noalloc(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(),
+                                             M, N, K, _stream_handle(stream)),
+               "swiglu_up_forward_noalloc")
+    return Y
 
 
 def swiglu_check_device_status(stream=None) -> int:

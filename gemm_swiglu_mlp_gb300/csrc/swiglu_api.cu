@@ -378,3 +378,64 @@ int swiglu_check_device_status(void *stream, uint32_t *raw_word) {
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// swiglu_up_forward_noalloc: the same forward for callers that cannot
+// allocate device memory (see include/swiglu.h). Its scratch is this
+// file-scope device array: every GPU that loads the library holds
+// SWIGLU_NOALLOC_SCRATCH_BYTES of it until the process exits. In host code
+// the name below is only a host-side stand-in for the array; the device
+// address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_swiglu_noalloc_scratch[SWIGLU_NOALLOC_SCRATCH_BYTES];
+
+namespace swiglu {
+namespace {
+
+struct NoAllocSetup {
+    std::once_flag once;
+    int status = SWIGLU_OK;
+    void *scratch = nullptr;  // device address of g_swiglu_noalloc_scratch
+};
+NoAllocSetup g_noalloc[kMaxDevices];
+
+}  // namespace
+}  // namespace swiglu
+
+extern "C" int swiglu_up_forward_noalloc(const void *A, const void *Wpacked, void *Y, int64_t M,
+                                         int64_t N, int64_t K, void *stream) {
+    if (!A || !Wpacked || !Y) return SWIGLU_ERR_INVALID_ARG;
+    if (M < 1 || N < 8 || K < 8 || (N % 8) != 0 || (K % 8) != 0) return SWIGLU_ERR_INVALID_ARG;
+    const int64_t lim = int64_t(1) << 31;
+    if (M >= lim || N >= lim || K >= lim) return SWIGLU_ERR_INVALID_ARG;
+    int dev;
+    DeviceState *st;
+    const int s = device_setup(&dev, &st);
+    if (s != SWIGLU_OK) return s;
+    // First call on this device (which is current): look up the array's
+    // device address.
+    NoAllocSetup &na = g_noalloc[dev];
+    std::call_once(na.once, [&na] {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_swiglu_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            na.status = SWIGLU_ERR_CUDA;
+            return;
+        }
+        na.scratch = p;
+        na.status = SWIGLU_OK;
+    });
+    if (na.status != SWIGLU_OK) return na.status;
+    const size_t need = swiglu_workspace_bytes(M, N, K);
+    if (need > SWIGLU_NOALLOC_SCRATCH_BYTES) return SWIGLU_ERR_UNSUPPORTED;
+    if (need > 0) {
+        // The array keeps whatever the previous call left: zero the tile
+        // counters (the only part that must start at zero) on this stream.
+        if (cudaMemsetAsync(na.scratch, 0, counter_region_bytes(st->sm_count),
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+            cudaGetLastError();
+            return SWIGLU_ERR_CUDA;
+        }
+    }
+    return swiglu_up_forward(A, Wpacked, Y, M, N, K, need ? na.scratch : nullptr,
+                             need ? static_cast<size_t>(SWIGLU_NOALLOC_SCRATCH_BYTES) : 0, stream);
+}

@@ -116,6 +116,45 @@ int swiglu_up_forward(const void *A, const void *Wpacked, void *Y,
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Scratch size of swiglu_up_forward_noalloc, fixed at build time: 32 MiB.
+ */
+#define SWIGLU_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * swiglu_up_forward for callers that cannot allocate device memory. (The
+ * paper has no counterpart; this is a property of this library's interface.)
+ * Some callers cannot provide the workspace that swiglu_up_forward may need:
+ * a runtime that plans all of its device memory when it starts and must not
+ * call cudaMalloc afterwards (cudaMalloc may synchronize the device and can
+ * fail once memory is fully committed), or a plugin interface that passes a
+ * kernel only its input and output buffers. This entry point takes the same
+ * A, Wpacked, Y, M, N, K and stream, and allocates nothing: it calls no
+ * cudaMalloc or cudaFree and no allocating library routine.
+ *
+ * Scratch: a device array inside the library of SWIGLU_NOALLOC_SCRATCH_BYTES
+ * (32 MiB), held by every GPU that loads the library until the process exits.
+ * Problems whose workspace (swiglu_workspace_bytes) is larger are rejected
+ * with SWIGLU_ERR_UNSUPPORTED before anything is launched; use
+ * swiglu_up_forward with a caller workspace for those. Problems that need no
+ * workspace never touch the array.
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * Each call that uses the array first clears its tile counters with an
+ * asynchronous memset on `stream`; the rest keeps the previous call's
+ * contents and is overwritten before it is read.
+ *
+ * All calls on one device share the one array: calls that overlap on the GPU
+ * (different streams running at the same time) race and may return wrong
+ * results. Serialize them (one stream, or events between streams).
+ * Results are bit-identical to swiglu_up_forward's for the same inputs.
+ * Errors: as swiglu_up_forward, plus SWIGLU_ERR_UNSUPPORTED for problems over
+ * the scratch size and SWIGLU_ERR_CUDA if the set-up or the memset fails.
+ */
+int swiglu_up_forward_noalloc(const void *A, const void *Wpacked, void *Y,
+                              int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the current device's status
  * word. Every wait inside the kernels is bounded (about a second); a kernel
  * that gives up sets a bit in the word, releases its tensor memory and

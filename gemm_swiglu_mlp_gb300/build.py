@@ -34,6 +34,18 @@ def nvcc_command(out_path: str, extra=()):
             "-Xptxas", "-v", *extra, "-o", out_path, *SOURCES]
 
 
+def build_fault_injection_library(out_path: str) -> str:
+    """Test-only build of the same sources with SWIGLU_TEST_FAULT_INJECTION:
+    adds swiglu_test_set_fault_injection() and shortens the wait limit. Never
+    used by the product binding; the failure-detection test loads it."""
+    proc = subprocess.run(nvcc_command(out_path, extra=("-DSWIGLU_TEST_FAULT_INJECTION",)),
+                          capture_output=True, text=True)
+    if proc.returncode != 0:
+        sys.stderr.write(proc.stdout + proc.stderr)
+        raise RuntimeError("nvcc failed building the fault-injection test library")
+    return out_path
+
+
 def up_to_date() -> bool:
     if not os.path.exists(LIB_PATH):
         return False

@@ -39,6 +39,9 @@ struct FusedArgs {
     WorkSched sched;
     float *partials;          // 2 * grid slots of kSlotCols * slot_rows floats (stream-K only)
     unsigned int *counters;   // one per stream-K tile, zero between launches
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+    int skip_first_fill;      // test build only: never fill the first pipeline stage
+#endif
 };
 
 __device__ __forceinline__ float silu_mul(float g, float u) {

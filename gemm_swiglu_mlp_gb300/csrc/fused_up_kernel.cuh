@@ -122,6 +122,10 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // The prologue above touched no global memory: the next launch may start
+    // now, and this one waits here for the previous launch's results.
+    griddep_launch_dependents();
+    griddep_wait();
     const WorkSched &sched = args.sched;
 
     // Producer bookkeeping kept for the drain after an abort: which stages
@@ -144,6 +148,17 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                         ok = false;
                         break;
                     }
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+                    // test build: leave the very first stage unfilled, so the
+                    // MMA warp's wait for it runs out (failure-detection test)
+                    if (args.skip_first_fill && kb == u.kb0 && stage == 0 && phase == 0) {
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
+#endif
                     mbar_arrive_expect_tx(full_bar(stage), args.stage_tx_bytes);
                     tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
                                 kb * C::BK, mb * C::BM);

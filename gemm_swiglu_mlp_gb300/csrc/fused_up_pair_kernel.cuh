@@ -120,6 +120,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // The prologue above touched no global memory: the next launch may start
+    // now, and this one waits here for the previous launch's results.
+    griddep_launch_dependents();
+    griddep_wait();
     const WorkSched &sched = args.sched;
 
     uint32_t issued_mask = 0, last_parity = 0;  // leader's drain bookkeeping
@@ -140,6 +144,18 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                         ok = false;
                         break;
                     }
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+                    // test build: the leader never arms or fills the first
+                    // stage, so the MMA wait for it runs out
+                    if (args.skip_first_fill && is_leader && kb == u.kb0 && stage == 0 &&
+                        phase == 0) {
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
+#endif
                     // every load of the pair completes on the LEADER's full barrier
                     if (is_leader) mbar_arrive_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
                     const uint32_t bar = mapa_shared(full_bar(stage), 0);

@@ -9,8 +9,13 @@
 namespace swiglu {
 
 // Upper bound on one wait, in SM clock cycles (~1 s at 1.9-2.1 GHz). A wait
-// that runs out reports failure instead of spinning forever.
+// that runs out reports failure instead of spinning forever. The test-only
+// fault-injection build uses ~10 ms so that its timeout test is quick.
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+constexpr long long kWaitLimitCycles = 20000000LL;
+#else
 constexpr long long kWaitLimitCycles = 2000000000LL;
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -58,6 +63,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitLimitCycles) return false;
     }
+}
+
+// ---------------------------------------------------------------- launch overlap
+// Programmatic dependent launch: let the next kernel in the stream be
+// scheduled (its CTAs start as this grid's CTAs exit and run their prologue)
+// ...
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// ... and, before touching global memory, wait until the previous kernel in
+// the stream has completed and its writes are visible. Both are no-ops when
+// the launch did not opt in.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- clusters

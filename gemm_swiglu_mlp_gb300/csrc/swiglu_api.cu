@@ -27,6 +27,10 @@ constexpr int64_t kPairMinM = 256;   // from this many tokens on, the 2-SM kerne
 using FusedC = FusedCfg<kFusedStages>;
 using PairC = PairCfg<kPairStages>;
 
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+int g_test_skip_first_fill = 0;  // set by swiglu_test_set_fault_injection
+#endif
+
 // Which kernel serves a call: the 2-SM (CTA pair) kernel for M >= 256, the
 // 1-SM kernel below. SWIGLU_FUSED_VARIANT=1sm|2sm overrides the choice (for
 // ablations and tests); it is read on every call.
@@ -216,6 +220,15 @@ using namespace swiglu;
 
 extern "C" {
 
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+// Exists only in the test-only fault-injection build (never in the product
+// library): makes the following launches leave their first pipeline stage
+// unfilled, so a bounded wait runs out and the timeout path can be tested.
+void swiglu_test_set_fault_injection(int skip_first_fill) {
+    swiglu::g_test_skip_first_fill = skip_first_fill;
+}
+#endif
+
 int swiglu_version(void) { return (0 << 16) | 1; }
 
 const char *swiglu_status_string(int status) {
@@ -325,35 +338,46 @@ int swiglu_up_forward(const void *A, const void *Wpacked, void *Y, int64_t M, in
     args.stage_tx_bytes = a_rows * FusedC::BK * 2 + FusedC::B_BYTES;
     args.slot_rows = slot_rows_for(M);
     args.sched = sched;
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+    args.skip_first_fill = g_test_skip_first_fill;
+#endif
     args.counters = ws_need ? static_cast<unsigned int *>(workspace) : nullptr;
     args.partials = ws_need ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                                         counter_region_bytes(st->sm_count))
                             : nullptr;
 
-    cudaStream_t s_ = static_cast<cudaStream_t>(stream);
+    // Both kernels are launched with programmatic stream serialization: a
+    // launch may begin while the previous kernel in the stream finishes; the
+    // kernel waits (griddepcontrol.wait) before it reads or writes global
+    // memory, so stream order is kept for every buffer.
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cudaError_t err;
     if (pair) {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
         cfg.gridDim = dim3(static_cast<unsigned>(2 * sched.grid));
         cfg.blockDim = dim3(PairC::THREADS);
         cfg.dynamicSmemBytes = PairC::SMEM_BYTES;
-        cfg.stream = s_;
-        cfg.attrs = attr;
+        err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages>, tmA, tmB, tmY, args);
+    } else {
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages>, tmA, tmB, tmY, args) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return SWIGLU_ERR_CUDA;
-        }
-        return SWIGLU_OK;
+        cfg.gridDim = dim3(static_cast<unsigned>(sched.grid));
+        cfg.blockDim = dim3(FusedC::THREADS);
+        cfg.dynamicSmemBytes = FusedC::SMEM_BYTES;
+        err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kFusedStages>, tmA, tmB, tmY, args);
     }
-    fused_up_kernel<kFusedStages><<<sched.grid, FusedC::THREADS, FusedC::SMEM_BYTES, s_>>>(
-        tmA, tmB, tmY, args);
-    if (cudaGetLastError() != cudaSuccess) return SWIGLU_ERR_CUDA;
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SWIGLU_ERR_CUDA;
+    }
     return SWIGLU_OK;
 }
 

@@ -288,6 +288,73 @@ def time_unfused_context(w, W1, W2, As, Ys, R, dev, stream, steps, fused_value):
                     "in BF16), then silu(Gate) * Up in BF16; same rotating inputs"}
 
 
+def time_mlp_context(w, W1, W2, sg, As, Wps, Ys, Wss, R, dev, stream, steps):
+    """Context for the pages' Figure 1 ("Tile-Level Activation Overlap for
+    Efficient LLM Inference", Section 1: SwiGLU and its intermediates as a
+    share of MLP time): the whole gated MLP out = Y W3 with a synthetic
+    down-projection W3 [N, K]. Fused: this library's up-projection, then
+    torch.matmul (cuBLAS) for the down-projection. Eager: three cuBLAS GEMMs
+    and silu * mul, each also timed alone for the activation's share."""
+    import numpy as np
+    import torch
+    import torch.nn.functional as F
+
+    import workloads
+    w3 = torch.from_numpy(workloads.make_W3(w).view(np.int16)).view(torch.bfloat16).to(dev)
+    w1 = torch.from_numpy(W1.view(np.int16)).view(torch.bfloat16).to(dev)
+    w2 = torch.from_numpy(W2.view(np.int16)).view(torch.bfloat16).to(dev)
+    W1s = [w1] + [w1.clone() for _ in range(R - 1)]
+    W2s = [w2] + [w2.clone() for _ in range(R - 1)]
+    W3s = [w3] + [w3.clone() for _ in range(R - 1)]
+    G = [torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    U = [torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    O = [torch.empty(w.M, w.K, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                fn(i)
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(steps):
+                fn(i)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps  # ms
+
+    ops = {
+        "gate_gemm": lambda i: torch.matmul(As[i % R], W1s[i % R], out=G[i % R]),
+        "up_gemm": lambda i: torch.matmul(As[i % R], W2s[i % R], out=U[i % R]),
+        "silu_mul": lambda i: torch.mul(F.silu(G[i % R]), U[i % R], out=Ys[i % R]),
+        "down_gemm": lambda i: torch.matmul(Ys[i % R], W3s[i % R], out=O[i % R]),
+    }
+    op_ms = {k: timed(f) for k, f in ops.items()}
+
+    def eager(i):
+        for f in ops.values():
+            f(i)
+
+    def fused(i):
+        j = i % R
+        sg.swiglu_up_forward(As[j], Wps[j], w.N, Y=Ys[j], workspace=Wss[j], stream=stream)
+        torch.matmul(Ys[j], W3s[j], out=O[j])
+
+    eager_ms = timed(eager)
+    fused_ms = timed(fused)
+    mlp_flops = w.flops + 2 * w.M * w.N * w.K
+    del W1s, W2s, W3s, G, U, O
+    return {"eager_mlp_ms": eager_ms, "fused_mlp_ms": fused_ms,
+            "mlp_speedup": eager_ms / fused_ms,
+            "fused_mlp_tflops": mlp_flops / (fused_ms * 1e-3) / 1e12,
+            "eager_op_ms": op_ms,
+            "activation_share_of_eager_mlp": op_ms["silu_mul"] / sum(op_ms.values()),
+            "what": "out = (SiLU(A W1) * (A W2)) W3, W3 [N, K] ~ N(0, 1/N) synthetic; fused = this "
+                    "library's up-projection + cuBLAS down-projection; eager = 3 cuBLAS GEMMs + "
+                    "silu*mul (Figure 1 of the pages measures this share on H100)"}
+
+
 def config_of(w, l2_note):
     c = {"workload": "%s: M=%d tokens, K=%d, N=%d, A~N(0,1), W1/W2~N(0,1/K), BF16 in/out, FP32 accumulate"
                      % (w.name, w.M, w.K, w.N),
@@ -427,9 +494,10 @@ def run_gb300(args, w):
     if not torch.equal(y_check.to(dev), Ys[(Ke - 1) % R]):
         raise RuntimeError("e2e loop: copied-out Y differs from the device result")
 
-    unfused = None
+    unfused = mlp = None
     if not args.no_context:
         unfused = time_unfused_context(w, W1, W2, As, Ys, R, dev, stream, min(K, 2000), value)
+        mlp = time_mlp_context(w, W1, W2, sg, As, Wps, Ys, Wss, R, dev, stream, min(K, 500))
 
     if rank != 0:
         if world > 1:
@@ -468,6 +536,8 @@ def run_gb300(args, w):
     }
     if unfused is not None:
         line["context_unfused_torch"] = unfused
+    if mlp is not None:
+        line["context_mlp"] = mlp
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, A, W1, W2)
     print(json.dumps(line), flush=True)

@@ -9,6 +9,7 @@ The names follow the C ABI:
 
     swiglu_packed_weight_bytes(N, K) -> int
     swiglu_pack_weights(W1, W2, Wpacked=None) -> Wpacked (uint8 tensor)
+    swiglu_pack_weights_nk(W1, W2, Wpacked=None) -> Wpacked  (nn.Linear [N, K] weights)
     swiglu_workspace_bytes(M, N, K) -> int
     swiglu_up_forward(A, Wpacked, N, Y=None, workspace=None) -> Y
     swiglu_check_device_status() -> raw status word (raises on timeout)
@@ -29,7 +30,8 @@ from .build import LIB_PATH
 
 __all__ = [
     "SwigluError", "load_library", "swiglu_version", "swiglu_status_string",
-    "swiglu_packed_weight_bytes", "swiglu_pack_weights", "swiglu_workspace_bytes",
+    "swiglu_packed_weight_bytes", "swiglu_pack_weights", "swiglu_pack_weights_nk",
+    "swiglu_workspace_bytes",
     "swiglu_up_forward", "swiglu_up_forward_noalloc", "swiglu_check_device_status",
     "EXPORTED_SYMBOLS",
 ]
@@ -42,13 +44,14 @@ SWIGLU_ERR_DEVICE_TIMEOUT = 4
 
 EXPORTED_SYMBOLS = (
     "swiglu_version", "swiglu_status_string", "swiglu_packed_weight_bytes",
-    "swiglu_pack_weights", "swiglu_workspace_bytes", "swiglu_up_forward",
-    "swiglu_up_forward_noalloc", "swiglu_check_device_status",
+    "swiglu_pack_weights", "swiglu_pack_weights_nk", "swiglu_workspace_bytes",
+    "swiglu_up_forward", "swiglu_up_forward_noalloc", "swiglu_check_device_status",
 )
 
 _lock = threading.Lock()
 _lib = None
 _workspaces = {}   # (device index, stream handle) -> zero-initialised uint8 tensor
+_ws_bytes = {}     # (device index, M, N, K, kernel override) -> workspace bytes
 
 
 class SwigluError(RuntimeError):
@@ -77,6 +80,8 @@ def load_library(path: str = LIB_PATH):
         lib.swiglu_packed_weight_bytes.restype = sz
         lib.swiglu_pack_weights.argtypes = [vp, vp, i64, i64, vp, vp]
         lib.swiglu_pack_weights.restype = ctypes.c_int
+        lib.swiglu_pack_weights_nk.argtypes = [vp, vp, i64, i64, vp, vp]
+        lib.swiglu_pack_weights_nk.restype = ctypes.c_int
         lib.swiglu_workspace_bytes.argtypes = [i64, i64, i64]
         lib.swiglu_workspace_bytes.restype = sz
         lib.swiglu_up_forward.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
@@ -151,6 +156,26 @@ def swiglu_pack_weights(W1: torch.Tensor, W2: torch.Tensor, Wpacked: torch.Tenso
     return Wpacked
 
 
+def swiglu_pack_weights_nk(W1: torch.Tensor, W2: torch.Tensor, Wpacked: torch.Tensor = None,
+                           stream=None) -> torch.Tensor:
+    """Pack nn.Linear-layout weights W1, W2 ([N, K] BF16 each, Gate = A W1^T)."""
+    lib = load_library()
+    _require_bf16_cuda(W1, "W1")
+    _require_bf16_cuda(W2, "W2")
+    if W1.dim() != 2 or W1.shape != W2.shape:
+        raise ValueError("W1 and W2 must both be [N, K]")
+    N, K = W1.shape
+    nbytes = swiglu_packed_weight_bytes(N, K)
+    if Wpacked is None:
+        Wpacked = torch.empty(nbytes, dtype=torch.uint8, device=W1.device)
+    elif Wpacked.numel() * Wpacked.element_size() < nbytes or not Wpacked.is_contiguous():
+        raise ValueError("Wpacked must be contiguous with at least %d bytes" % nbytes)
+    with torch.cuda.device(W1.device):
+        _check(lib.swiglu_pack_weights_nk(W1.data_ptr(), W2.data_ptr(), N, K, Wpacked.data_ptr(),
+                                          _stream_handle(stream)), "swiglu_pack_weights_nk")
+    return Wpacked
+
+
 def swiglu_up_forward(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: torch.Tensor = None,
                       workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
     """Y[M, N] = SiLU(A x W1) (.) (A x W2) from A [M, K] BF16 and packed weights."""
@@ -169,8 +194,16 @@ def swiglu_up_forward(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: torch.T
         _require_bf16_cuda(Y, "Y")
         if tuple(Y.shape) != (M, N):
             raise ValueError("Y must be [%d, %d]" % (M, N))
-    with torch.cuda.device(A.device):
-        ws_need = swiglu_workspace_bytes(M, N, K)
+    dev = A.device.index
+    switch = dev != torch.cuda.current_device()
+    if switch:
+        prev = torch.cuda.current_device()
+        torch.cuda.set_device(dev)
+    try:
+        key = (dev, M, N, K, os.environ.get("SWIGLU_FUSED_VARIANT"))
+        ws_need = _ws_bytes.get(key)
+        if ws_need is None:
+            ws_need = _ws_bytes[key] = swiglu_workspace_bytes(M, N, K)
         ws_ptr, ws_bytes = None, 0
         if ws_need:
             if workspace is None:
@@ -179,6 +212,9 @@ def swiglu_up_forward(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: torch.T
         _check(lib.swiglu_up_forward(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(), M, N, K,
                                      ws_ptr, ws_bytes, _stream_handle(stream)),
                "swiglu_up_forward")
+    finally:
+        if switch:
+            torch.cuda.set_device(prev)
     return Y
 
 

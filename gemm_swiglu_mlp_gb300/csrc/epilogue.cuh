@@ -35,6 +35,8 @@ __host__ __device__ __forceinline__ int slot_rows_for(long long M) {
 struct FusedArgs {
     int M, N, K;
     int stage_tx_bytes;       // bytes one stage's TMA loads deliver (A box + weight tile)
+    int a_tx_bytes;           // the A box's share of it
+    uint16_t *Y;              // Y [M, N] row-major BF16 (direct stores of column sub-tiles)
     int slot_rows;            // rows per workspace slot
     WorkSched sched;
     float *partials;          // 2 * grid slots of kSlotCols * slot_rows floats (stream-K only)
@@ -104,10 +106,13 @@ __device__ __forceinline__ void stage_y32(uint32_t ybuf, int lane, int c, const 
     }
 }
 
-__device__ __forceinline__ void tmem_ld_gu(uint32_t tbase, int c, float (&g)[32], float (&u)[32]) {
+// Gate columns [c, c+32) and the matching Up columns (up_off columns further
+// on: 128 for a whole tile, the sub-tile width for a column sub-tile).
+__device__ __forceinline__ void tmem_ld_gu(uint32_t tbase, int c, float (&g)[32], float (&u)[32],
+                                           int up_off = 128) {
     uint32_t gr[32], ur[32];
     tmem_ld_32x32b_x32(tbase + c, gr);
-    tmem_ld_32x32b_x32(tbase + 128 + c, ur);
+    tmem_ld_32x32b_x32(tbase + up_off + c, ur);
     tmem_ld_wait();
     reg_fence32(gr);
     reg_fence32(ur);
@@ -115,6 +120,33 @@ __device__ __forceinline__ void tmem_ld_gu(uint32_t tbase, int c, float (&g)[32]
     for (int i = 0; i < 32; ++i) {
         g[i] = __uint_as_float(gr[i]);
         u[i] = __uint_as_float(ur[i]);
+    }
+}
+
+// Epilogue of a column sub-tile (width 64 or 32): TMEM holds Gate in columns
+// [0, width) and Up in [width, 2*width). Each thread owns one output row and
+// stores its `width` outputs straight to global memory in 16-byte pieces
+// (rows >= M and columns >= N are skipped; N is a multiple of 8, so a piece
+// is either wholly inside or wholly outside).
+__device__ __forceinline__ void epilogue_subtile_store(uint32_t tbase, int width, int row,
+                                                       int col0, const FusedArgs &args) {
+    for (int c = 0; c < width; c += 32) {
+        float g[32], v[32];
+        tmem_ld_gu(tbase, c, g, v, width);
+        if (row < args.M) {
+            uint16_t *dst = args.Y + static_cast<size_t>(row) * args.N + col0 + c;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (col0 + c + 8 * j >= args.N) break;
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = 8 * j + 2 * e;
+                    w[e] = pack_bf16x2(silu_mul(g[i], v[i]), silu_mul(g[i + 1], v[i + 1]));
+                }
+                *reinterpret_cast<uint4 *>(dst + 8 * j) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
     }
 }
 

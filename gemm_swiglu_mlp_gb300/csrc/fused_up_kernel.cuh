@@ -77,6 +77,8 @@ template <int STAGES>
 __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
     fused_up_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmB64,
+                    const __grid_constant__ CUtensorMap tmB32,
                     const __grid_constant__ CUtensorMap tmY, const FusedArgs args) {
     using C = FusedCfg<STAGES>;
     extern __shared__ uint8_t smem_raw[];
@@ -159,11 +161,24 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                         continue;
                     }
 #endif
-                    mbar_arrive_expect_tx(full_bar(stage), args.stage_tx_bytes);
-                    tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
-                                kb * C::BK, mb * C::BM);
-                    tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, full_bar(stage), 0, 0,
-                                nb * sched.k_blocks + kb);
+                    const uint32_t b_dst = sbase + C::OFF_B + stage * C::B_BYTES;
+                    const int wtile = nb * sched.k_blocks + kb;
+                    if (u.width == C::BN) {
+                        mbar_arrive_expect_tx(full_bar(stage), args.stage_tx_bytes);
+                        tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
+                                    kb * C::BK, mb * C::BM);
+                        tma_load_3d(b_dst, &tmB, full_bar(stage), 0, 0, wtile);
+                    } else {
+                        // column sub-tile: its Gate rows, then the matching Up rows
+                        const CUtensorMap *tmBn = (u.width == 64) ? &tmB64 : &tmB32;
+                        mbar_arrive_expect_tx(full_bar(stage),
+                                              args.a_tx_bytes + 2 * u.width * C::BK * 2);
+                        tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
+                                    kb * C::BK, mb * C::BM);
+                        tma_load_3d(b_dst, tmBn, full_bar(stage), 0, u.sub * u.width, wtile);
+                        tma_load_3d(b_dst + u.width * C::BK * 2, tmBn, full_bar(stage), 0,
+                                    C::BN + u.sub * u.width, wtile);
+                    }
                     issued_mask |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -195,6 +210,9 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::UMMA_N);
+                // Gate|Up columns of this unit: 256, or 2 x the sub-tile width
+                const uint32_t idesc_u =
+                    (u.width == C::BN) ? idesc : idesc_bf16_f32(C::BM, 2 * u.width);
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
                         ok = false;
@@ -206,7 +224,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < C::BK / C::UMMA_K; ++k) {
                         // +32 bytes along K per step inside the 128-byte swizzle row
-                        umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
+                        umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc_u,
                                   (kb != u.kb0 || k != 0) ? 1u : 0u);
                     }
                     umma_commit(empty_bar(stage));
@@ -264,7 +282,16 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
             const bool split = c_hi > c_lo;
             bool store_y = true;
 
-            if (!split) {
+            if (u.width != C::BN) {
+                // column sub-tile: straight from TMEM to global memory
+                if (rows_live)
+                    epilogue_subtile_store(tbase, u.width, row0 + lane, nb * C::BN + u.sub * u.width,
+                                           args);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                store_y = false;
+            } else if (!split) {
                 if (rows_live) {
                     if (lane == 0) bulk_wait_group_read0();  // last store has read ybuf
                     __syncwarp();

@@ -66,6 +66,8 @@ template <int STAGES>
 __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     fused_up_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmB64,
+                         const __grid_constant__ CUtensorMap tmB32,
                          const __grid_constant__ CUtensorMap tmY, const FusedArgs args) {
     using C = PairCfg<STAGES>;
     extern __shared__ uint8_t smem_raw[];
@@ -156,13 +158,19 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                         continue;
                     }
 #endif
-                    // every load of the pair completes on the LEADER's full barrier
-                    if (is_leader) mbar_arrive_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
+                    // every load of the pair completes on the LEADER's full barrier;
+                    // a column sub-tile loads only its Gate (leader) or Up (peer) rows
+                    const int brows = u.width;
+                    if (is_leader)
+                        mbar_arrive_expect_tx(full_bar(stage), 2 * (C::A_BYTES + brows * C::BK * 2));
                     const uint32_t bar = mapa_shared(full_bar(stage), 0);
                     tma_load_2d_pair(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, bar, kb * C::BK,
                                      pm * C::UMMA_M + C::BM * static_cast<int>(rank));
-                    tma_load_3d_pair(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, bar, 0,
-                                     C::BN * static_cast<int>(rank), nb * sched.k_blocks + kb);
+                    const CUtensorMap *tmBu =
+                        (brows == C::BN) ? &tmB : (brows == 64 ? &tmB64 : &tmB32);
+                    tma_load_3d_pair(sbase + C::OFF_B + stage * C::B_BYTES, tmBu, bar, 0,
+                                     C::BN * static_cast<int>(rank) + u.sub * brows,
+                                     nb * sched.k_blocks + kb);
                     issued_mask |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -194,6 +202,8 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::UMMA_N);
+                const uint32_t idesc_u =
+                    (u.width == C::BN) ? idesc : idesc_bf16_f32(C::UMMA_M, 2 * u.width);
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
                         ok = false;
@@ -204,7 +214,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                     const uint64_t b_desc = smem_desc_k128(sbase + C::OFF_B + stage * C::B_BYTES);
 #pragma unroll
                     for (int k = 0; k < C::BK / C::UMMA_K; ++k)
-                        umma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
+                        umma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc_u,
                                        (kb != u.kb0 || k != 0) ? 1u : 0u);
                     umma_commit_pair_mc(empty_bar(stage), 0x3);
                     if (++stage == STAGES) {
@@ -256,7 +266,15 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
             const bool split = c_hi > c_lo;
             bool store_y = true;
 
-            if (!split) {
+            if (u.width != C::BN) {
+                if (rows_live)
+                    epilogue_subtile_store(tbase, u.width, row0 + lane, nb * C::BN + u.sub * u.width,
+                                           args);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tempty_leader);
+                store_y = false;
+            } else if (!split) {
                 if (rows_live) {
                     if (lane == 0) bulk_wait_group_read0();
                     __syncwarp();

@@ -49,4 +49,33 @@ __global__ void __launch_bounds__(256) pack_weights_kernel(const uint16_t *__res
     }
 }
 
+// Packing from nn.Linear-style weights: W1, W2 [N, K] row-major (each row is
+// one output column's K weights). The packed tile wants exactly such rows
+// (K-major), so this is a row gather: tile (j, b) row r < 128 is
+// W1[128j + r][64b .. 64b+63], row r >= 128 the same of W2; zero outside N
+// and K. Same output layout as pack_weights_kernel.
+__global__ void __launch_bounds__(256) pack_weights_nk_kernel(const uint16_t *__restrict__ W1,
+                                                               const uint16_t *__restrict__ W2,
+                                                               uint16_t *__restrict__ Wp, int K,
+                                                               int N, int KB) {
+    const int b = blockIdx.x;                // k-block
+    const int p0 = blockIdx.y * kPackTile;   // first packed row (over all 2*Np rows)
+    const int j = p0 / 256;
+    const int r0 = p0 % 256;
+    const bool up = r0 >= 128;
+    const int n0 = 128 * j + (r0 & 127);
+    const uint16_t *__restrict__ W = up ? W2 : W1;
+    uint16_t *__restrict__ out =
+        Wp + ((static_cast<int64_t>(j) * KB + b) * 256 + r0) * kPackTile;
+    // 64 rows x 64 k: each thread moves 16 bytes (8 elements) per step
+    for (int i = threadIdx.x; i < kPackTile * kPackTile / 8; i += blockDim.x) {
+        const int rr = i / (kPackTile / 8), c8 = (i % (kPackTile / 8)) * 8;
+        const int n = n0 + rr, k = b * kPackTile + c8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (n < N && k < K)   // K % 8 == 0: an 8-element piece is wholly in or out
+            v = *reinterpret_cast<const uint4 *>(W + static_cast<int64_t>(n) * K + k);
+        *reinterpret_cast<uint4 *>(out + rr * kPackTile + c8) = v;
+    }
+}
+
 }  // namespace swiglu

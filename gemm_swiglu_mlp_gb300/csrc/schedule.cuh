@@ -11,9 +11,9 @@
 //     contiguous ranges whose lengths differ by at most one. A tile whose
 //     iterations span several CTAs' ranges is summed through a workspace
 //     (fused_up_kernel.cuh, split epilogue).
-// The stream-K part absorbs the last partial wave of tiles (and, for decode
-// shapes with fewer tiles than SMs, all of them), so every CTA does the same
-// amount of MMA work up to one k-block.
+//   * or, instead of stream-K, a column-split tail: the tiles past the last
+//     full wave run as 2 or 4 sub-tiles of 64 or 32 columns each, round
+//     robin (plan_schedule below says which, when).
 #pragma once
 
 #include <cstdint>
@@ -42,8 +42,10 @@ struct WorkSched {
     int num_tiles;
     int k_blocks;
     int grid;
-    int dp_tiles;        // a multiple of grid whenever sk_iters > 0
+    int dp_tiles;        // a multiple of grid whenever sk_iters > 0 or n_split > 1
     long long sk_iters;  // (num_tiles - dp_tiles) * k_blocks; >= grid when > 0
+    int n_split;         // 1, or: tiles [dp_tiles, num_tiles) run as n_split
+                         // column sub-tiles of 128 / n_split columns each
     TileOrder order;
 
     // first stream-K iteration of CTA c (c = grid gives sk_iters)
@@ -62,10 +64,12 @@ struct WorkSched {
 };
 
 struct Unit {
-    int tile;  // linear tile index in TileOrder
-    int kb0;   // k-block range [kb0, kb1)
+    int tile;   // linear tile index in TileOrder
+    int kb0;    // k-block range [kb0, kb1)
     int kb1;
-    int sk;    // stream-K tile index (tile - dp_tiles), or -1 for a data-parallel tile
+    int sk;     // stream-K tile index (tile - dp_tiles), or -1 for a data-parallel tile
+    int width;  // output columns of this unit: 128, or 128 / n_split for a sub-tile
+    int sub;    // which sub-tile of the 128-column tile (columns sub*width ..)
 };
 
 // A CTA's units in execution order: its data-parallel tiles, then the pieces
@@ -73,6 +77,7 @@ struct Unit {
 struct UnitIter {
     int k_blocks, grid, dp_tiles;
     int dp_next;
+    int n_split, ns_next, ns_units;  // column sub-tiles of the tail
     long long x, x_end;
 
     __host__ __device__ __forceinline__ void init(const WorkSched &s, int cta) {
@@ -80,16 +85,31 @@ struct UnitIter {
         grid = s.grid;
         dp_tiles = s.dp_tiles;
         dp_next = cta;
+        n_split = s.n_split;
+        ns_next = cta;
+        ns_units = s.n_split > 1 ? (s.num_tiles - s.dp_tiles) * s.n_split : 0;
         x = s.sk_begin(cta);
         x_end = s.sk_begin(cta + 1);
     }
     __host__ __device__ __forceinline__ bool next(Unit &u) {
+        u.width = 128;
+        u.sub = 0;
         if (dp_next < dp_tiles) {
             u.tile = dp_next;
             u.kb0 = 0;
             u.kb1 = k_blocks;
             u.sk = -1;
             dp_next += grid;
+            return true;
+        }
+        if (ns_next < ns_units) {
+            u.tile = dp_tiles + ns_next / n_split;
+            u.sub = ns_next % n_split;
+            u.width = 128 / n_split;
+            u.kb0 = 0;
+            u.kb1 = k_blocks;
+            u.sk = -1;
+            ns_next += grid;
             return true;
         }
         if (x >= x_end) return false;
@@ -106,41 +126,77 @@ struct UnitIter {
     }
 };
 
-// Host-side choice of grid and split. Whole tiles round robin (no
-// workspace) unless that leaves the grid poorly used: with W = ceil(T/G)
-// waves, the data-parallel efficiency is T / (W * G); below
-// `min_dp_efficiency` the stream-K split is used. Splitting costs a partial
-// write and a dependent read-back on the critical path at the end of the
-// kernel, more than a mostly full last wave loses (and for weight-streaming
-// shapes a short last wave loses little: its CTAs get more bandwidth each).
-// `min_sk_iters` keeps every CTA's stream-K share at a few k-blocks so tiles
-// are not cut into slivers.
+// Host-side choice of grid and split, from how well whole tiles fill the
+// grid: with W = ceil(T/G) waves the data-parallel efficiency is
+// T / (W * G).
+//   * >= 0.95: whole tiles round robin, nothing else.
+//   * otherwise, the tiles past the last full wave may run as n_split
+//     column sub-tiles (64 or 32 columns: smaller UMMA N, same k loop), which
+//     shortens the last wave without any workspace. A sub-tile still loads a
+//     whole A tile per k-block for a fraction of the MMA work, so where the
+//     MMA feed is the limit (compute-bound shapes) this only pays when SMs
+//     would otherwise idle outright: fewer tiles than half the grid. For
+//     weight-streaming shapes (`weight_bound`: few token rows, the bytes per
+//     unit scale with its width) it is taken whenever it reaches 0.9.
+//   * otherwise, whole tiles if their efficiency is >= 0.85;
+//   * otherwise the stream-K split of the k-block iterations (workspace).
+// Splitting K costs a partial write and a dependent read-back at the end of
+// the kernel, more than a mostly full last wave loses, and for
+// weight-streaming shapes a short last wave loses little: its CTAs get more
+// bandwidth each. `min_sk_iters` keeps every CTA's stream-K share at a few
+// k-blocks so tiles are not cut into slivers.
 inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_count,
-                               int group_m, int min_sk_iters = 4,
-                               double min_dp_efficiency = 0.85) {
+                               int group_m, int min_sk_iters = 4, bool weight_bound = false) {
     WorkSched s{};
     s.num_tiles = m_tiles * n_tiles;
     s.k_blocks = k_blocks;
+    s.n_split = 1;
     s.order.m_tiles = m_tiles;
     s.order.n_tiles = n_tiles;
     s.order.group_m = group_m < m_tiles ? group_m : m_tiles;
-    const long long total = static_cast<long long>(s.num_tiles) * k_blocks;
-    long long g = sm_count;
-    const int waves = (s.num_tiles + sm_count - 1) / sm_count;
-    if (static_cast<double>(s.num_tiles) >= min_dp_efficiency * waves * sm_count) {
+    const int T = s.num_tiles, G = sm_count;
+    const int waves = (T + G - 1) / G;
+    const double eff_dp = static_cast<double>(T) / (static_cast<double>(waves) * G);
+    const int full = (T / G) * G;   // tiles in complete waves
+    const int tail = T - full;
+    if (eff_dp < 0.95 && tail > 0) {
+        int best = 1;
+        double best_eff = eff_dp;
+        for (int split = 2; split <= 4; split *= 2) {
+            const int units = tail * split;
+            const double t = static_cast<double>(full / G) +
+                             static_cast<double>((units + G - 1) / G) / split;
+            const double e = (static_cast<double>(T) / G) / t;
+            if (e > best_eff + 1e-9) {
+                best = split;
+                best_eff = e;
+            }
+        }
+        const bool take = weight_bound ? best_eff >= 0.9 : (best_eff >= 0.85 && 2 * T < G);
+        if (best > 1 && take) {
+            s.grid = G;
+            s.dp_tiles = full;
+            s.n_split = best;
+            s.sk_iters = 0;
+            return s;
+        }
+    }
+    if (eff_dp >= 0.85) {
         // data-parallel: every tile whole, no workspace
-        s.grid = s.num_tiles < sm_count ? s.num_tiles : sm_count;
-        s.dp_tiles = s.num_tiles;
+        s.grid = T < G ? T : G;
+        s.dp_tiles = T;
         s.sk_iters = 0;
         return s;
     }
+    const long long total = static_cast<long long>(T) * k_blocks;
+    long long g = G;
     const long long max_grid = total / (min_sk_iters > 0 ? min_sk_iters : 1);
     if (g > max_grid) g = max_grid > 0 ? max_grid : 1;
     s.grid = static_cast<int>(g);
-    const int full_waves = s.num_tiles / s.grid;
+    const int full_waves = T / s.grid;
     // keep one full wave plus the remainder in the stream-K part
     s.dp_tiles = (full_waves >= 2 ? full_waves - 1 : 0) * s.grid;
-    s.sk_iters = static_cast<long long>(s.num_tiles - s.dp_tiles) * k_blocks;
+    s.sk_iters = static_cast<long long>(T - s.dp_tiles) * k_blocks;
     if (s.sk_iters < s.grid) {  // tiny problem: one iteration per CTA at most
         s.grid = static_cast<int>(s.sk_iters);
     }

@@ -150,8 +150,10 @@ WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, bool pair) {
     const int m_tiles = static_cast<int>((M + rows - 1) / rows);
     const int n_tiles = static_cast<int>((N + FusedC::BN - 1) / FusedC::BN);
     const int k_blocks = static_cast<int>((K + FusedC::BK - 1) / FusedC::BK);
+    // few token rows: the kernel streams weights (HBM-bound), see plan_schedule
+    const bool weight_bound = M <= 128;
     return plan_schedule(m_tiles, n_tiles, k_blocks, workers, pair ? kGroupM / 2 : kGroupM,
-                         kMinStreamKIters);
+                         kMinStreamKIters, weight_bound);
 }
 
 // Workspace layout: a counter region at offset 0 whose size depends only on
@@ -247,8 +249,10 @@ size_t swiglu_packed_weight_bytes(int64_t N, int64_t K) {
     return static_cast<size_t>(2 * round_up(N, 128)) * static_cast<size_t>(round_up(K, 64)) * 2u;
 }
 
-int swiglu_pack_weights(const void *W1, const void *W2, int64_t K, int64_t N, void *Wpacked,
-                        void *stream) {
+// Argument checks shared by both pack entry points; on success returns the
+// launch grid. The weights are 2*K*N elements each way round.
+static int pack_checks(const void *W1, const void *W2, int64_t K, int64_t N, void *Wpacked,
+                       dim3 *grid) {
     if (!W1 || !W2 || !Wpacked) return SWIGLU_ERR_INVALID_ARG;
     if (K <= 0 || N <= 0 || (K % 8) != 0 || (N % 8) != 0) return SWIGLU_ERR_INVALID_ARG;
     if (K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31)) return SWIGLU_ERR_INVALID_ARG;
@@ -260,15 +264,40 @@ int swiglu_pack_weights(const void *W1, const void *W2, int64_t K, int64_t N, vo
     const int64_t rows = 2 * round_up(N, 128);
     const int64_t kblocks = (K + kPackTile - 1) / kPackTile;
     if (rows / kPackTile > 65535) return SWIGLU_ERR_UNSUPPORTED;
+    *grid = dim3(static_cast<unsigned>(kblocks), static_cast<unsigned>(rows / kPackTile));
+    return SWIGLU_OK;
+}
+
+int swiglu_pack_weights(const void *W1, const void *W2, int64_t K, int64_t N, void *Wpacked,
+                        void *stream) {
+    dim3 grid;
+    int s = pack_checks(W1, W2, K, N, Wpacked, &grid);
+    if (s != SWIGLU_OK) return s;
     int dev;
     DeviceState *st;
-    const int s = device_setup(&dev, &st);
+    s = device_setup(&dev, &st);
     if (s != SWIGLU_OK) return s;
-    const dim3 grid(static_cast<unsigned>(kblocks), static_cast<unsigned>(rows / kPackTile));
     pack_weights_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t *>(W1), static_cast<const uint16_t *>(W2),
         static_cast<uint16_t *>(Wpacked), static_cast<int>(K), static_cast<int>(N),
-        static_cast<int>(kblocks));
+        static_cast<int>(grid.x));
+    if (cudaGetLastError() != cudaSuccess) return SWIGLU_ERR_CUDA;
+    return SWIGLU_OK;
+}
+
+int swiglu_pack_weights_nk(const void *W1, const void *W2, int64_t N, int64_t K, void *Wpacked,
+                           void *stream) {
+    dim3 grid;
+    int s = pack_checks(W1, W2, K, N, Wpacked, &grid);
+    if (s != SWIGLU_OK) return s;
+    int dev;
+    DeviceState *st;
+    s = device_setup(&dev, &st);
+    if (s != SWIGLU_OK) return s;
+    pack_weights_nk_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(W1), static_cast<const uint16_t *>(W2),
+        static_cast<uint16_t *>(Wpacked), static_cast<int>(K), static_cast<int>(N),
+        static_cast<int>(grid.x));
     if (cudaGetLastError() != cudaSuccess) return SWIGLU_ERR_CUDA;
     return SWIGLU_OK;
 }
@@ -325,9 +354,11 @@ int swiglu_up_forward(const void *A, const void *Wpacked, void *Y, int64_t M, in
         (pair || M >= FusedC::BM) ? FusedC::BM : static_cast<int>(round_up(M, 8));
     const uint64_t weight_tiles =
         static_cast<uint64_t>(sched.order.n_tiles) * static_cast<uint64_t>(sched.k_blocks);
-    CUtensorMap tmA, tmB, tmY;
+    CUtensorMap tmA, tmB, tmB64, tmB32, tmY;
     if (!encode_bf16_2d(&tmA, A, K, M, FusedC::BK, a_rows) ||
         !encode_packed_weights(&tmB, Wpacked, weight_tiles, pair ? 128u : 256u) ||
+        !encode_packed_weights(&tmB64, Wpacked, weight_tiles, 64u) ||
+        !encode_packed_weights(&tmB32, Wpacked, weight_tiles, 32u) ||
         !encode_bf16_2d(&tmY, Y, N, M, 64, 32))
         return SWIGLU_ERR_CUDA;
 
@@ -336,6 +367,8 @@ int swiglu_up_forward(const void *A, const void *Wpacked, void *Y, int64_t M, in
     args.N = static_cast<int>(N);
     args.K = static_cast<int>(K);
     args.stage_tx_bytes = a_rows * FusedC::BK * 2 + FusedC::B_BYTES;
+    args.a_tx_bytes = a_rows * FusedC::BK * 2;
+    args.Y = static_cast<uint16_t *>(Y);
     args.slot_rows = slot_rows_for(M);
     args.sched = sched;
 #ifdef SWIGLU_TEST_FAULT_INJECTION
@@ -366,13 +399,15 @@ int swiglu_up_forward(const void *A, const void *Wpacked, void *Y, int64_t M, in
         cfg.gridDim = dim3(static_cast<unsigned>(2 * sched.grid));
         cfg.blockDim = dim3(PairC::THREADS);
         cfg.dynamicSmemBytes = PairC::SMEM_BYTES;
-        err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages>, tmA, tmB, tmY, args);
+        err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages>, tmA, tmB, tmB64, tmB32,
+                                 tmY, args);
     } else {
         cfg.numAttrs = 1;
         cfg.gridDim = dim3(static_cast<unsigned>(sched.grid));
         cfg.blockDim = dim3(FusedC::THREADS);
         cfg.dynamicSmemBytes = FusedC::SMEM_BYTES;
-        err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kFusedStages>, tmA, tmB, tmY, args);
+        err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kFusedStages>, tmA, tmB, tmB64, tmB32, tmY,
+                                 args);
     }
     if (err != cudaSuccess) {
         cudaGetLastError();

@@ -79,6 +79,17 @@ int swiglu_pack_weights(const void *W1, const void *W2, int64_t K, int64_t N,
                         void *Wpacked, void *stream);
 
 /*
+ * Same as swiglu_pack_weights, from weights stored the way PyTorch's
+ * nn.Linear stores them: W1 and W2 (device, BF16) are [N, K] row-major (one
+ * row of K weights per output column; Gate = A x W1^T). The packed layout
+ * keeps such rows K-major, so this is a row gather without a transpose.
+ * Same requirements, errors and output as swiglu_pack_weights; the packed
+ * result is byte-identical to swiglu_pack_weights(W1^T, W2^T).
+ */
+int swiglu_pack_weights_nk(const void *W1, const void *W2, int64_t N, int64_t K,
+                           void *Wpacked, void *stream);
+
+/*
  * Bytes of device workspace that swiglu_up_forward needs for (M, N, K) on
  * the current device (the split of K over CTAs depends on its SM count).
  * 0 means none: pass workspace = NULL, workspace_bytes = 0. The workspace

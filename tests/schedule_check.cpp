@@ -1,6 +1,6 @@
 // Host-side check of the fused kernel's work schedule (schedule.cuh), compiled
 // with g++ by tests/test_schedule.py. For each (m_tiles, n_tiles, k_blocks,
-// sm_count) given on stdin it verifies that:
+// sm_count, min_sk_iters, weight_bound) given on stdin it verifies that:
 //   * the units of all CTAs cover every (tile, k-block) exactly once;
 //   * data-parallel tiles are whole and spread round robin;
 //   * for every stream-K tile, the contributor range [sk_owner(first),
@@ -28,19 +28,21 @@ static int fail(const char *what, int a, int b) {
 }
 
 int main() {
-    int mt, nt, kb, sms, min_iters;
+    int mt, nt, kb, sms, min_iters, wbound;
     int bad = 0;
-    while (std::scanf("%d %d %d %d %d", &mt, &nt, &kb, &sms, &min_iters) == 5) {
-        const WorkSched s = plan_schedule(mt, nt, kb, sms, 16, min_iters);
+    while (std::scanf("%d %d %d %d %d %d", &mt, &nt, &kb, &sms, &min_iters, &wbound) == 6) {
+        const WorkSched s = plan_schedule(mt, nt, kb, sms, 16, min_iters, wbound != 0);
         const int T = mt * nt;
         if (s.grid < 1 || s.grid > sms) { bad |= fail("grid", s.grid, sms); continue; }
         if (s.sk_iters > 0 && s.dp_tiles % s.grid != 0) { bad |= fail("dp multiple", s.dp_tiles, s.grid); continue; }
-        if (s.sk_iters == 0 && s.dp_tiles != T) { bad |= fail("dp-only must cover all tiles", s.dp_tiles, T); continue; }
-        if (s.sk_iters != (long long)(T - s.dp_tiles) * kb) { bad |= fail("sk_iters", T, s.dp_tiles); continue; }
+        if (s.sk_iters == 0 && s.n_split == 1 && s.dp_tiles != T) { bad |= fail("dp-only must cover all tiles", s.dp_tiles, T); continue; }
+        if (s.n_split != 1 && (s.sk_iters != 0 || s.dp_tiles % s.grid != 0 || (s.n_split != 2 && s.n_split != 4))) { bad |= fail("column split", s.n_split, s.dp_tiles); continue; }
+        if (s.n_split == 1 && s.sk_iters != (long long)(T - s.dp_tiles) * kb) { bad |= fail("sk_iters", T, s.dp_tiles); continue; }
         if (s.sk_iters > 0 && s.sk_iters < s.grid) { bad |= fail("sk < grid", (int)s.sk_iters, s.grid); continue; }
         // the workspace counter region holds 2 counters per CTA-pair half: stream-K tiles < 2 * grid
         if (s.sk_iters > 0 && T - s.dp_tiles >= 2 * s.grid) { bad |= fail("sk tiles >= 2*grid", T - s.dp_tiles, s.grid); continue; }
-        std::vector<int> cover((size_t)T * kb, 0);
+        // coverage counts (tile, k-block, 32-column quarter) cells
+        std::vector<int> cover((size_t)T * kb * 4, 0);
         std::map<int, std::vector<std::pair<int, int>>> contrib;  // sk tile -> (cta, kb0)
         std::vector<long long> work(s.grid, 0);
         std::set<long long> coords_seen;
@@ -50,12 +52,19 @@ int main() {
             Unit u;
             int n_dp = 0;
             while (it.next(u)) {
-                if (u.tile < 0 || u.tile >= T || u.kb0 < 0 || u.kb1 > kb || u.kb0 >= u.kb1) {
+                if (u.tile < 0 || u.tile >= T || u.kb0 < 0 || u.kb1 > kb || u.kb0 >= u.kb1 ||
+                    (u.width != 128 && u.width != 64 && u.width != 32) || u.sub < 0 ||
+                    (u.sub + 1) * u.width > 128) {
                     bad |= fail("unit range", u.tile, u.kb0);
                     break;
                 }
-                for (int k = u.kb0; k < u.kb1; ++k) cover[(size_t)u.tile * kb + k]++;
-                work[c] += u.kb1 - u.kb0;
+                if (u.width != 128 && (u.sk >= 0 || u.tile < s.dp_tiles || u.width != 128 / s.n_split))
+                    bad |= fail("sub-tile outside the split tail", u.tile, u.width);
+                for (int k = u.kb0; k < u.kb1; ++k)
+                    for (int q = u.sub * u.width / 32; q < (u.sub + 1) * u.width / 32; ++q)
+                        cover[((size_t)u.tile * kb + k) * 4 + q]++;
+                // work in quarter-tile k-blocks (a 32-column sub-tile does a quarter of the MMA)
+                work[c] += (long long)(u.kb1 - u.kb0) * (u.width / 32);
                 if (u.sk < 0) {
                     ++n_dp;
                     if (u.kb0 != 0 || u.kb1 != kb) bad |= fail("dp not whole", u.tile, c);
@@ -69,10 +78,10 @@ int main() {
                 coords_seen.insert((long long)mb * nt + nb);
             }
             const int want_dp = s.dp_tiles / s.grid + (c < s.dp_tiles % s.grid ? 1 : 0);
-            if (n_dp != want_dp) bad |= fail("dp per cta", n_dp, c);
+            if (s.n_split == 1 && n_dp != want_dp) bad |= fail("dp per cta", n_dp, c);
         }
         for (size_t i = 0; i < cover.size(); ++i)
-            if (cover[i] != 1) { bad |= fail("coverage", (int)(i / kb), cover[i]); break; }
+            if (cover[i] != 1) { bad |= fail("coverage", (int)(i / kb / 4), cover[i]); break; }
         if ((int)coords_seen.size() != T) bad |= fail("tile order not a bijection", (int)coords_seen.size(), T);
         std::set<int> slots_used;
         int split_tiles = 0, max_contrib = 0;
@@ -96,16 +105,18 @@ int main() {
         }
         long long wmin = work[0], wmax = work[0];
         for (long long w : work) { wmin = w < wmin ? w : wmin; wmax = w > wmax ? w : wmax; }
-        // stream-K: balanced to one k-block; data-parallel: to one whole tile,
-        // and then only when the grid is used at least 85% (the plan's threshold)
-        if (s.sk_iters > 0 && wmax - wmin > 1) bad |= fail("imbalance", (int)wmin, (int)wmax);
-        if (s.sk_iters == 0) {
-            if (wmax - wmin > kb) bad |= fail("dp imbalance", (int)wmin, (int)wmax);
+        // stream-K: balanced to one k-block (4 quarter units); data-parallel:
+        // to one whole tile, and only when the grid is used at least 85%;
+        // column-split tail: to one sub-tile
+        if (s.sk_iters > 0 && wmax - wmin > 4) bad |= fail("imbalance", (int)wmin, (int)wmax);
+        if (s.sk_iters == 0 && s.n_split == 1) {
+            if (wmax - wmin > 4 * kb) bad |= fail("dp imbalance", (int)wmin, (int)wmax);
             const int waves = (T + sms - 1) / sms;
             if (T < 0.85 * waves * sms) bad |= fail("dp chosen below threshold", T, waves * sms);
         }
-        std::printf("mt=%d nt=%d kb=%d sms=%d grid=%d dp=%d sk_iters=%lld split=%d max_contrib=%d work=[%lld,%lld]\n",
-                    mt, nt, kb, sms, s.grid, s.dp_tiles, s.sk_iters, split_tiles, max_contrib, wmin, wmax);
+        if (s.n_split > 1 && wmax - wmin > 4 * kb / s.n_split) bad |= fail("split imbalance", (int)wmin, (int)wmax);
+        std::printf("mt=%d nt=%d kb=%d sms=%d grid=%d dp=%d sk_iters=%lld n_split=%d split=%d max_contrib=%d work=[%lld,%lld]\n",
+                    mt, nt, kb, sms, s.grid, s.dp_tiles, s.sk_iters, s.n_split, split_tiles, max_contrib, wmin, wmax);
     }
     return bad;
 }

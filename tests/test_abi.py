@@ -102,6 +102,7 @@ def test_forward_rejects_bad_arguments_on_host(lib, args):
 def test_pack_rejects_bad_arguments_on_host(lib, args):
     W1, W2, Wp, K, N = args
     assert lib.swiglu_pack_weights(W1, W2, K, N, Wp, None) == 1
+    assert lib.swiglu_pack_weights_nk(W1, W2, N, K, Wp, None) == 1
 
 
 def test_valid_call_without_gpu_reports_error_not_crash(lib):

@@ -1,0 +1,88 @@
+"""Failure detection without a GPU fault.
+
+Every wait inside the fused kernels is bounded. A test-only build of the same
+sources (SWIGLU_TEST_FAULT_INJECTION, ~10 ms wait limit, never loaded by the
+product binding) can leave the first pipeline stage unfilled, so the MMA
+warp's wait for it runs out. The kernel must then record the timeout in the
+device status word, drain what is in flight, free its tensor memory and exit;
+the host reads the status with swiglu_check_device_status, and the same CUDA
+context must go on computing correct results. Nothing here traps, faults or
+hangs a GPU: the only failure is a wait on a barrier that nothing completes.
+"""
+import ctypes
+import os
+
+import numpy as np
+import pytest
+
+import workloads
+from tests.parity import compare, from_device_bf16, to_device_bf16
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+TIMEOUT_STATUS = 4        # SWIGLU_ERR_DEVICE_TIMEOUT
+MMA_TIMEOUT_BIT = 2       # kStatusMmaTimeout
+
+
+@pytest.fixture(scope="module")
+def fi_lib(tmp_path_factory):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gemm_swiglu_mlp_gb300 import build
+    path = str(tmp_path_factory.mktemp("fi") / "libswiglu_faultinject.so")
+    build.build_fault_injection_library(path)
+    lib = ctypes.CDLL(path)
+    vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    lib.swiglu_test_set_fault_injection.argtypes = [ctypes.c_int]
+    lib.swiglu_test_set_fault_injection.restype = None
+    lib.swiglu_pack_weights.argtypes = [vp, vp, i64, i64, vp, vp]
+    lib.swiglu_up_forward.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+    lib.swiglu_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.swiglu_workspace_bytes.restype = sz
+    lib.swiglu_packed_weight_bytes.argtypes = [i64, i64]
+    lib.swiglu_packed_weight_bytes.restype = sz
+    lib.swiglu_check_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    torch.cuda.set_device(0)
+    return lib
+
+
+def _run(lib, A, Wp, M, N, K, stream):
+    Y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    ws_bytes = lib.swiglu_workspace_bytes(M, N, K)
+    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    st = lib.swiglu_up_forward(A.data_ptr(), Wp.data_ptr(), Y.data_ptr(), M, N, K,
+                               ws.data_ptr() if ws_bytes else None, ws_bytes, stream)
+    assert st == 0
+    raw = ctypes.c_uint32(0)
+    status = lib.swiglu_check_device_status(stream, ctypes.byref(raw))
+    return Y, status, raw.value
+
+
+@pytest.mark.parametrize("variant,M,N,K", [("1sm", 128, 256, 512), ("2sm", 512, 256, 512)])
+def test_wait_timeout_is_reported_and_context_survives(fi_lib, monkeypatch, variant, M, N, K):
+    monkeypatch.setenv("SWIGLU_FUSED_VARIANT", variant)
+    import oracle
+    A, W1, W2 = workloads.random_case(M, N, K, seed=77)
+    Ad = to_device_bf16(A, "cuda")
+    W1d, W2d = to_device_bf16(W1, "cuda"), to_device_bf16(W2, "cuda")
+    Wp = torch.empty(fi_lib.swiglu_packed_weight_bytes(N, K), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert fi_lib.swiglu_pack_weights(W1d.data_ptr(), W2d.data_ptr(), K, N, Wp.data_ptr(),
+                                      stream) == 0
+
+    # 1) a launch whose first stage is never filled: the bounded wait runs out
+    fi_lib.swiglu_test_set_fault_injection(1)
+    try:
+        _, status, raw = _run(fi_lib, Ad, Wp, M, N, K, stream)
+    finally:
+        fi_lib.swiglu_test_set_fault_injection(0)
+    assert status == TIMEOUT_STATUS
+    assert raw & MMA_TIMEOUT_BIT
+
+    # 2) the word was cleared by the read, and the context still works
+    Y, status, raw = _run(fi_lib, Ad, Wp, M, N, K, stream)
+    assert status == 0 and raw == 0
+    r = compare(from_device_bf16(Y), oracle.swiglu_up(A, W1, W2)["Y"])
+    assert r["mismatches"] == 0 and r["over_bound"] == 0, r

@@ -67,6 +67,17 @@ def test_pack_is_the_documented_permutation(sg, K, N, seed):
     assert np.array_equal(u1, W1) and np.array_equal(u2, W2)
 
 
+@pytest.mark.parametrize("K,N,seed", [(8, 8, 11), (200, 264, 12), (896, 4864, 13)])
+def test_pack_from_linear_layout_matches(sg, K, N, seed):
+    # nn.Linear keeps W as [N, K]: packing W^T that way gives the same bytes
+    _, W1, W2 = workloads.random_case(1, N, K, seed)
+    a = sg.swiglu_pack_weights(to_device_bf16(W1, "cuda"), to_device_bf16(W2, "cuda"))
+    b = sg.swiglu_pack_weights_nk(to_device_bf16(np.ascontiguousarray(W1.T), "cuda"),
+                                  to_device_bf16(np.ascontiguousarray(W2.T), "cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
 SMALL = [
     (1, 8, 8),          # smallest legal problem: one partial tile everywhere
     (7, 136, 72),       # ragged M, N (128 + 8) and K (64 + 8)
@@ -80,6 +91,10 @@ SMALL = [
     (1, 136, 4096),     # one token, long K split many ways
     (2048, 392, 520),   # data-parallel tiles plus a stream-K tail
     (513, 136, 72),     # one row into a third 256-row pair tile
+    (100, 4600, 200),   # 36 tiles on 152 SMs: 32-column sub-tiles, ragged last sub-tile
+    (64, 9000, 136),    # 71 tiles: 64-column sub-tiles
+    (1280, 11776, 64),  # whole-tile waves plus a column-split tail
+    (64, 27648, 256),   # weight-streaming: one wave plus half-width tail units
 ]
 
 

@@ -25,13 +25,14 @@ def _cases():
     for w in workloads.WORKLOADS:
         mt, nt, kb = -(-w.M // 128), -(-w.N // 128), -(-w.K // 64)
         for sms in (152, 148, 132):
-            cases.append((mt, nt, kb, sms, 8))
+            cases.append((mt, nt, kb, sms, 8, int(w.M <= 128)))
+            cases.append((-(-w.M // 256), nt, kb, sms // 2, 8, 0))   # CTA-pair kernel
     rng = np.random.Generator(np.random.PCG64(3))
-    for _ in range(300):
+    for _ in range(400):
         cases.append((int(rng.integers(1, 40)), int(rng.integers(1, 40)), int(rng.integers(1, 30)),
-                      int(rng.integers(1, 200)), int(rng.integers(1, 10))))
-    cases += [(1, 1, 1, 152, 8), (1, 1, 200, 152, 8), (1, 152, 3, 152, 8), (2, 152, 5, 152, 8),
-              (1, 153, 7, 152, 1), (64, 231, 128, 152, 8)]
+                      int(rng.integers(1, 200)), int(rng.integers(1, 10)), int(rng.integers(0, 2))))
+    cases += [(1, 1, 1, 152, 8, 1), (1, 1, 200, 152, 8, 0), (1, 152, 3, 152, 8, 1),
+              (2, 152, 5, 152, 8, 0), (1, 153, 7, 152, 1, 1), (64, 231, 128, 152, 8, 0)]
     return cases
 
 

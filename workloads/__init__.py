@@ -126,6 +126,12 @@ def make_W(w: Workload, which: int) -> np.ndarray:
     return f32_to_bf16_bits(_normal(seed, (w.K, w.N), float(w.K) ** -0.5))
 
 
+def make_W3(w: Workload) -> np.ndarray:
+    """Down-projection weight W3 [N, K] ~ N(0, 1/N), seed 5000 + c: only for
+    measuring the whole gated MLP, out = Y W3, around the up-projection."""
+    return f32_to_bf16_bits(_normal(5000 + w.seed_index, (w.N, w.K), float(w.N) ** -0.5))
+
+
 def make_inputs(w: Workload):
     """(A [M,K], W1 [K,N], W2 [K,N]) as BF16 bit patterns (uint16)."""
     return make_A(w), make_W(w, 1), make_W(w, 2)

@@ -13,7 +13,9 @@ summary's problem statement; SiLU(x) = x / (1 + e^-x).
 
 Parity status: pinned (brute force with exact rationals on tiny shapes,
 closed forms W1 = 0 / W2 = 0 / rank-1, SiLU identities and textbook values,
-BF16 rounding on hand-built bit patterns including ties).
+BF16 rounding on hand-built bit patterns including ties; FP8 E4M3 decoding
+on hand-derived patterns and an exact field-by-field decoder, and the FP8
+definition by exact-rational brute force with scales).
 """
 from __future__ import annotations
 
@@ -66,6 +68,15 @@ def _load():
                                      i64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                      u16p, f64p, f64p, f64p, ctypes.c_int]
     lib.oracle_swiglu_up.restype = ctypes.c_int
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_double.restype = ctypes.c_double
+    lib.oracle_swiglu_up_fp8.argtypes = [u8p, u8p, u8p,
+                                         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                         i64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         u16p, f64p, f64p, f64p, ctypes.c_int]
+    lib.oracle_swiglu_up_fp8.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -80,6 +91,10 @@ def double_to_bf16(x: float) -> int:
 
 def silu(x: float) -> float:
     return _load().oracle_silu(float(x))
+
+
+def e4m3_to_double(bits: int) -> float:
+    return _load().oracle_e4m3_to_double(int(bits))
 
 
 def _ptr(a, ctype):
@@ -126,6 +141,49 @@ def swiglu_up(A: np.ndarray, W1: np.ndarray, W2: np.ndarray, rows=None,
                               int(nthreads))
     if rc != 0:
         raise RuntimeError("oracle_swiglu_up failed (status %d)" % rc)
+    out = {"Y": Y}
+    if want_unrounded:
+        out["Yd"] = Yd
+    if want_gate_up:
+        out["G"] = G
+        out["U"] = U
+    return out
+
+
+def swiglu_up_fp8(A8: np.ndarray, W18: np.ndarray, W28: np.ndarray, s_a: float, s_w1: float,
+                  s_w2: float, rows=None, want_unrounded: bool = False,
+                  want_gate_up: bool = False, nthreads: int = 0, cols=None):
+    """Oracle Y for FP8 E4M3 inputs (numpy uint8) with per-tensor scales:
+    A = s_a * A8 [M, K], W1 = s_w1 * W1_8 [K, N], W2 = s_w2 * W2_8 [K, N].
+    Same outputs as swiglu_up (Y BF16 bits; G and U are the scaled sums)."""
+    lib = _load()
+    A8 = np.ascontiguousarray(A8, dtype=np.uint8)
+    W18 = np.ascontiguousarray(W18, dtype=np.uint8)
+    W28 = np.ascontiguousarray(W28, dtype=np.uint8)
+    M, K = A8.shape
+    K1, N = W18.shape
+    if K1 != K or W28.shape != (K, N):
+        raise ValueError("shape mismatch: A %s W1 %s W2 %s" % (A8.shape, W18.shape, W28.shape))
+    if rows is None:
+        rows_arr, R = None, M
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        R = rows_arr.shape[0]
+    n0, n1 = (0, N) if cols is None else (int(cols[0]), int(cols[1]))
+    C = max(0, n1 - n0)
+    Y = np.empty((R, C), dtype=np.uint16)
+    Yd = np.empty((R, C), dtype=np.float64) if want_unrounded else None
+    G = np.empty((R, C), dtype=np.float64) if want_gate_up else None
+    U = np.empty((R, C), dtype=np.float64) if want_gate_up else None
+    rc = lib.oracle_swiglu_up_fp8(_ptr(A8, ctypes.c_uint8), _ptr(W18, ctypes.c_uint8),
+                                  _ptr(W28, ctypes.c_uint8), M, N, K,
+                                  float(s_a), float(s_w1), float(s_w2),
+                                  _ptr(rows_arr, ctypes.c_int64), R, n0, n1,
+                                  _ptr(Y, ctypes.c_uint16), _ptr(Yd, ctypes.c_double),
+                                  _ptr(G, ctypes.c_double), _ptr(U, ctypes.c_double),
+                                  int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_swiglu_up_fp8 failed (status %d)" % rc)
     out = {"Y": Y}
     if want_unrounded:
         out["Yd"] = Yd

@@ -106,3 +106,15 @@ def near_tie(x: decimal.Decimal, rel: float = 1e-12) -> bool:
     lo, hi, _ = _bf16_grid_neighbours(fx)
     mid = (lo + hi) / 2
     return abs(abs(fx) - mid) <= Fraction(rel) * abs(fx)
+
+
+def e4m3_fraction(bits: int) -> Fraction:
+    """Decode an FP8 E4M3 pattern field by field (finite values only)."""
+    bits = int(bits) & 0xFF
+    sign = -1 if bits & 0x80 else 1
+    exp = (bits >> 3) & 0xF
+    man = bits & 0x7
+    assert not (exp == 0xF and man == 0x7), "nan"
+    if exp == 0:
+        return sign * Fraction(man, 1 << 9)
+    return sign * Fraction(8 + man, 8) * (Fraction(2) ** (exp - 7))

@@ -235,3 +235,77 @@ def test_column_range_matches_full(oracle_mod):
     assert np.array_equal(part["G"], full["G"][[8, 2], 13:51])
     with pytest.raises(RuntimeError):
         oracle_mod.swiglu_up(A, W1, W2, cols=(10, 71))
+
+
+# ----------------------------------------------------------------- FP8 E4M3
+def _golden_e4m3_cases():
+    cases = []
+    with open(os.path.join(HERE, "golden", "e4m3_decode_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            b, v = line.split()[:2]
+            cases.append((int(b, 16), float("nan") if v == "nan" else float.fromhex(v)))
+    return cases
+
+
+@pytest.mark.parametrize("bits,value", _golden_e4m3_cases())
+def test_e4m3_decode_hand_derived(oracle_mod, bits, value):
+    got = oracle_mod.e4m3_to_double(bits)
+    if math.isnan(value):
+        assert math.isnan(got)
+    else:
+        assert got == value and math.copysign(1, got) == math.copysign(1, value)
+
+
+def test_e4m3_decode_matches_field_decoder(oracle_mod):
+    for b in range(256):
+        if (b & 0x7F) == 0x7F:
+            assert math.isnan(oracle_mod.e4m3_to_double(b))
+            continue
+        assert Fraction(oracle_mod.e4m3_to_double(b)) == exact.e4m3_fraction(b), hex(b)
+
+
+def test_e4m3_quantizer_round_trip_and_ties():
+    # every finite pattern encodes back to itself; ties go to the even pattern
+    pats = np.array([b for b in range(256) if (b & 0x7F) != 0x7F], np.uint8)
+    vals = workloads.e4m3_bits_to_f64(pats)
+    back = workloads.f32_to_e4m3_bits(vals)
+    assert np.array_equal(back[vals != 0], pats[vals != 0])
+    # 1 + 1/16 lies halfway between 1.0 (0x38, even) and 1.125 (0x39): -> 0x38
+    # 1 + 3/16 lies halfway between 1.125 (odd) and 1.25 (0x3a, even): -> 0x3a
+    # 2^-10 lies halfway between 0 and the smallest subnormal: -> 0
+    got = workloads.f32_to_e4m3_bits(np.array([1 + 1 / 16, 1 + 3 / 16, 2.0 ** -10, 500.0]))
+    assert got.tolist() == [0x38, 0x3A, 0x00, 0x7E]
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(1, 1, 1, 1), (3, 5, 7, 2), (8, 8, 8, 3), (2, 9, 4, 4)])
+def test_fp8_bruteforce_exact_tiny(oracle_mod, M, N, K, seed):
+    A8, W18, W28, sa, s1, s2 = workloads.random_case_fp8(M, N, K, seed=200 + seed, a_scale=2.0)
+    out = oracle_mod.swiglu_up_fp8(A8, W18, W28, sa, s1, s2, want_gate_up=True,
+                                   want_unrounded=True)
+    for m in range(M):
+        for n in range(N):
+            dg = sum((exact.e4m3_fraction(A8[m, k]) * exact.e4m3_fraction(W18[k, n])
+                      for k in range(K)), Fraction(0))
+            du = sum((exact.e4m3_fraction(A8[m, k]) * exact.e4m3_fraction(W28[k, n])
+                      for k in range(K)), Fraction(0))
+            g = dg * Fraction(sa) * Fraction(s1)
+            u = du * Fraction(sa) * Fraction(s2)
+            # the E4M3 sums are exact; scaling rounds once in binary64
+            assert out["G"][m, n] == float(g) and out["U"][m, n] == float(u)
+            y = exact.silu_decimal(exact.frac_to_decimal(g)) * exact.frac_to_decimal(u)
+            if exact.near_tie(y):
+                continue
+            assert int(out["Y"][m, n]) == exact.round_bf16_exact(y), (m, n)
+
+
+def test_fp8_unit_scales_equal_bf16_definition(oracle_mod):
+    # E4M3 values are exact BF16 values: with unit scales both oracle entry
+    # points must agree bit for bit
+    A8, W18, W28, _, _, _ = workloads.random_case_fp8(5, 12, 16, seed=31)
+    to_bf16 = lambda b: workloads.f32_to_bf16_bits(workloads.e4m3_bits_to_f64(b).astype(np.float32))
+    y8 = oracle_mod.swiglu_up_fp8(A8, W18, W28, 1.0, 1.0, 1.0)["Y"]
+    y16 = oracle_mod.swiglu_up(to_bf16(A8), to_bf16(W18), to_bf16(W28))["Y"]
+    assert np.array_equal(y8, y16)

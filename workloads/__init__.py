@@ -106,7 +106,7 @@ def _normal(seed: int, shape, scale: float) -> np.ndarray:
     return x
 
 
-def make_A(w: Workload) -> np.ndarray:
+def make_A_f32(w: Workload) -> np.ndarray:
     c = w.seed_index
     a = _normal(1000 + c, (w.M, w.K), 1.0)
     if w.variant == "stress":
@@ -115,15 +115,91 @@ def make_A(w: Workload) -> np.ndarray:
         n_out = int(round(0.01 * w.K))
         perm = np.random.Generator(np.random.PCG64(4000 + c)).permutation(w.K)
         a[:, perm[:n_out]] *= np.float32(20.0)
-    return f32_to_bf16_bits(a)
+    return a
 
 
-def make_W(w: Workload, which: int) -> np.ndarray:
+def make_W_f32(w: Workload, which: int) -> np.ndarray:
     """which = 1 (gate weight W1) or 2 (up weight W2); [K, N] row-major."""
     assert which in (1, 2)
     c = w.seed_index
     seed = (2000 if which == 1 else 3000) + c
-    return f32_to_bf16_bits(_normal(seed, (w.K, w.N), float(w.K) ** -0.5))
+    return _normal(seed, (w.K, w.N), float(w.K) ** -0.5)
+
+
+def make_A(w: Workload) -> np.ndarray:
+    return f32_to_bf16_bits(make_A_f32(w))
+
+
+def make_W(w: Workload, which: int) -> np.ndarray:
+    """which = 1 (gate weight W1) or 2 (up weight W2); [K, N] row-major BF16 bits."""
+    return f32_to_bf16_bits(make_W_f32(w, which))
+
+
+E4M3_MAX = 448.0
+
+
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Values -> FP8 E4M3 bit patterns (uint8), round to nearest even,
+    saturating at +-448 (callers scale into range first). Computed in
+    binary64: the spacing is 2^(e-3) in the binade [2^e, 2^(e+1)) for
+    e >= -6 and 2^-9 below 2^-6 (subnormals)."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = np.signbit(x)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -6, 8)
+    q = np.exp2(e - 3)
+    v = np.rint(a / q) * q                      # numpy rint: ties to even
+    v = np.minimum(v, E4M3_MAX)
+    out = np.zeros(x.shape, dtype=np.uint8)
+    sub = v < 2.0 ** -6
+    out[sub] = np.rint(v[sub] / 2.0 ** -9).astype(np.uint8)
+    nz = ~sub
+    en = np.floor(np.log2(v[nz]))
+    man = np.rint((v[nz] / np.exp2(en) - 1.0) * 8).astype(np.int64)
+    out[nz] = ((en.astype(np.int64) + 7) << 3 | man).astype(np.uint8)
+    out[sign] |= np.uint8(0x80)
+    return out
+
+
+def e4m3_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    """FP8 E4M3 bit patterns -> binary64 (exact; NaN for S.1111.111)."""
+    b = np.asarray(b, dtype=np.uint8).astype(np.int64)
+    e = (b >> 3) & 0xF
+    m = b & 0x7
+    v = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7))
+    v = np.where((e == 0xF) & (m == 0x7), np.nan, v)
+    return np.where(b & 0x80, -v, v)
+
+
+def quantize_e4m3(x: np.ndarray):
+    """Per-tensor FP8: scale s = amax / 448 (binary32), patterns of x / s.
+    The quantized tensor stands for s * decode(patterns)."""
+    x = np.asarray(x, dtype=np.float32)
+    amax = float(np.max(np.abs(x))) if x.size else 0.0
+    s = np.float32(amax / E4M3_MAX) if amax > 0 else np.float32(1.0)
+    return f32_to_e4m3_bits(x.astype(np.float64) / float(s)), float(s)
+
+
+def make_inputs_fp8(w: Workload):
+    """FP8 E4M3 versions of the same draws: (A8, W1_8, W2_8, s_a, s_w1, s_w2)."""
+    a8, sa = quantize_e4m3(make_A_f32(w))
+    w18, s1 = quantize_e4m3(make_W_f32(w, 1))
+    w28, s2 = quantize_e4m3(make_W_f32(w, 2))
+    return a8, w18, w28, sa, s1, s2
+
+
+def random_case_fp8(M: int, N: int, K: int, seed: int, a_scale: float = 1.0):
+    """A small seeded FP8 case: (A8, W1_8, W2_8, s_a, s_w1, s_w2)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    a = rng.standard_normal(size=(M, K), dtype=np.float32) * np.float32(a_scale)
+    s = np.float32(float(max(K, 1)) ** -0.5)
+    w1 = rng.standard_normal(size=(K, N), dtype=np.float32) * s
+    w2 = rng.standard_normal(size=(K, N), dtype=np.float32) * s
+    a8, sa = quantize_e4m3(a)
+    w18, s1 = quantize_e4m3(w1)
+    w28, s2 = quantize_e4m3(w2)
+    return a8, w18, w28, sa, s1, s2
 
 
 def make_W3(w: Workload) -> np.ndarray:

@@ -2,13 +2,16 @@
 """Benchmark of the fused SwiGLU up-projection Y = SiLU(A x W1) (.) (A x W2).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--workload LABEL]
+                    [--workload LABEL] [--dtype bf16|fp8]
 
 One step = one call of swiglu_up_forward (the whole fused path: both GEMMs,
 the activation and the BF16 store) over one batch of M tokens. Default
 workload: the Qwen-2.5-1.5B-shaped up-projection, M=2048, K=1536, N=8960.
 Inputs are seeded synthetic data (workloads/), generated once and resident in
-HBM before the timed region. Consecutive steps rotate over several copies of
+HBM before the timed region. `--dtype fp8` runs swiglu_up_forward_fp8 on the
+E4M3 quantization of the same draws (per-tensor scales, BF16 Y); its tensor
+roofline is the measured BF16 peak times the nominal FP8/BF16 ratio of 2.
+Consecutive steps rotate over several copies of
 A, the packed weights and Y whose total exceeds twice the L2 size, so no step
 finds its operands in L2.
 
@@ -59,14 +62,15 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_label: str):
+def recorded_traffic(workload_label: str, dtype: str = "bf16"):
     """DRAM bytes per launch of the fused kernel from the committed ncu summary,
     only if it was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
+    key = workload_label if dtype == "bf16" else "%s/%s" % (workload_label, dtype)
     try:
         with open(path) as f:
             d = json.load(f)
-        rec = d.get("workloads", {}).get(workload_label)
+        rec = d.get("workloads", {}).get(key)
         if rec and d.get("kernel_source_hash") == kernel_source_hash():
             return float(rec["dram_bytes_per_launch"])
     except Exception:
@@ -74,13 +78,29 @@ def recorded_traffic(workload_label: str):
     return None
 
 
-def roofline_us(w, peaks):
-    return max(w.flops / (peaks["bf16_tflops"] * 1e12), w.roofline_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
+FP8_OVER_BF16 = 2.0      # nominal dense tensor rate ratio (4.5 vs 2.25 PFLOP/s)
 
 
-def bound_of(w, peaks) -> str:
-    t_tc = w.flops / (peaks["bf16_tflops"] * 1e12)
-    t_hbm = w.roofline_bytes / (peaks["hbm_gbs"] * 1e9)
+def tensor_peak(peaks, dtype: str, key: str = "bf16_tflops") -> float:
+    return peaks[key] * (FP8_OVER_BF16 if dtype == "fp8" else 1.0)
+
+
+def algorithmic_bytes(w, dtype: str) -> int:
+    """Compulsory HBM bytes of one launch: A and both weights read once, Y
+    written once (element size 1 for FP8 inputs, 2 for BF16; Y is BF16)."""
+    if dtype == "fp8":
+        return w.M * w.K + 2 * w.K * w.N + 2 * w.M * w.N
+    return w.roofline_bytes
+
+
+def roofline_us(w, peaks, dtype: str = "bf16"):
+    return max(w.flops / (tensor_peak(peaks, dtype) * 1e12),
+               algorithmic_bytes(w, dtype) / (peaks["hbm_gbs"] * 1e9)) * 1e6
+
+
+def bound_of(w, peaks, dtype: str = "bf16") -> str:
+    t_tc = w.flops / (tensor_peak(peaks, dtype) * 1e12)
+    t_hbm = algorithmic_bytes(w, dtype) / (peaks["hbm_gbs"] * 1e9)
     return "tensor" if t_tc >= t_hbm else "hbm"
 
 
@@ -183,27 +203,35 @@ def aggregate_value(flops_per_step: float, steps: int, world: int, elapsed_max_s
 
 
 # ----------------------------------------------------------------------------- CPU oracle legs
-def oracle_sample_rate(w, A, W1, W2, rows: int, cols: int, threads: int = 0):
+def oracle_inputs(w, dtype: str):
+    """The workload's inputs as the oracle takes them: (A, W1, W2) BF16 bits,
+    or (A8, W1_8, W2_8, s_a, s_w1, s_w2) for FP8."""
+    import workloads
+    return workloads.make_inputs_fp8(w) if dtype == "fp8" else workloads.make_inputs(w)
+
+
+def oracle_sample_rate(w, inputs, rows: int, cols: int, threads: int = 0):
     """Times the oracle on `rows` rows x `cols` columns; returns (seconds, flops)."""
     import numpy as np
 
     import oracle
     rng = np.random.Generator(np.random.PCG64(77))
     r = np.sort(rng.choice(w.M, size=min(rows, w.M), replace=False))
+    fn = oracle.swiglu_up_fp8 if len(inputs) == 6 else oracle.swiglu_up
     t0 = time.perf_counter()
-    oracle.swiglu_up(A, W1, W2, rows=r, cols=(0, cols), nthreads=threads)
+    fn(*inputs, rows=r, cols=(0, cols), nthreads=threads)
     dt = time.perf_counter() - t0
     return dt, 4.0 * len(r) * cols * w.K
 
 
-def cpu_baseline(w, A, W1, W2, target_s: float = 12.0):
+def cpu_baseline(w, inputs, target_s: float = 12.0):
     """The oracle as it stands, on every host core, on a bounded row sample."""
     cores = len(os.sched_getaffinity(0))
-    dt, fl = oracle_sample_rate(w, A, W1, W2, rows=cores, cols=w.N)
+    dt, fl = oracle_sample_rate(w, inputs, rows=cores, cols=w.N)
     rows_per_s = cores / dt
     rows = int(min(w.M, max(cores, (target_s - dt) * rows_per_s)))
     rows = max(cores, rows // cores * cores)
-    dt2, fl2 = oracle_sample_rate(w, A, W1, W2, rows=rows, cols=w.N)
+    dt2, fl2 = oracle_sample_rate(w, inputs, rows=rows, cols=w.N)
     return {"value": fl2 / dt2 / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": "%d of %d rows x all %d columns (K=%d), %.1f s" % (rows, w.M, w.N, w.K, dt2)}
 
@@ -211,26 +239,23 @@ def cpu_baseline(w, A, W1, W2, target_s: float = 12.0):
 def run_reference(args, w):
     """Reference arm: the CPU oracle timed on this host's cores, one bounded
     sample of the workload per step."""
-    import numpy as np
-
-    import workloads
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    A, W1, W2 = workloads.make_inputs(w)
+    inputs = oracle_inputs(w, args.dtype)
     cores = len(os.sched_getaffinity(0))
     rows = min(cores, w.M)
     # size the per-step column block so that warmup + steps fit the budget
-    dt, _ = oracle_sample_rate(w, A, W1, W2, rows=rows, cols=min(w.N, 256))
+    dt, _ = oracle_sample_rate(w, inputs, rows=rows, cols=min(w.N, 256))
     per_col = dt / min(w.N, 256)
     budget = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)
     cols = int(max(8, min(w.N, budget / max(per_col, 1e-9))) // 8 * 8)
     for _ in range(args.warmup):
-        oracle_sample_rate(w, A, W1, W2, rows=rows, cols=cols)
+        oracle_sample_rate(w, inputs, rows=rows, cols=cols)
     t0 = time.perf_counter()
     flops = 0.0
     for _ in range(args.steps):
-        _, fl = oracle_sample_rate(w, A, W1, W2, rows=rows, cols=cols)
+        _, fl = oracle_sample_rate(w, inputs, rows=rows, cols=cols)
         flops += fl
     el = time.perf_counter() - t0
     value = flops / el / 1e12
@@ -239,7 +264,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / max(1, args.steps) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_of(w, None),
+        "data": "synthetic", "config": config_of(w, None, args.dtype),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -355,9 +380,11 @@ def time_mlp_context(w, W1, W2, sg, As, Wps, Ys, Wss, R, dev, stream, steps):
                     "silu*mul (Figure 1 of the pages measures this share on H100)"}
 
 
-def config_of(w, l2_note):
-    c = {"workload": "%s: M=%d tokens, K=%d, N=%d, A~N(0,1), W1/W2~N(0,1/K), BF16 in/out, FP32 accumulate"
-                     % (w.name, w.M, w.K, w.N),
+def config_of(w, l2_note, dtype: str = "bf16"):
+    io = ("FP8 E4M3 in (per-tensor amax/448 scales), BF16 out" if dtype == "fp8"
+          else "BF16 in/out")
+    c = {"workload": "%s: M=%d tokens, K=%d, N=%d, A~N(0,1), W1/W2~N(0,1/K), %s, FP32 accumulate"
+                     % (w.name, w.M, w.K, w.N, io),
          "M": w.M, "K": w.K, "N": w.N, "parallelism": "replicas"}
     if l2_note:
         c["l2"] = l2_note
@@ -383,24 +410,39 @@ def run_gb300(args, w):
     from tests.parity import to_device_bf16
 
     peaks, peaks_src = load_peaks()
-    A, W1, W2 = workloads.make_inputs(w)
-    A_d = to_device_bf16(A, dev)
-    Wp = sg.swiglu_pack_weights(to_device_bf16(W1, dev), to_device_bf16(W2, dev))
+    fp8 = args.dtype == "fp8"
+    inputs = oracle_inputs(w, args.dtype)
+    if fp8:
+        A, W18, W28, s_a, s_w1, s_w2 = inputs
+        A_d = torch.from_numpy(A).to(dev)
+        Wp = sg.swiglu_pack_weights_fp8(torch.from_numpy(W18).to(dev), torch.from_numpy(W28).to(dev))
+        a_elem = 1
+    else:
+        A, W1, W2 = inputs
+        A_d = to_device_bf16(A, dev)
+        Wp = sg.swiglu_pack_weights(to_device_bf16(W1, dev), to_device_bf16(W2, dev))
+        a_elem = 2
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    per_set = w.M * w.K * 2 + Wp.numel() + w.M * w.N * 2
+    per_set = w.M * w.K * a_elem + Wp.numel() + w.M * w.N * 2
     R = max(2, -(-2 * l2 // per_set))
     As = [A_d] + [A_d.clone() for _ in range(R - 1)]
     Wps = [Wp] + [Wp.clone() for _ in range(R - 1)]
     Ys = [torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
-    ws = sg.swiglu_workspace_bytes(w.M, w.N, w.K)
+    ws = (sg.swiglu_workspace_bytes_fp8 if fp8 else sg.swiglu_workspace_bytes)(w.M, w.N, w.K)
     Wss = [torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev) if ws else None for _ in range(R)]
     l2_note = "rotating %d input sets (%.0f MB total, > 2x the %.0f MB L2)" % (
         R, R * per_set / 1e6, l2 / 1e6)
     stream = torch.cuda.current_stream(dev)
 
+    def forward(j):
+        if fp8:
+            sg.swiglu_up_forward_fp8(As[j], Wps[j], w.N, s_a, s_w1, s_w2, Y=Ys[j],
+                                     workspace=Wss[j], stream=stream)
+        else:
+            sg.swiglu_up_forward(As[j], Wps[j], w.N, Y=Ys[j], workspace=Wss[j], stream=stream)
+
     def step(i):
-        j = i % R
-        sg.swiglu_up_forward(As[j], Wps[j], w.N, Y=Ys[j], workspace=Wss[j], stream=stream)
+        forward(i % R)
 
     sampler = ClockSampler(local)
     time.sleep(0.3)
@@ -440,7 +482,8 @@ def run_gb300(args, w):
     # consecutive steps overlap on three streams; slot j's device buffers are
     # reused only after step j-R has finished with them (events).
     Ke = min(K, 2000)
-    A_h = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).pin_memory()
+    A_h = (torch.from_numpy(A) if fp8 else
+           torch.from_numpy(A.view(np.int16)).view(torch.bfloat16)).pin_memory()
     Y_h = [torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory() for _ in range(R)]
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
@@ -459,7 +502,7 @@ def run_gb300(args, w):
         stream.wait_event(ev_in[j])
         if used[j]:
             stream.wait_event(ev_out[j])         # Y slot free once its copy-out is done
-        sg.swiglu_up_forward(As[j], Wps[j], w.N, Y=Ys[j], workspace=Wss[j], stream=stream)
+        forward(j)
         ev_comp[j].record(stream)
         s_out.wait_event(ev_comp[j])
         with torch.cuda.stream(s_out):
@@ -495,7 +538,7 @@ def run_gb300(args, w):
         raise RuntimeError("e2e loop: copied-out Y differs from the device result")
 
     unfused = mlp = None
-    if not args.no_context:
+    if not args.no_context and not fp8:
         unfused = time_unfused_context(w, W1, W2, As, Ys, R, dev, stream, min(K, 2000), value)
         mlp = time_mlp_context(w, W1, W2, sg, As, Wps, Ys, Wss, R, dev, stream, min(K, 500))
 
@@ -505,29 +548,33 @@ def run_gb300(args, w):
             dist.destroy_process_group()
         return 0
 
-    bound = bound_of(w, peaks)
+    bound = bound_of(w, peaks, args.dtype)
+    abytes = algorithmic_bytes(w, args.dtype)
     if bound == "tensor":
         achieved = w.flops / avg_launch / 1e12
-        peak = peaks["bf16_tflops"]
+        peak = tensor_peak(peaks, args.dtype)
+        src = ("%s burst bf16 x %g (nominal fp8/bf16 ratio)" % (peaks_src, FP8_OVER_BF16) if fp8
+               else "%s burst bf16" % peaks_src)
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_source": "%s burst bf16" % peaks_src,
-                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
+                "frac": achieved / peak, "peak_source": src,
+                "frac_of_sustained": achieved / tensor_peak(peaks, args.dtype,
+                                                            "bf16_tflops_sustained")}
     else:
-        achieved = w.roofline_bytes / avg_launch / 1e9
+        achieved = abytes / avg_launch / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": "%s copy bandwidth" % peaks_src}
-    roof["traffic"] = recorded_traffic(w.c)
-    roof["algorithmic_per_launch"] = w.flops if bound == "tensor" else w.roofline_bytes
+    roof["traffic"] = recorded_traffic(w.c, args.dtype)
+    roof["algorithmic_per_launch"] = w.flops if bound == "tensor" else abytes
     roof["avg_launch_us"] = avg_launch * 1e6
-    roof["frac_of_roofline_time"] = roofline_us(w, peaks) * 1e-6 / avg_launch
+    roof["frac_of_roofline_time"] = roofline_us(w, peaks, args.dtype) * 1e-6 / avg_launch
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": elapsed_max / K * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, l2_note), "roofline": roof,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": w.M * w.K * 2,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3" if fp8 else "bf16",
+        "data": "synthetic", "config": config_of(w, l2_note, args.dtype), "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": w.M * w.K * a_elem,
                 "d2h_bytes_per_step": w.M * w.N * 2, "steps": Ke,
                 "ms_per_step": e_el / Ke * 1e3,
                 "how": "pinned host A -> device, forward, device Y -> pinned host, every step; "
@@ -539,7 +586,7 @@ def run_gb300(args, w):
     if mlp is not None:
         line["context_mlp"] = mlp
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, A, W1, W2)
+        line["cpu_baseline"] = cpu_baseline(w, inputs)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -558,6 +605,8 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-context", action="store_true",
                    help="skip timing the unfused PyTorch path (context only)")
+    p.add_argument("--dtype", choices=("bf16", "fp8"), default="bf16",
+                   help="input type: bf16, or fp8 (E4M3 with per-tensor scales)")
     p.add_argument("--variant", choices=("auto", "1sm", "2sm"), default="auto",
                    help="fused kernel: auto (2-SM pairs for M >= 256), or force one (ablation)")
     args = p.parse_args(argv)

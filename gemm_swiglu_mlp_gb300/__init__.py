@@ -33,7 +33,8 @@ __all__ = [
     "swiglu_packed_weight_bytes", "swiglu_pack_weights", "swiglu_pack_weights_nk",
     "swiglu_workspace_bytes",
     "swiglu_up_forward", "swiglu_up_forward_noalloc", "swiglu_check_device_status",
-    "EXPORTED_SYMBOLS",
+    "swiglu_packed_weight_bytes_fp8", "swiglu_pack_weights_fp8", "swiglu_workspace_bytes_fp8",
+    "swiglu_up_forward_fp8", "EXPORTED_SYMBOLS",
 ]
 
 SWIGLU_OK = 0
@@ -46,12 +47,14 @@ EXPORTED_SYMBOLS = (
     "swiglu_version", "swiglu_status_string", "swiglu_packed_weight_bytes",
     "swiglu_pack_weights", "swiglu_pack_weights_nk", "swiglu_workspace_bytes",
     "swiglu_up_forward", "swiglu_up_forward_noalloc", "swiglu_check_device_status",
+    "swiglu_packed_weight_bytes_fp8", "swiglu_pack_weights_fp8", "swiglu_workspace_bytes_fp8",
+    "swiglu_up_forward_fp8",
 )
 
 _lock = threading.Lock()
 _lib = None
 _workspaces = {}   # (device index, stream handle) -> zero-initialised uint8 tensor
-_ws_bytes = {}     # (device index, M, N, K, kernel override) -> workspace bytes
+_ws_bytes = {}     # (device index, M, N, K, kernel and schedule overrides) -> workspace bytes
 
 
 class SwigluError(RuntimeError):
@@ -88,6 +91,15 @@ def load_library(path: str = LIB_PATH):
         lib.swiglu_up_forward.restype = ctypes.c_int
         lib.swiglu_up_forward_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         lib.swiglu_up_forward_noalloc.restype = ctypes.c_int
+        lib.swiglu_packed_weight_bytes_fp8.argtypes = [i64, i64]
+        lib.swiglu_packed_weight_bytes_fp8.restype = sz
+        lib.swiglu_pack_weights_fp8.argtypes = [vp, vp, i64, i64, vp, vp]
+        lib.swiglu_pack_weights_fp8.restype = ctypes.c_int
+        lib.swiglu_workspace_bytes_fp8.argtypes = [i64, i64, i64]
+        lib.swiglu_workspace_bytes_fp8.restype = sz
+        f32 = ctypes.c_float
+        lib.swiglu_up_forward_fp8.argtypes = [vp, vp, vp, i64, i64, i64, f32, f32, f32, vp, sz, vp]
+        lib.swiglu_up_forward_fp8.restype = ctypes.c_int
         lib.swiglu_check_device_status.argtypes = [vp, u32p]
         lib.swiglu_check_device_status.restype = ctypes.c_int
         _lib = lib
@@ -200,7 +212,8 @@ def swiglu_up_forward(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: torch.T
         prev = torch.cuda.current_device()
         torch.cuda.set_device(dev)
     try:
-        key = (dev, M, N, K, os.environ.get("SWIGLU_FUSED_VARIANT"))
+        key = (dev, M, N, K, os.environ.get("SWIGLU_FUSED_VARIANT"),
+               os.environ.get("SWIGLU_SCHEDULE"))
         ws_need = _ws_bytes.get(key)
         if ws_need is None:
             ws_need = _ws_bytes[key] = swiglu_workspace_bytes(M, N, K)
@@ -249,6 +262,68 @@ def swiglu_up_forward_noalloc(A: torch.Tensor, Wpacked: torch.Tensor, N: int,
         _check(lib.swiglu_up_forward_noalloc(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(),
                                              M, N, K, _stream_handle(stream)),
                "swiglu_up_forward_noalloc")
+    return Y
+
+
+def _require_u8_cuda(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != torch.uint8:
+        raise TypeError("%s must hold E4M3 bytes as uint8, got %s" % (name, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def swiglu_packed_weight_bytes_fp8(N: int, K: int) -> int:
+    return int(load_library().swiglu_packed_weight_bytes_fp8(int(N), int(K)))
+
+
+def swiglu_workspace_bytes_fp8(M: int, N: int, K: int) -> int:
+    return int(load_library().swiglu_workspace_bytes_fp8(int(M), int(N), int(K)))
+
+
+def swiglu_pack_weights_fp8(W1: torch.Tensor, W2: torch.Tensor, Wpacked: torch.Tensor = None,
+                            stream=None) -> torch.Tensor:
+    """Pack FP8 E4M3 weights W1, W2 ([K, N] uint8 bytes each)."""
+    lib = load_library()
+    _require_u8_cuda(W1, "W1")
+    _require_u8_cuda(W2, "W2")
+    if W1.dim() != 2 or W1.shape != W2.shape:
+        raise ValueError("W1 and W2 must both be [K, N]")
+    K, N = W1.shape
+    nbytes = swiglu_packed_weight_bytes_fp8(N, K)
+    if Wpacked is None:
+        Wpacked = torch.empty(nbytes, dtype=torch.uint8, device=W1.device)
+    with torch.cuda.device(W1.device):
+        _check(lib.swiglu_pack_weights_fp8(W1.data_ptr(), W2.data_ptr(), K, N, Wpacked.data_ptr(),
+                                           _stream_handle(stream)), "swiglu_pack_weights_fp8")
+    return Wpacked
+
+
+def swiglu_up_forward_fp8(A: torch.Tensor, Wpacked: torch.Tensor, N: int, scale_a: float,
+                          scale_w1: float, scale_w2: float, Y: torch.Tensor = None,
+                          workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Y = SiLU(A W1) (.) (A W2) with A = scale_a*A8 ([M, K] E4M3 bytes) and
+    packed FP8 weights standing for scale_w1*W1_8 and scale_w2*W2_8."""
+    lib = load_library()
+    _require_u8_cuda(A, "A")
+    M, K = A.shape
+    N = int(N)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        _require_bf16_cuda(Y, "Y")
+    with torch.cuda.device(A.device):
+        ws_need = swiglu_workspace_bytes_fp8(M, N, K)
+        ws_ptr, ws_bytes = None, 0
+        if ws_need:
+            if workspace is None:
+                workspace = _default_workspace(A.device, ws_need, stream)
+            ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+        _check(lib.swiglu_up_forward_fp8(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(), M, N, K,
+                                         float(scale_a), float(scale_w1), float(scale_w2),
+                                         ws_ptr, ws_bytes, _stream_handle(stream)),
+               "swiglu_up_forward_fp8")
     return Y
 
 

@@ -22,6 +22,35 @@ enum : unsigned int {
     kStatusDrainTimeout = 8u,
 };
 
+// Input element types. A shared-memory row is always 128 bytes (one
+// 128-byte swizzle row): 64 BF16 or 128 FP8 values per k-block, and one
+// UMMA consumes 32 bytes of each row (K = 16 BF16 or 32 FP8), four per
+// k-block either way.
+struct ElemBF16 {
+    static constexpr int kBK = 64;       // elements per k-block
+    static constexpr bool kFp8 = false;
+    __host__ __device__ static constexpr uint32_t idesc(int M, int N) { return idesc_bf16_f32(M, N); }
+    __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        umma_bf16(d, a, b, id, acc);
+    }
+    __device__ static void mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        umma_bf16_pair(d, a, b, id, acc);
+    }
+};
+struct ElemE4M3 {
+    static constexpr int kBK = 128;
+    static constexpr bool kFp8 = true;
+    __host__ __device__ static constexpr uint32_t idesc(int M, int N) { return idesc_e4m3_f32(M, N); }
+    __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        umma_f8(d, a, b, id, acc);
+    }
+    __device__ static void mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        umma_f8_pair(d, a, b, id, acc);
+    }
+};
+constexpr int kRowBytes = 128;   // bytes per shared-memory row of a k-block
+constexpr int kKSteps = 4;       // UMMAs per k-block (32 bytes of each row apiece)
+
 // FP32 Gate|Up partial of one tile in the workspace: 256 columns (Gate
 // 0..127, Up 128..255) x slot_rows rows, column-major so that the 32 lanes of
 // a warp (32 consecutive rows) touch 128 contiguous bytes per column.
@@ -37,6 +66,8 @@ struct FusedArgs {
     int stage_tx_bytes;       // bytes one stage's TMA loads deliver (A box + weight tile)
     int a_tx_bytes;           // the A box's share of it
     uint16_t *Y;              // Y [M, N] row-major BF16 (direct stores of column sub-tiles)
+    float gate_scale;         // Gate = gate_scale * accumulator (FP8: s_a * s_w1; BF16: 1)
+    float up_scale;           // Up = up_scale * accumulator (FP8: s_a * s_w2; BF16: 1)
     int slot_rows;            // rows per workspace slot
     WorkSched sched;
     float *partials;          // 2 * grid slots of kSlotCols * slot_rows floats (stream-K only)
@@ -85,16 +116,17 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
 }
 
 // y for 32 consecutive columns [c, c+32) of this thread's row, from FP32 Gate
-// and Up values, written as BF16 into the warp's swizzled staging buffer.
+// and Up accumulators (times their scales), written as BF16 into the warp's
+// swizzled staging buffer.
 __device__ __forceinline__ void stage_y32(uint32_t ybuf, int lane, int c, const float (&g)[32],
-                                          const float (&u)[32]) {
+                                          const float (&u)[32], float gs, float us) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int i = 8 * j + 2 * e;
-            w[e] = pack_bf16x2(silu_mul(g[i], u[i]), silu_mul(g[i + 1], u[i + 1]));
+            w[e] = pack_bf16x2(silu_mul(g[i] * gs, u[i] * us), silu_mul(g[i + 1] * gs, u[i + 1] * us));
         }
         // 128-byte swizzle: 16-byte chunk index XOR (row % 8)
         const int col = c + 8 * j;
@@ -142,7 +174,8 @@ __device__ __forceinline__ void epilogue_subtile_store(uint32_t tbase, int width
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = 8 * j + 2 * e;
-                    w[e] = pack_bf16x2(silu_mul(g[i], v[i]), silu_mul(g[i + 1], v[i + 1]));
+                    w[e] = pack_bf16x2(silu_mul(g[i] * args.gate_scale, v[i] * args.up_scale),
+                                       silu_mul(g[i + 1] * args.gate_scale, v[i + 1] * args.up_scale));
                 }
                 *reinterpret_cast<uint4 *>(dst + 8 * j) = make_uint4(w[0], w[1], w[2], w[3]);
             }

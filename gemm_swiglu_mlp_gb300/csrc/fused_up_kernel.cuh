@@ -50,7 +50,7 @@ template <int STAGES>
 struct FusedCfg {
     static constexpr int BM = 128;                // token rows per tile = UMMA M
     static constexpr int BN = 128;                // output columns per tile
-    static constexpr int BK = 64;                 // K per stage: 128-byte rows
+    static constexpr int BK = 64;                 // BF16 elements per 128-byte row
     static constexpr int UMMA_N = 2 * BN;         // Gate | Up
     static constexpr int UMMA_K = 16;
     static constexpr int A_BYTES = BM * BK * 2;   // 16 KB
@@ -73,7 +73,7 @@ struct FusedCfg {
     static_assert(UMMA_N == kSlotCols, "workspace slot shape");
 };
 
-template <int STAGES>
+template <int STAGES, typename E>
 __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
     fused_up_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -166,17 +166,17 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                     if (u.width == C::BN) {
                         mbar_arrive_expect_tx(full_bar(stage), args.stage_tx_bytes);
                         tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
-                                    kb * C::BK, mb * C::BM);
+                                    kb * E::kBK, mb * C::BM);
                         tma_load_3d(b_dst, &tmB, full_bar(stage), 0, 0, wtile);
                     } else {
                         // column sub-tile: its Gate rows, then the matching Up rows
                         const CUtensorMap *tmBn = (u.width == 64) ? &tmB64 : &tmB32;
                         mbar_arrive_expect_tx(full_bar(stage),
-                                              args.a_tx_bytes + 2 * u.width * C::BK * 2);
+                                              args.a_tx_bytes + 2 * u.width * kRowBytes);
                         tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
-                                    kb * C::BK, mb * C::BM);
+                                    kb * E::kBK, mb * C::BM);
                         tma_load_3d(b_dst, tmBn, full_bar(stage), 0, u.sub * u.width, wtile);
-                        tma_load_3d(b_dst + u.width * C::BK * 2, tmBn, full_bar(stage), 0,
+                        tma_load_3d(b_dst + u.width * kRowBytes, tmBn, full_bar(stage), 0,
                                     C::BN + u.sub * u.width, wtile);
                     }
                     issued_mask |= 1u << stage;
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(C::BM, C::UMMA_N);
+            constexpr uint32_t idesc = E::idesc(C::BM, C::UMMA_N);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::UMMA_N);
                 // Gate|Up columns of this unit: 256, or 2 x the sub-tile width
                 const uint32_t idesc_u =
-                    (u.width == C::BN) ? idesc : idesc_bf16_f32(C::BM, 2 * u.width);
+                    (u.width == C::BN) ? idesc : E::idesc(C::BM, 2 * u.width);
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
                         ok = false;
@@ -222,10 +222,10 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                     const uint64_t a_desc = smem_desc_k128(sbase + C::OFF_A + stage * C::A_BYTES);
                     const uint64_t b_desc = smem_desc_k128(sbase + C::OFF_B + stage * C::B_BYTES);
 #pragma unroll
-                    for (int k = 0; k < C::BK / C::UMMA_K; ++k) {
+                    for (int k = 0; k < kKSteps; ++k) {
                         // +32 bytes along K per step inside the 128-byte swizzle row
-                        umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc_u,
-                                  (kb != u.kb0 || k != 0) ? 1u : 0u);
+                        E::mma(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc_u,
+                               (kb != u.kb0 || k != 0) ? 1u : 0u);
                     }
                     umma_commit(empty_bar(stage));
                     if (++stage == STAGES) {
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                     for (int c = 0; c < C::BN; c += 32) {
                         float g[32], v[32];
                         tmem_ld_gu(tbase, c, g, v);
-                        stage_y32(ybuf, lane, c, g, v);
+                        stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
                     }
                 }
                 tc_fence_before();
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                                     v[i] = (k == c_lo) ? pu : v[i] + pu;
                                 }
                             }
-                            stage_y32(ybuf, lane, c, g, v);
+                            stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
                         }
                     }
                     if (leader) args.counters[u.sk] = 0u;  // ready for the next launch

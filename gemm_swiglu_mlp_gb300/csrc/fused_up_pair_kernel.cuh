@@ -62,7 +62,7 @@ struct PairCfg {
     static_assert(UMMA_N == kSlotCols, "workspace slot shape");
 };
 
-template <int STAGES>
+template <int STAGES, typename E>
 __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     fused_up_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
@@ -162,9 +162,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                     // a column sub-tile loads only its Gate (leader) or Up (peer) rows
                     const int brows = u.width;
                     if (is_leader)
-                        mbar_arrive_expect_tx(full_bar(stage), 2 * (C::A_BYTES + brows * C::BK * 2));
+                        mbar_arrive_expect_tx(full_bar(stage), 2 * (C::A_BYTES + brows * kRowBytes));
                     const uint32_t bar = mapa_shared(full_bar(stage), 0);
-                    tma_load_2d_pair(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, bar, kb * C::BK,
+                    tma_load_2d_pair(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, bar, kb * E::kBK,
                                      pm * C::UMMA_M + C::BM * static_cast<int>(rank));
                     const CUtensorMap *tmBu =
                         (brows == C::BN) ? &tmB : (brows == 64 ? &tmB64 : &tmB32);
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0 && is_leader) {
-            constexpr uint32_t idesc = idesc_bf16_f32(C::UMMA_M, C::UMMA_N);
+            constexpr uint32_t idesc = E::idesc(C::UMMA_M, C::UMMA_N);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::UMMA_N);
                 const uint32_t idesc_u =
-                    (u.width == C::BN) ? idesc : idesc_bf16_f32(C::UMMA_M, 2 * u.width);
+                    (u.width == C::BN) ? idesc : E::idesc(C::UMMA_M, 2 * u.width);
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
                         ok = false;
@@ -213,9 +213,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                     const uint64_t a_desc = smem_desc_k128(sbase + C::OFF_A + stage * C::A_BYTES);
                     const uint64_t b_desc = smem_desc_k128(sbase + C::OFF_B + stage * C::B_BYTES);
 #pragma unroll
-                    for (int k = 0; k < C::BK / C::UMMA_K; ++k)
-                        umma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc_u,
-                                       (kb != u.kb0 || k != 0) ? 1u : 0u);
+                    for (int k = 0; k < kKSteps; ++k)
+                        E::mma_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc_u,
+                                    (kb != u.kb0 || k != 0) ? 1u : 0u);
                     umma_commit_pair_mc(empty_bar(stage), 0x3);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                     for (int c = 0; c < C::BN; c += 32) {
                         float g[32], v[32];
                         tmem_ld_gu(tbase, c, g, v);
-                        stage_y32(ybuf, lane, c, g, v);
+                        stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
                     }
                 }
                 tc_fence_before();
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                                     v[i] = (p == c_lo) ? pu : v[i] + pu;
                                 }
                             }
-                            stage_y32(ybuf, lane, c, g, v);
+                            stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
                         }
                     }
                     if (lead_thread) *counter = 0u;

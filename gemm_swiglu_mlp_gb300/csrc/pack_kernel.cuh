@@ -1,6 +1,7 @@
-// Weight packing: W1, W2 [K, N] row-major BF16 -> Wpacked, tile-contiguous.
+// Weight packing: W1, W2 [K, N] row-major -> Wpacked, tile-contiguous.
 //
-// Wpacked is [NB][KB][256][64] BF16 with NB = ceil(N/128), KB = ceil(K/64):
+// BF16: Wpacked is [NB][KB][256][64] with NB = ceil(N/128), KB = ceil(K/64)
+// (FP8: [NB][KB][256][128], KB = ceil(K/128); the same 128-byte rows):
 // element (j, b, r, kk) is W1[64b + kk][128j + r] for r < 128 (Gate) and
 // W2[64b + kk][128j + r - 128] for r >= 128 (Up); zero where the column is
 // >= N or the k index is >= K. One (j, b) tile is one contiguous 32 KB block
@@ -18,34 +19,36 @@ namespace swiglu {
 
 constexpr int kPackTile = 64;
 
-// One CTA transposes a 64 (k) x 64 (n) tile through shared memory: reads
-// are coalesced along n, and the 64 packed rows it writes (64 x 128 bytes)
-// are one contiguous 8 KB run of the output.
-__global__ void __launch_bounds__(256) pack_weights_kernel(const uint16_t *__restrict__ W1,
-                                                            const uint16_t *__restrict__ W2,
-                                                            uint16_t *__restrict__ Wp, int K,
-                                                            int N, int KB) {
-    __shared__ uint16_t tile[kPackTile][kPackTile + 2];
+// One CTA transposes a KT (k) x 64 (n) tile through shared memory: reads are
+// coalesced along n, and the 64 packed rows it writes (64 x 128 bytes) are
+// one contiguous 8 KB run of the output. T = uint16_t with KT = 64 packs
+// BF16 weights; T = uint8_t with KT = 128 packs FP8 weights into the same
+// byte geometry (128-byte rows).
+template <typename T, int KT>
+__global__ void __launch_bounds__(256) pack_weights_kernel(const T *__restrict__ W1,
+                                                            const T *__restrict__ W2,
+                                                            T *__restrict__ Wp, int K, int N,
+                                                            int KB) {
+    __shared__ T tile[KT][kPackTile + 2];
     const int b = blockIdx.x;                // k-block
-    const int k0 = b * kPackTile;
+    const int k0 = b * KT;
     const int p0 = blockIdx.y * kPackTile;   // first packed row (over all 2*Np rows)
     const int j = p0 / 256;                  // output-column block
     const int r0 = p0 % 256;                 // 64-row chunks never straddle Gate/Up halves
     const bool up = r0 >= 128;
     const int n0 = 128 * j + (r0 & 127);
-    const uint16_t *__restrict__ W = up ? W2 : W1;
+    const T *__restrict__ W = up ? W2 : W1;
 
-    for (int i = threadIdx.x; i < kPackTile * kPackTile; i += blockDim.x) {
+    for (int i = threadIdx.x; i < KT * kPackTile; i += blockDim.x) {
         const int kk = i / kPackTile, nn = i % kPackTile;
         const int k = k0 + kk, n = n0 + nn;
-        tile[kk][nn] = (k < K && n < N) ? W[static_cast<int64_t>(k) * N + n] : uint16_t(0);
+        tile[kk][nn] = (k < K && n < N) ? W[static_cast<int64_t>(k) * N + n] : T(0);
     }
     __syncthreads();
-    uint16_t *__restrict__ out =
-        Wp + ((static_cast<int64_t>(j) * KB + b) * 256 + r0) * kPackTile;
-    for (int i = threadIdx.x; i < kPackTile * kPackTile; i += blockDim.x) {
-        const int nn = i / kPackTile, kk = i % kPackTile;
-        out[nn * kPackTile + kk] = tile[kk][nn];
+    T *__restrict__ out = Wp + ((static_cast<int64_t>(j) * KB + b) * 256 + r0) * KT;
+    for (int i = threadIdx.x; i < KT * kPackTile; i += blockDim.x) {
+        const int nn = i / KT, kk = i % KT;
+        out[nn * KT + kk] = tile[kk][nn];
     }
 }
 

@@ -145,8 +145,17 @@ struct UnitIter {
 // weight-streaming shapes a short last wave loses little: its CTAs get more
 // bandwidth each. `min_sk_iters` keeps every CTA's stream-K share at a few
 // k-blocks so tiles are not cut into slivers.
+// Schedule choice: kSchedAuto is the rule above; the others force one form
+// (for ablations and tests): whole tiles only, the column-split tail, the
+// stream-K split of the last full wave plus the remainder, or the stream-K
+// split of the remainder alone (the tiles past the last full wave; one more
+// wave joins when the remainder gives a CTA fewer than min_sk_iters).
+enum SchedMode { kSchedAuto = 0, kSchedDataParallel = 1, kSchedColumnSplit = 2,
+                 kSchedStreamK = 3, kSchedStreamKTail = 4 };
+
 inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_count,
-                               int group_m, int min_sk_iters = 4, bool weight_bound = false) {
+                               int group_m, int min_sk_iters = 4, bool weight_bound = false,
+                               int mode = kSchedAuto) {
     WorkSched s{};
     s.num_tiles = m_tiles * n_tiles;
     s.k_blocks = k_blocks;
@@ -159,7 +168,22 @@ inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_co
     const double eff_dp = static_cast<double>(T) / (static_cast<double>(waves) * G);
     const int full = (T / G) * G;   // tiles in complete waves
     const int tail = T - full;
-    if (eff_dp < 0.95 && tail > 0) {
+    if (mode == kSchedDataParallel || (mode != kSchedAuto && tail == 0)) {
+        s.grid = T < G ? T : G;
+        s.dp_tiles = T;
+        s.sk_iters = 0;
+        return s;
+    }
+    if (mode == kSchedStreamKTail && full > 0) {
+        s.grid = G;
+        s.dp_tiles = full;
+        if (static_cast<long long>(tail) * k_blocks <
+            static_cast<long long>(G) * (min_sk_iters > 0 ? min_sk_iters : 1))
+            s.dp_tiles -= G;
+        s.sk_iters = static_cast<long long>(T - s.dp_tiles) * k_blocks;
+        return s;
+    }
+    if ((mode == kSchedAuto && eff_dp < 0.95 && tail > 0) || mode == kSchedColumnSplit) {
         int best = 1;
         double best_eff = eff_dp;
         for (int split = 2; split <= 4; split *= 2) {
@@ -173,7 +197,8 @@ inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_co
             }
         }
         const bool take = weight_bound ? best_eff >= 0.9 : (best_eff >= 0.85 && 2 * T < G);
-        if (best > 1 && take) {
+        if (mode == kSchedColumnSplit && best == 1) best = 2;
+        if (best > 1 && (take || mode == kSchedColumnSplit)) {
             s.grid = G;
             s.dp_tiles = full;
             s.n_split = best;
@@ -181,7 +206,7 @@ inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_co
             return s;
         }
     }
-    if (eff_dp >= 0.85) {
+    if (mode == kSchedAuto && eff_dp >= 0.85) {
         // data-parallel: every tile whole, no workspace
         s.grid = T < G ? T : G;
         s.dp_tiles = T;

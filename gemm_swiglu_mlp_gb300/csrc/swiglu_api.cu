@@ -92,10 +92,16 @@ int device_setup(int *dev_out, DeviceState **st_out) {
             st.status = SWIGLU_ERR_UNSUPPORTED;
             return;
         }
-        if (cudaFuncSetAttribute(fused_up_kernel<kFusedStages>,
+        if (cudaFuncSetAttribute(fused_up_kernel<kFusedStages, ElemBF16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  FusedC::SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages>,
+            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PairC::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_kernel<kFusedStages, ElemE4M3>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 FusedC::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemE4M3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairC::SMEM_BYTES) != cudaSuccess) {
             cudaGetLastError();
@@ -115,7 +121,8 @@ int device_setup(int *dev_out, DeviceState **st_out) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, fused_up_pair_kernel<kPairStages>, &cfg) !=
+        if (cudaOccupancyMaxActiveClusters(&clusters, fused_up_pair_kernel<kPairStages, ElemBF16>,
+                                           &cfg) !=
                 cudaSuccess ||
             clusters < 1) {
             cudaGetLastError();
@@ -145,15 +152,27 @@ int current_sm_count() {
 
 // Schedule of one call. `workers` = CTAs (1-SM kernel) or CTA pairs (2-SM
 // kernel) that run at once; a 2-SM tile has 256 rows.
-WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, bool pair) {
+// SWIGLU_SCHEDULE=dp|split|sk|sk-tail forces one schedule form (ablations);
+// unset or anything else: the automatic choice.
+int schedule_mode() {
+    const char *v = std::getenv("SWIGLU_SCHEDULE");
+    if (!v) return kSchedAuto;
+    if (std::strcmp(v, "dp") == 0) return kSchedDataParallel;
+    if (std::strcmp(v, "split") == 0) return kSchedColumnSplit;
+    if (std::strcmp(v, "sk") == 0) return kSchedStreamK;
+    if (std::strcmp(v, "sk-tail") == 0) return kSchedStreamKTail;
+    return kSchedAuto;
+}
+
+WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, bool pair, int kbk = 64) {
     const int rows = pair ? PairC::UMMA_M : FusedC::BM;
     const int m_tiles = static_cast<int>((M + rows - 1) / rows);
     const int n_tiles = static_cast<int>((N + FusedC::BN - 1) / FusedC::BN);
-    const int k_blocks = static_cast<int>((K + FusedC::BK - 1) / FusedC::BK);
+    const int k_blocks = static_cast<int>((K + kbk - 1) / kbk);
     // few token rows: the kernel streams weights (HBM-bound), see plan_schedule
     const bool weight_bound = M <= 128;
     return plan_schedule(m_tiles, n_tiles, k_blocks, workers, pair ? kGroupM / 2 : kGroupM,
-                         kMinStreamKIters, weight_bound);
+                         kMinStreamKIters, weight_bound, schedule_mode());
 }
 
 // Workspace layout: a counter region at offset 0 whose size depends only on
@@ -183,35 +202,41 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     return a0 < b0 + nb && b0 < a0 + na;
 }
 
-// Tensor map over the tile-contiguous packed weights [tiles][256][64]: a box
-// is box_rows x 64 of one tile (the whole 32 KB tile for the 1-SM kernel, the
-// Gate or the Up half for one CTA of a pair), 128-byte swizzled.
-bool encode_packed_weights(CUtensorMap *m, const void *base, uint64_t tiles, uint32_t box_rows) {
+// Tensor map over the tile-contiguous packed weights [tiles][256][row]: a
+// box is box_rows rows of one tile (the whole 32 KB tile for the 1-SM kernel,
+// the Gate or the Up half for one CTA of a pair, or a column sub-tile's rows),
+// 128-byte swizzled. `elems` is the row length in elements (64 BF16 or 128
+// FP8 values: 128 bytes either way).
+bool encode_packed_weights(CUtensorMap *m, const void *base, uint64_t tiles, uint32_t box_rows,
+                           bool fp8) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {64, 256, tiles};
-    const cuuint64_t strides[2] = {64 * 2, 256 * 64 * 2};
-    const cuuint32_t box[3] = {64, box_rows, 1};
+    const uint64_t elems = fp8 ? 128 : 64;
+    const cuuint64_t dims[3] = {elems, 256, tiles};
+    const cuuint64_t strides[2] = {128, 256 * 128};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(elems), box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D BF16 tensor map over a row-major [rows, cols] matrix with a
-// 128-byte-swizzled box of box_rows x box_cols (box_cols * 2 <= 128 bytes).
-bool encode_bf16_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
-                    uint32_t box_cols, uint32_t box_rows) {
+// 2-D tensor map over a row-major [rows, cols] matrix of BF16 (2-byte) or
+// FP8 (1-byte) elements with a 128-byte-swizzled box of box_rows x box_cols
+// (box_cols * element size <= 128 bytes).
+bool encode_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+               uint32_t box_rows, bool fp8 = false) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return false;
+    const uint64_t esize = fp8 ? 1 : 2;
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint64_t strides[1] = {cols * esize};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -277,7 +302,7 @@ int swiglu_pack_weights(const void *W1, const void *W2, int64_t K, int64_t N, vo
     DeviceState *st;
     s = device_setup(&dev, &st);
     if (s != SWIGLU_OK) return s;
-    pack_weights_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+    pack_weights_kernel<uint16_t, 64><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t *>(W1), static_cast<const uint16_t *>(W2),
         static_cast<uint16_t *>(Wpacked), static_cast<int>(K), static_cast<int>(N),
         static_cast<int>(grid.x));
@@ -302,30 +327,46 @@ int swiglu_pack_weights_nk(const void *W1, const void *W2, int64_t N, int64_t K,
     return SWIGLU_OK;
 }
 
-size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+}  // extern "C"
+
+namespace swiglu {
+namespace {
+
+// Workspace bytes for a forward of element type E (same plan as the launch).
+template <typename E>
+size_t workspace_bytes_impl(int64_t M, int64_t N, int64_t K) {
     if (M < 1 || N < 1 || K < 1 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
         K >= (int64_t(1) << 31))
         return 0;
     const bool pair = use_pair_kernel(M);
     int dev;
     DeviceState *st;
-    if (device_setup(&dev, &st) == SWIGLU_OK)  // the same plan swiglu_up_forward will use
-        return workspace_bytes_for(plan_for(M, N, K, pair ? st->pair_clusters : st->sm_count, pair),
-                                   M, pair, st->sm_count);
+    if (device_setup(&dev, &st) == SWIGLU_OK)  // the same plan the forward will use
+        return workspace_bytes_for(
+            plan_for(M, N, K, pair ? st->pair_clusters : st->sm_count, pair, E::kBK), M, pair,
+            st->sm_count);
     const int sms = current_sm_count();         // no usable device: a size for its SM count
-    return workspace_bytes_for(plan_for(M, N, K, pair ? sms / 2 : sms, pair), M, pair, sms);
+    return workspace_bytes_for(plan_for(M, N, K, pair ? sms / 2 : sms, pair, E::kBK), M, pair,
+                               sms);
 }
 
-int swiglu_up_forward(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t N,
-                      int64_t K, void *workspace, size_t workspace_bytes, void *stream) {
+// The fused forward for element type E (BF16, or FP8 E4M3 with per-tensor
+// scales folded into gate_scale / up_scale). A and Wpacked hold E elements;
+// Y is BF16.
+template <typename E>
+int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t N, int64_t K,
+                 float gate_scale, float up_scale, void *workspace, size_t workspace_bytes,
+                 void *stream, size_t packed_bytes) {
+    const size_t esize = E::kFp8 ? 1 : 2;
+    const int64_t kmul = E::kFp8 ? 16 : 8;   // 16-byte rows of A
     if (!A || !Wpacked || !Y) return SWIGLU_ERR_INVALID_ARG;
-    if (M < 1 || N < 8 || K < 8 || (N % 8) != 0 || (K % 8) != 0) return SWIGLU_ERR_INVALID_ARG;
+    if (M < 1 || N < 8 || K < kmul || (N % 8) != 0 || (K % kmul) != 0) return SWIGLU_ERR_INVALID_ARG;
     const int64_t lim = int64_t(1) << 31;
     if (M >= lim || N >= lim || K >= lim) return SWIGLU_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(Wpacked) || !aligned16(Y)) return SWIGLU_ERR_INVALID_ARG;
     const size_t ybytes = static_cast<size_t>(M) * N * 2;
-    if (overlaps(Y, ybytes, A, static_cast<size_t>(M) * K * 2) ||
-        overlaps(Y, ybytes, Wpacked, swiglu_packed_weight_bytes(N, K)))
+    const size_t abytes = static_cast<size_t>(M) * K * esize;
+    if (overlaps(Y, ybytes, A, abytes) || overlaps(Y, ybytes, Wpacked, packed_bytes))
         return SWIGLU_ERR_INVALID_ARG;
     const int64_t tiles = ((M + FusedC::BM - 1) / FusedC::BM) * ((N + FusedC::BN - 1) / FusedC::BN);
     if (tiles >= lim) return SWIGLU_ERR_UNSUPPORTED;
@@ -336,15 +377,15 @@ int swiglu_up_forward(const void *A, const void *Wpacked, void *Y, int64_t M, in
     if (s != SWIGLU_OK) return s;
 
     const bool pair = use_pair_kernel(M);
-    const WorkSched sched = plan_for(M, N, K, pair ? st->pair_clusters : st->sm_count, pair);
+    const WorkSched sched =
+        plan_for(M, N, K, pair ? st->pair_clusters : st->sm_count, pair, E::kBK);
     const size_t ws_need = workspace_bytes_for(sched, M, pair, st->sm_count);
     if (ws_need > 0) {
         if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
             workspace_bytes < ws_need)
             return SWIGLU_ERR_INVALID_ARG;
-        if (overlaps(workspace, ws_need, Y, ybytes) ||
-            overlaps(workspace, ws_need, A, static_cast<size_t>(M) * K * 2) ||
-            overlaps(workspace, ws_need, Wpacked, swiglu_packed_weight_bytes(N, K)))
+        if (overlaps(workspace, ws_need, Y, ybytes) || overlaps(workspace, ws_need, A, abytes) ||
+            overlaps(workspace, ws_need, Wpacked, packed_bytes))
             return SWIGLU_ERR_INVALID_ARG;
     }
 
@@ -355,20 +396,22 @@ int swiglu_up_forward(const void *A, const void *Wpacked, void *Y, int64_t M, in
     const uint64_t weight_tiles =
         static_cast<uint64_t>(sched.order.n_tiles) * static_cast<uint64_t>(sched.k_blocks);
     CUtensorMap tmA, tmB, tmB64, tmB32, tmY;
-    if (!encode_bf16_2d(&tmA, A, K, M, FusedC::BK, a_rows) ||
-        !encode_packed_weights(&tmB, Wpacked, weight_tiles, pair ? 128u : 256u) ||
-        !encode_packed_weights(&tmB64, Wpacked, weight_tiles, 64u) ||
-        !encode_packed_weights(&tmB32, Wpacked, weight_tiles, 32u) ||
-        !encode_bf16_2d(&tmY, Y, N, M, 64, 32))
+    if (!encode_2d(&tmA, A, K, M, E::kBK, a_rows, E::kFp8) ||
+        !encode_packed_weights(&tmB, Wpacked, weight_tiles, pair ? 128u : 256u, E::kFp8) ||
+        !encode_packed_weights(&tmB64, Wpacked, weight_tiles, 64u, E::kFp8) ||
+        !encode_packed_weights(&tmB32, Wpacked, weight_tiles, 32u, E::kFp8) ||
+        !encode_2d(&tmY, Y, N, M, 64, 32))
         return SWIGLU_ERR_CUDA;
 
     FusedArgs args;
     args.M = static_cast<int>(M);
     args.N = static_cast<int>(N);
     args.K = static_cast<int>(K);
-    args.stage_tx_bytes = a_rows * FusedC::BK * 2 + FusedC::B_BYTES;
-    args.a_tx_bytes = a_rows * FusedC::BK * 2;
+    args.stage_tx_bytes = a_rows * kRowBytes + FusedC::B_BYTES;
+    args.a_tx_bytes = a_rows * kRowBytes;
     args.Y = static_cast<uint16_t *>(Y);
+    args.gate_scale = gate_scale;
+    args.up_scale = up_scale;
     args.slot_rows = slot_rows_for(M);
     args.sched = sched;
 #ifdef SWIGLU_TEST_FAULT_INJECTION
@@ -399,21 +442,83 @@ int swiglu_up_forward(const void *A, const void *Wpacked, void *Y, int64_t M, in
         cfg.gridDim = dim3(static_cast<unsigned>(2 * sched.grid));
         cfg.blockDim = dim3(PairC::THREADS);
         cfg.dynamicSmemBytes = PairC::SMEM_BYTES;
-        err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages>, tmA, tmB, tmB64, tmB32,
-                                 tmY, args);
+        err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages, E>, tmA, tmB, tmB64,
+                                 tmB32, tmY, args);
     } else {
         cfg.numAttrs = 1;
         cfg.gridDim = dim3(static_cast<unsigned>(sched.grid));
         cfg.blockDim = dim3(FusedC::THREADS);
         cfg.dynamicSmemBytes = FusedC::SMEM_BYTES;
-        err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kFusedStages>, tmA, tmB, tmB64, tmB32, tmY,
-                                 args);
+        err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kFusedStages, E>, tmA, tmB, tmB64, tmB32,
+                                 tmY, args);
     }
     if (err != cudaSuccess) {
         cudaGetLastError();
         return SWIGLU_ERR_CUDA;
     }
     return SWIGLU_OK;
+}
+
+}  // namespace
+}  // namespace swiglu
+
+extern "C" {
+
+size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    return workspace_bytes_impl<ElemBF16>(M, N, K);
+}
+
+int swiglu_up_forward(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t N,
+                      int64_t K, void *workspace, size_t workspace_bytes, void *stream) {
+    return forward_impl<ElemBF16>(A, Wpacked, Y, M, N, K, 1.0f, 1.0f, workspace,
+                                  workspace_bytes, stream, swiglu_packed_weight_bytes(N, K));
+}
+
+size_t swiglu_packed_weight_bytes_fp8(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0) return 0;
+    return static_cast<size_t>(2 * round_up(N, 128)) * static_cast<size_t>(round_up(K, 128));
+}
+
+int swiglu_pack_weights_fp8(const void *W1, const void *W2, int64_t K, int64_t N, void *Wpacked,
+                            void *stream) {
+    if (!W1 || !W2 || !Wpacked) return SWIGLU_ERR_INVALID_ARG;
+    if (K <= 0 || N <= 0 || (K % 16) != 0 || (N % 8) != 0) return SWIGLU_ERR_INVALID_ARG;
+    if (K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31)) return SWIGLU_ERR_INVALID_ARG;
+    if (!aligned16(W1) || !aligned16(W2) || !aligned16(Wpacked)) return SWIGLU_ERR_INVALID_ARG;
+    const size_t wbytes = static_cast<size_t>(K) * N;
+    const size_t pbytes = swiglu_packed_weight_bytes_fp8(N, K);
+    if (overlaps(Wpacked, pbytes, W1, wbytes) || overlaps(Wpacked, pbytes, W2, wbytes))
+        return SWIGLU_ERR_INVALID_ARG;
+    const int64_t rows = 2 * round_up(N, 128);
+    const int64_t kblocks = (K + 127) / 128;
+    if (rows / kPackTile > 65535) return SWIGLU_ERR_UNSUPPORTED;
+    int dev;
+    DeviceState *st;
+    const int s = device_setup(&dev, &st);
+    if (s != SWIGLU_OK) return s;
+    const dim3 grid(static_cast<unsigned>(kblocks), static_cast<unsigned>(rows / kPackTile));
+    pack_weights_kernel<uint8_t, 128><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(W1), static_cast<const uint8_t *>(W2),
+        static_cast<uint8_t *>(Wpacked), static_cast<int>(K), static_cast<int>(N),
+        static_cast<int>(kblocks));
+    if (cudaGetLastError() != cudaSuccess) return SWIGLU_ERR_CUDA;
+    return SWIGLU_OK;
+}
+
+size_t swiglu_workspace_bytes_fp8(int64_t M, int64_t N, int64_t K) {
+    return workspace_bytes_impl<ElemE4M3>(M, N, K);
+}
+
+int swiglu_up_forward_fp8(const void *A8, const void *Wpacked8, void *Y, int64_t M, int64_t N,
+                          int64_t K, float scale_a, float scale_w1, float scale_w2, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+    const float gs = scale_a * scale_w1, us = scale_a * scale_w2;
+    if (!(scale_a > 0.0f) || !(scale_w1 > 0.0f) || !(scale_w2 > 0.0f) || !isfinite(scale_a) ||
+        !isfinite(scale_w1) || !isfinite(scale_w2) || !isfinite(gs) || !isfinite(us) ||
+        !(gs > 0.0f) || !(us > 0.0f))
+        return SWIGLU_ERR_INVALID_ARG;   // also rejects NaN, and products that leave FP32
+    return forward_impl<ElemE4M3>(A8, Wpacked8, Y, M, N, K, gs, us, workspace, workspace_bytes, stream,
+                                  swiglu_packed_weight_bytes_fp8(N, K));
 }
 
 int swiglu_check_device_status(void *stream, uint32_t *raw_word) {

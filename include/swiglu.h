@@ -165,6 +165,48 @@ int swiglu_up_forward(const void *A, const void *Wpacked, void *Y,
 int swiglu_up_forward_noalloc(const void *A, const void *Wpacked, void *Y,
                               int64_t M, int64_t N, int64_t K, void *stream);
 
+/* ------------------------------------------------------------------------
+ * FP8 (E4M3) inputs with per-tensor scales. The paper names FP8 only as the
+ * motivation for fusing (Section 1: as tensor-core arithmetic gets cheaper,
+ * the activation's memory traffic matters more); these entry points are this
+ * library's extension. The inputs stand for A = scale_a * A8,
+ * W1 = scale_w1 * W1_8, W2 = scale_w2 * W2_8 (E4M3: 1 sign, 4 exponent bits
+ * with bias 7, 3 significand bits, max 448). Gate and Up are accumulated from
+ * the raw E4M3 products in FP32 in tensor memory (tcgen05.mma kind::f8f6f4),
+ * multiplied by scale_a*scale_w1 and scale_a*scale_w2, then
+ * Y = SiLU(Gate) * Up is rounded to BF16 as in swiglu_up_forward.
+ * ---------------------------------------------------------------------- */
+
+/* Packed FP8 weight bytes: [NB][KB][256][128] bytes, NB = ceil(N/128),
+ * KB = ceil(K/128): the BF16 layout with 128 E4M3 values per 128-byte row.
+ * Returns 0 if N <= 0 or K <= 0. */
+size_t swiglu_packed_weight_bytes_fp8(int64_t N, int64_t K);
+
+/* Packs W1_8 and W2_8 (device, E4M3 bytes, [K, N] row-major each) into
+ * Wpacked8 (device, swiglu_packed_weight_bytes_fp8(N, K) bytes). A byte
+ * permutation plus zero padding. Requirements: K > 0, N > 0, K % 16 == 0,
+ * N % 8 == 0, pointers non-null and 16-byte aligned, no overlap. */
+int swiglu_pack_weights_fp8(const void *W1_8, const void *W2_8, int64_t K, int64_t N,
+                            void *Wpacked8, void *stream);
+
+/* Workspace bytes of swiglu_up_forward_fp8 for (M, N, K) on the current
+ * device (0: none needed). Same rules as swiglu_workspace_bytes. */
+size_t swiglu_workspace_bytes_fp8(int64_t M, int64_t N, int64_t K);
+
+/* Y = SiLU(A x W1) (.) (A x W2) from FP8 inputs.
+ *   A8        device, E4M3, [M, K] row-major
+ *   Wpacked8  device, output of swiglu_pack_weights_fp8 for this (N, K)
+ *   Y         device, BF16, [M, N] row-major; fully overwritten
+ *   scale_a, scale_w1, scale_w2: the per-tensor scales (finite, > 0)
+ *   workspace: as swiglu_up_forward, sized by swiglu_workspace_bytes_fp8
+ * Requirements: as swiglu_up_forward, with K % 16 == 0 (16-byte rows of A8).
+ * Errors: as swiglu_up_forward; SWIGLU_ERR_INVALID_ARG also for a scale that
+ * is not a positive number. */
+int swiglu_up_forward_fp8(const void *A8, const void *Wpacked8, void *Y,
+                          int64_t M, int64_t N, int64_t K,
+                          float scale_a, float scale_w1, float scale_w2,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
 /*
  * Synchronizes `stream`, then reads and clears the current device's status
  * word. Every wait inside the kernels is bounded (about a second); a kernel

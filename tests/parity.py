@@ -55,14 +55,20 @@ def ulp_bf16(x: np.ndarray) -> np.ndarray:
 ACCUM_C = 4.0
 
 
-def fp32_accumulation_bound(A_bits, W1_bits, W2_bits, G, U):
+def fp32_accumulation_bound(A_bits, W1_bits, W2_bits, G, U, values=None):
     """Per-element FP32 accumulation error scale E (module docstring) for the
-    output rows of A_bits [R, K], given the oracle's binary64 sums G, U [R, N]."""
-    K = A_bits.shape[1]
+    output rows of A_bits [R, K], given the oracle's binary64 sums G, U [R, N].
+    `values` = (A, W1, W2) as real values replaces the BF16 bit patterns (FP8
+    inputs: the dequantized values)."""
+    if values is None:
+        A_v, W1_v, W2_v = bits_to_f64(A_bits), bits_to_f64(W1_bits), bits_to_f64(W2_bits)
+    else:
+        A_v, W1_v, W2_v = values
+    K = A_v.shape[1]
     scale = ACCUM_C * 2.0 ** -24 * np.sqrt(K)
-    a2 = np.square(bits_to_f64(A_bits)).astype(np.float32)
-    n1 = np.sqrt((a2 @ np.square(bits_to_f64(W1_bits)).astype(np.float32)).astype(np.float64))
-    n2 = np.sqrt((a2 @ np.square(bits_to_f64(W2_bits)).astype(np.float32)).astype(np.float64))
+    a2 = np.square(A_v).astype(np.float32)
+    n1 = np.sqrt((a2 @ np.square(W1_v).astype(np.float32)).astype(np.float64))
+    n2 = np.sqrt((a2 @ np.square(W2_v).astype(np.float32)).astype(np.float64))
     with np.errstate(over="ignore"):
         sig = 1.0 / (1.0 + np.exp(-G))
     dsilu = sig * (1.0 + G * (1.0 - sig))
@@ -139,3 +145,20 @@ def unpack_reference(P: np.ndarray, K: int, N: int):
     w1 = T[:, :, :128, :].transpose(1, 3, 0, 2).reshape(KB * 64, NB * 128)
     w2 = T[:, :, 128:, :].transpose(1, 3, 0, 2).reshape(KB * 64, NB * 128)
     return w1[:K, :N], w2[:K, :N]
+
+
+def pack_reference_fp8(W1: np.ndarray, W2: np.ndarray) -> np.ndarray:
+    """The FP8 packed layout: [NB][KB][256][128] bytes, KB = ceil(K/128),
+    Gate rows then Up rows as in pack_reference. Flat uint8 array."""
+    K, N = W1.shape
+    NB, KB = -(-N // 128), -(-K // 128)
+    w1 = np.zeros((KB * 128, NB * 128), np.uint8)
+    w2 = np.zeros((KB * 128, NB * 128), np.uint8)
+    w1[:K, :N] = W1
+    w2[:K, :N] = W2
+    P = np.zeros((NB, KB, 256, 128), np.uint8)
+    for j in range(NB):
+        for b in range(KB):
+            P[j, b, :128] = w1[128 * b:128 * b + 128, 128 * j:128 * j + 128].T
+            P[j, b, 128:] = w2[128 * b:128 * b + 128, 128 * j:128 * j + 128].T
+    return P.reshape(-1)

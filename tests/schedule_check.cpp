@@ -1,6 +1,7 @@
 // Host-side check of the fused kernel's work schedule (schedule.cuh), compiled
 // with g++ by tests/test_schedule.py. For each (m_tiles, n_tiles, k_blocks,
-// sm_count, min_sk_iters, weight_bound) given on stdin it verifies that:
+// sm_count, min_sk_iters, weight_bound, schedule mode) given on stdin it
+// verifies that:
 //   * the units of all CTAs cover every (tile, k-block) exactly once;
 //   * data-parallel tiles are whole and spread round robin;
 //   * for every stream-K tile, the contributor range [sk_owner(first),
@@ -28,10 +29,11 @@ static int fail(const char *what, int a, int b) {
 }
 
 int main() {
-    int mt, nt, kb, sms, min_iters, wbound;
+    int mt, nt, kb, sms, min_iters, wbound, mode;
     int bad = 0;
-    while (std::scanf("%d %d %d %d %d %d", &mt, &nt, &kb, &sms, &min_iters, &wbound) == 6) {
-        const WorkSched s = plan_schedule(mt, nt, kb, sms, 16, min_iters, wbound != 0);
+    while (std::scanf("%d %d %d %d %d %d %d", &mt, &nt, &kb, &sms, &min_iters, &wbound, &mode) ==
+           7) {
+        const WorkSched s = plan_schedule(mt, nt, kb, sms, 16, min_iters, wbound != 0, mode);
         const int T = mt * nt;
         if (s.grid < 1 || s.grid > sms) { bad |= fail("grid", s.grid, sms); continue; }
         if (s.sk_iters > 0 && s.dp_tiles % s.grid != 0) { bad |= fail("dp multiple", s.dp_tiles, s.grid); continue; }
@@ -106,13 +108,15 @@ int main() {
         long long wmin = work[0], wmax = work[0];
         for (long long w : work) { wmin = w < wmin ? w : wmin; wmax = w > wmax ? w : wmax; }
         // stream-K: balanced to one k-block (4 quarter units); data-parallel:
-        // to one whole tile, and only when the grid is used at least 85%;
+        // to one whole tile, and (automatic choice) only when the grid is used
+        // at least 85%;
         // column-split tail: to one sub-tile
         if (s.sk_iters > 0 && wmax - wmin > 4) bad |= fail("imbalance", (int)wmin, (int)wmax);
         if (s.sk_iters == 0 && s.n_split == 1) {
             if (wmax - wmin > 4 * kb) bad |= fail("dp imbalance", (int)wmin, (int)wmax);
             const int waves = (T + sms - 1) / sms;
-            if (T < 0.85 * waves * sms) bad |= fail("dp chosen below threshold", T, waves * sms);
+            if (mode == kSchedAuto && T < 0.85 * waves * sms)
+                bad |= fail("dp chosen below threshold", T, waves * sms);
         }
         if (s.n_split > 1 && wmax - wmin > 4 * kb / s.n_split) bad |= fail("split imbalance", (int)wmin, (int)wmax);
         std::printf("mt=%d nt=%d kb=%d sms=%d grid=%d dp=%d sk_iters=%lld n_split=%d split=%d max_contrib=%d work=[%lld,%lld]\n",

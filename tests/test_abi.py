@@ -105,6 +105,25 @@ def test_pack_rejects_bad_arguments_on_host(lib, args):
     assert lib.swiglu_pack_weights_nk(W1, W2, N, K, Wp, None) == 1
 
 
+def test_fp8_sizes_and_host_validation(lib):
+    import gemm_swiglu_mlp_gb300 as sg
+    assert sg.swiglu_packed_weight_bytes_fp8(4864, 896) == 2 * 4864 * 896
+    assert sg.swiglu_packed_weight_bytes_fp8(136, 64) == 2 * 256 * 128     # N -> 256, K -> 128
+    assert sg.swiglu_packed_weight_bytes_fp8(0, 64) == 0
+    assert sg.swiglu_workspace_bytes_fp8(2048, 8960, 1536) >= 0
+    f = lib.swiglu_up_forward_fp8
+    ok = (P, Q, R, 4, 8, 16)
+    for bad in [(0, Q, R, 4, 8, 16), (P, Q, R, 4, 8, 8),               # null; K % 16 != 0
+                (P, Q, R, 4, 12, 16), (P + 8, Q, R, 4, 8, 16), (P, Q, P, 4, 8, 16)]:
+        assert f(*bad, 1.0, 1.0, 1.0, None, 0, None) == 1, bad
+    for sa, s1, s2 in [(0.0, 1.0, 1.0), (1.0, -1.0, 1.0), (1.0, 1.0, float("nan")),
+                       (float("inf"), 1.0, 1.0), (1e30, 1e30, 1.0), (1e-30, 1e-30, 1.0)]:
+        assert f(*ok, sa, s1, s2, None, 0, None) == 1, (sa, s1, s2)
+    for bad in [(0, Q, R, 64, 64), (P, Q, R, 64, 4), (P, Q, R, 8, 64), (P + 4, Q, R, 64, 64)]:
+        W1, W2, Wp, K, N = bad
+        assert lib.swiglu_pack_weights_fp8(W1, W2, K, N, Wp, None) == 1, bad
+
+
 def test_valid_call_without_gpu_reports_error_not_crash(lib):
     import torch
     if torch.cuda.is_available():

@@ -1,0 +1,21 @@
+"""bench.py's roofline bookkeeping, checked by hand (no GPU)."""
+import bench
+import workloads
+
+
+def test_algorithmic_bytes_by_hand():
+    w = workloads.BY_LABEL["1"]                     # M=2048, K=1536, N=8960
+    assert bench.algorithmic_bytes(w, "bf16") == 2 * (2048 * 1536 + 2 * 1536 * 8960 + 2048 * 8960)
+    assert bench.algorithmic_bytes(w, "fp8") == 2048 * 1536 + 2 * 1536 * 8960 + 2 * 2048 * 8960
+
+
+def test_fp8_peak_is_twice_bf16_and_moves_the_ridge():
+    peaks = {"hbm_gbs": 7000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1800.0}
+    assert bench.tensor_peak(peaks, "fp8") == 4000.0
+    assert bench.tensor_peak(peaks, "fp8", "bf16_tflops_sustained") == 3600.0
+    w = workloads.BY_LABEL["1"]
+    assert bench.bound_of(w, peaks, "bf16") == "tensor"
+    t = bench.roofline_us(w, peaks, "fp8")
+    assert abs(t - max(w.flops / 4e15, bench.algorithmic_bytes(w, "fp8") / 7e12) * 1e6) < 1e-9
+    decode = workloads.BY_LABEL["10"]
+    assert bench.bound_of(decode, peaks, "fp8") == "hbm"

@@ -36,8 +36,13 @@ def _cases():
     return cases
 
 
-def test_schedule_covers_every_iteration_once_and_balances(checker):
-    inp = "\n".join(" ".join(map(str, c)) for c in _cases()) + "\n"
+MODES = {"auto": 0, "dp": 1, "split": 2, "sk": 3, "sk-tail": 4}
+
+
+@pytest.mark.parametrize("mode", sorted(MODES))
+def test_schedule_covers_every_iteration_once_and_balances(checker, mode):
+    cases = [c + (MODES[mode],) for c in _cases()]
+    inp = "\n".join(" ".join(map(str, c)) for c in cases) + "\n"
     r = subprocess.run([checker], input=inp, capture_output=True, text=True)
     assert r.returncode == 0, r.stdout[-3000:]
-    assert r.stdout.count("\n") == len(_cases())
+    assert r.stdout.count("\n") == len(cases)

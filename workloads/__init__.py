@@ -178,7 +178,12 @@ def quantize_e4m3(x: np.ndarray):
     x = np.asarray(x, dtype=np.float32)
     amax = float(np.max(np.abs(x))) if x.size else 0.0
     s = np.float32(amax / E4M3_MAX) if amax > 0 else np.float32(1.0)
-    return f32_to_e4m3_bits(x.astype(np.float64) / float(s)), float(s)
+    flat = x.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint8)
+    step = 1 << 20                               # elementwise: chunks only bound temporaries
+    for i in range(0, flat.size, step):
+        out[i:i + step] = f32_to_e4m3_bits(flat[i:i + step].astype(np.float64) / float(s))
+    return out.reshape(x.shape), float(s)
 
 
 def make_inputs_fp8(w: Workload):

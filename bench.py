@@ -273,7 +273,17 @@ def run_reference(args, w):
     return 0
 
 
-def time_unfused_context(w, W1, W2, As, Ys, R, dev, stream, steps, fused_value):
+def fusion_efficiency(w, t_unfused_s: float, t_fused_s: float, hbm_gbs: float) -> float:
+    """Time the fusion saved over the time the HBM traffic it removes would
+    take at the measured copy bandwidth. The removed traffic is the pages'
+    count ("Tile-Level Activation Overlap for Efficient LLM Inference",
+    technical summary, contributions and results): Gate and Up each written
+    and read once in BF16, 8*M*N bytes. Above 1 means the fused kernel also
+    gains from overlap (the summary reports this for its Kernel-2)."""
+    return (t_unfused_s - t_fused_s) / (8.0 * w.M * w.N / (hbm_gbs * 1e9))
+
+
+def time_unfused_context(w, W1, W2, As, Ys, R, dev, stream, steps, fused_value, hbm_gbs):
     """Context only (not this library): the unfused PyTorch path the pages
     compare against ("Tile-Level Activation Overlap for Efficient LLM
     Inference", Section 1: two GEMMs that write Gate and Up to HBM, then the
@@ -309,6 +319,8 @@ def time_unfused_context(w, W1, W2, As, Ys, R, dev, stream, steps, fused_value):
     del W1s, W2s
     return {"value": v, "unit": UNIT, "ms_per_step": el / steps * 1e3, "steps": steps,
             "fused_speedup": fused_value / v,
+            "fusion_efficiency": fusion_efficiency(w, el / steps, w.flops / (fused_value * 1e12),
+                                                   hbm_gbs),
             "what": "torch.matmul(A, W1), torch.matmul(A, W2) (cuBLAS, Gate/Up written to HBM "
                     "in BF16), then silu(Gate) * Up in BF16; same rotating inputs"}
 
@@ -476,6 +488,22 @@ def run_gb300(args, w):
     value = aggregate_value(w.flops, K, world, elapsed_max)
     avg_launch = elapsed / K
 
+    # ---- L2-warm context: the same launches on one input set, so A and the
+    # weights stay in L2 from call to call when they fit (not the headline).
+    Kw = min(K, 2000)
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1_ = torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        forward(0)
+    w0.record(stream)
+    for _ in range(Kw):
+        forward(0)
+    w1_.record(stream)
+    torch.cuda.synchronize(dev)
+    warm_s = w0.elapsed_time(w1_) * 1e-3 / Kw
+    l2_warm = {"avg_launch_us": warm_s * 1e6, "tflops": w.flops / warm_s / 1e12, "steps": Kw,
+               "what": "one input set reused every call (operands L2-resident when they fit)"}
+
     # ---- end to end through the public API, as a serving loop runs it: every
     # step copies its A from pinned host memory, runs the forward and copies
     # its Y back to pinned host memory. Copy-in, compute and copy-out of
@@ -539,7 +567,8 @@ def run_gb300(args, w):
 
     unfused = mlp = None
     if not args.no_context and not fp8:
-        unfused = time_unfused_context(w, W1, W2, As, Ys, R, dev, stream, min(K, 2000), value)
+        unfused = time_unfused_context(w, W1, W2, As, Ys, R, dev, stream, min(K, 2000), value,
+                                       peaks["hbm_gbs"])
         mlp = time_mlp_context(w, W1, W2, sg, As, Wps, Ys, Wss, R, dev, stream, min(K, 500))
 
     if rank != 0:
@@ -579,7 +608,7 @@ def run_gb300(args, w):
                 "ms_per_step": e_el / Ke * 1e3,
                 "how": "pinned host A -> device, forward, device Y -> pinned host, every step; "
                        "copy-in, compute and copy-out of consecutive steps overlap on 3 streams"},
-        "gpu_launches": K, "clocks": sampler.summary(),
+        "gpu_launches": K, "clocks": sampler.summary(), "context_l2_warm": l2_warm,
     }
     if unfused is not None:
         line["context_unfused_torch"] = unfused

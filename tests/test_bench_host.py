@@ -19,3 +19,11 @@ def test_fp8_peak_is_twice_bf16_and_moves_the_ridge():
     assert abs(t - max(w.flops / 4e15, bench.algorithmic_bytes(w, "fp8") / 7e12) * 1e6) < 1e-9
     decode = workloads.BY_LABEL["10"]
     assert bench.bound_of(decode, peaks, "fp8") == "hbm"
+
+
+def test_fusion_efficiency_by_hand():
+    w = workloads.BY_LABEL["0"]                     # M=128, N=4864
+    removed_s = 8 * 128 * 4864 / 5000e9             # 8*M*N bytes at 5000 GB/s
+    assert abs(bench.fusion_efficiency(w, 10e-6 + removed_s, 10e-6, 5000.0) - 1.0) < 1e-12
+    assert abs(bench.fusion_efficiency(w, 10e-6 + 2 * removed_s, 10e-6, 5000.0) - 2.0) < 1e-12
+    assert bench.fusion_efficiency(w, 10e-6, 10e-6, 5000.0) == 0.0

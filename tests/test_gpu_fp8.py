@@ -83,14 +83,14 @@ def test_fp8_forward_small_full_compare(sg, orc, monkeypatch, variant, M, N, K):
 
 
 @pytest.mark.parametrize("label", ["1", "3", "10"])
-def test_fp8_workload_full_size_sampled_rows(sg, orc, label):
+def test_fp8_workload_full_size(sg, orc, label):
+    """Full-size FP8 runs of the 1.5B prefill, 7B decode and 72B decode
+    shapes, every output element compared."""
     w = workloads.BY_LABEL[label]
     A8, W18, W28, sa, s1, s2 = workloads.make_inputs_fp8(w)
     got = _run(sg, A8, W18, W28, sa, s1, s2)
-    rng = np.random.Generator(np.random.PCG64(7000 + w.seed_index))
-    rows = sorted({0, w.M - 1, w.M // 2} | set(rng.choice(w.M, size=min(w.M, 11), replace=False).tolist()))
-    ref = orc.swiglu_up_fp8(A8, W18, W28, sa, s1, s2, rows=rows, want_gate_up=True)
-    _check(got[rows], ref, A8[rows], W18, W28, sa, s1, s2, w.name)
+    ref = orc.swiglu_up_fp8(A8, W18, W28, sa, s1, s2, want_gate_up=True)
+    _check(got, ref, A8, W18, W28, sa, s1, s2, w.name)
 
 
 def test_fp8_rejects_bad_scales(sg):

@@ -155,31 +155,37 @@ __device__ __forceinline__ void tmem_ld_gu(uint32_t tbase, int c, float (&g)[32]
     }
 }
 
-// Epilogue of a column sub-tile (width 64 or 32): TMEM holds Gate in columns
-// [0, width) and Up in [width, 2*width). Each thread owns one output row and
-// stores its `width` outputs straight to global memory in 16-byte pieces
-// (rows >= M and columns >= N are skipped; N is a multiple of 8, so a piece
-// is either wholly inside or wholly outside).
+// y for 32 consecutive columns [col, col+32) of one output row, from FP32
+// Gate and Up (times their scales), stored straight to global memory in
+// 16-byte pieces. Rows >= M and columns >= N are skipped; N is a multiple of
+// 8, so a piece is either wholly inside or wholly outside.
+__device__ __forceinline__ void store_y32_global(int row, int col, const float (&g)[32],
+                                                 const float (&u)[32], const FusedArgs &args) {
+    if (row >= args.M) return;
+    uint16_t *dst = args.Y + static_cast<size_t>(row) * args.N + col;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (col + 8 * j >= args.N) break;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 8 * j + 2 * e;
+            w[e] = pack_bf16x2(silu_mul(g[i] * args.gate_scale, u[i] * args.up_scale),
+                               silu_mul(g[i + 1] * args.gate_scale, u[i + 1] * args.up_scale));
+        }
+        *reinterpret_cast<uint4 *>(dst + 8 * j) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Epilogue of a column sub-tile (width 64 or 32), or of a whole tile stored
+// without shared-memory staging (width 128): TMEM holds Gate in columns
+// [0, width) and Up in [width, 2*width). Each thread owns one output row.
 __device__ __forceinline__ void epilogue_subtile_store(uint32_t tbase, int width, int row,
                                                        int col0, const FusedArgs &args) {
     for (int c = 0; c < width; c += 32) {
         float g[32], v[32];
         tmem_ld_gu(tbase, c, g, v, width);
-        if (row < args.M) {
-            uint16_t *dst = args.Y + static_cast<size_t>(row) * args.N + col0 + c;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (col0 + c + 8 * j >= args.N) break;
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = 8 * j + 2 * e;
-                    w[e] = pack_bf16x2(silu_mul(g[i] * args.gate_scale, v[i] * args.up_scale),
-                                       silu_mul(g[i + 1] * args.gate_scale, v[i + 1] * args.up_scale));
-                }
-                *reinterpret_cast<uint4 *>(dst + 8 * j) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
+        store_y32_global(row, col0 + c, g, v, args);
     }
 }
 

@@ -124,11 +124,36 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    // The prologue above touched no global memory: the next launch may start
-    // now, and this one waits here for the previous launch's results.
-    griddep_launch_dependents();
-    griddep_wait();
     const WorkSched &sched = args.sched;
+    // The prologue above touched no global memory: the next launch may start
+    // now, and this one waits here for the previous launch's results. While
+    // it waits, the producer asks L2 for this CTA's first pipeline stages (a
+    // prefetch only moves device memory into L2, where every SM's writes
+    // land, so what the previous launch writes afterwards is still what the
+    // loads below see).
+    griddep_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        UnitIter it;
+        it.init(sched, cta);
+        Unit u;
+        if (it.next(u)) {
+            int mb, nb;
+            sched.order.coords(u.tile, mb, nb);
+            const int kend = (u.kb1 - u.kb0 < STAGES) ? u.kb1 : u.kb0 + STAGES;
+            for (int kb = u.kb0; kb < kend; ++kb) {
+                const int wtile = nb * sched.k_blocks + kb;
+                tma_prefetch_2d(&tmA, kb * E::kBK, mb * C::BM);
+                if (u.width == C::BN) {
+                    tma_prefetch_3d(&tmB, 0, 0, wtile);
+                } else {
+                    const CUtensorMap *tmBn = (u.width == 64) ? &tmB64 : &tmB32;
+                    tma_prefetch_3d(tmBn, 0, u.sub * u.width, wtile);
+                    tma_prefetch_3d(tmBn, 0, C::BN + u.sub * u.width, wtile);
+                }
+            }
+        }
+    }
+    griddep_wait();
 
     // Producer bookkeeping kept for the drain after an abort: which stages
     // received a load, and the parity of the phase of the last one.

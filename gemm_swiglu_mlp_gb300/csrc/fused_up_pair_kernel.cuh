@@ -122,11 +122,31 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    // The prologue above touched no global memory: the next launch may start
-    // now, and this one waits here for the previous launch's results.
-    griddep_launch_dependents();
-    griddep_wait();
     const WorkSched &sched = args.sched;
+    // The prologue above touched no global memory: the next launch may start
+    // now, and this one waits here for the previous launch's results. While
+    // it waits (the previous launch's last tiles), the producer asks L2 for
+    // this CTA's first pipeline stages: a prefetch reads device memory into
+    // L2 only, and L2 is where every SM's writes land, so data the previous
+    // launch writes afterwards is still what the loads below see.
+    griddep_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        UnitIter it;
+        it.init(sched, pair);
+        Unit u;
+        if (it.next(u)) {
+            int pm, nb;
+            sched.order.coords(u.tile, pm, nb);
+            const CUtensorMap *tmBu = (u.width == C::BN) ? &tmB : (u.width == 64 ? &tmB64 : &tmB32);
+            const int kend = (u.kb1 - u.kb0 < STAGES) ? u.kb1 : u.kb0 + STAGES;
+            for (int kb = u.kb0; kb < kend; ++kb) {
+                tma_prefetch_2d(&tmA, kb * E::kBK, pm * C::UMMA_M + C::BM * static_cast<int>(rank));
+                tma_prefetch_3d(tmBu, 0, C::BN * static_cast<int>(rank) + u.sub * u.width,
+                                nb * sched.k_blocks + kb);
+            }
+        }
+    }
+    griddep_wait();
 
     uint32_t issued_mask = 0, last_parity = 0;  // leader's drain bookkeeping
 

@@ -138,13 +138,17 @@ struct UnitIter {
 //     would otherwise idle outright: fewer tiles than half the grid. For
 //     weight-streaming shapes (`weight_bound`: few token rows, the bytes per
 //     unit scale with its width) it is taken whenever it reaches 0.9.
-//   * otherwise, whole tiles if their efficiency is >= 0.85;
-//   * otherwise the stream-K split of the k-block iterations (workspace).
+//   * otherwise, whole tiles whenever they fill at least half the grid;
+//   * otherwise (a handful of tiles: most SMs would idle) the stream-K split
+//     of the k-block iterations (workspace).
 // Splitting K costs a partial write and a dependent read-back at the end of
-// the kernel, more than a mostly full last wave loses, and for
-// weight-streaming shapes a short last wave loses little: its CTAs get more
-// bandwidth each. `min_sk_iters` keeps every CTA's stream-K share at a few
-// k-blocks so tiles are not cut into slivers.
+// the kernel. Measured on GB300 it costs more than an idle tail: with 0.76
+// of the grid used by whole tiles (72B shape, 32 tokens) whole tiles took
+// 144 us and stream-K 153 us, and on the 1.5B prefill shape stream-K of the
+// last wave took 83.5 us against 73.7 us; for weight-streaming shapes a
+// short last wave also loses little, as its CTAs get more bandwidth each.
+// `min_sk_iters` keeps every CTA's stream-K share at a few k-blocks so tiles
+// are not cut into slivers.
 // Schedule choice: kSchedAuto is the rule above; the others force one form
 // (for ablations and tests): whole tiles only, the column-split tail, the
 // stream-K split of the last full wave plus the remainder, or the stream-K
@@ -206,7 +210,7 @@ inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_co
             return s;
         }
     }
-    if (mode == kSchedAuto && eff_dp >= 0.85) {
+    if (mode == kSchedAuto && 2 * T >= G) {
         // data-parallel: every tile whole, no workspace
         s.grid = T < G ? T : G;
         s.dp_tiles = T;

@@ -139,6 +139,22 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, 
 // 2-SM variants: the destination is this CTA's shared memory, the
 // completion is signalled on `bar`, a shared::cluster address that may be
 // the leader (even) CTA's barrier of the pair.
+// L2 prefetch of one tensor-map box (no shared memory, no barrier): a hint
+// that only moves data from device memory into L2.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *m, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int32_t x, int32_t y,
+                                                int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *m, uint32_t bar,
                                                  int32_t x, int32_t y) {
     asm volatile(

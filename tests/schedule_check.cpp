@@ -109,13 +109,13 @@ int main() {
         for (long long w : work) { wmin = w < wmin ? w : wmin; wmax = w > wmax ? w : wmax; }
         // stream-K: balanced to one k-block (4 quarter units); data-parallel:
         // to one whole tile, and (automatic choice) only when the grid is used
-        // at least 85%;
+        // at least 85% or the tiles fill at least half of it;
         // column-split tail: to one sub-tile
         if (s.sk_iters > 0 && wmax - wmin > 4) bad |= fail("imbalance", (int)wmin, (int)wmax);
         if (s.sk_iters == 0 && s.n_split == 1) {
             if (wmax - wmin > 4 * kb) bad |= fail("dp imbalance", (int)wmin, (int)wmax);
             const int waves = (T + sms - 1) / sms;
-            if (mode == kSchedAuto && T < 0.85 * waves * sms)
+            if (mode == kSchedAuto && T < 0.85 * waves * sms && 2 * T < sms)
                 bad |= fail("dp chosen below threshold", T, waves * sms);
         }
         if (s.n_split > 1 && wmax - wmin > 4 * kb / s.n_split) bad |= fail("split imbalance", (int)wmin, (int)wmax);

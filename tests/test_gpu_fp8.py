@@ -82,6 +82,19 @@ def test_fp8_forward_small_full_compare(sg, orc, monkeypatch, variant, M, N, K):
     _check(got, ref, A8, W18, W28, sa, s1, s2, (variant, M, N, K))
 
 
+@pytest.mark.parametrize("variant", ["1sm", "2sm"])
+@pytest.mark.parametrize("mode", ["dp", "split", "sk", "sk-tail"])
+def test_fp8_every_schedule_form_matches(sg, orc, monkeypatch, variant, mode):
+    """The FP8 path under each forced work split (k-blocks of 128 here)."""
+    monkeypatch.setenv("SWIGLU_FUSED_VARIANT", variant)
+    monkeypatch.setenv("SWIGLU_SCHEDULE", mode)
+    M, N, K = 1300, 2000, 2064
+    A8, W18, W28, sa, s1, s2 = workloads.random_case_fp8(M, N, K, seed=92)
+    got = _run(sg, A8, W18, W28, sa, s1, s2)
+    ref = orc.swiglu_up_fp8(A8, W18, W28, sa, s1, s2, want_gate_up=True)
+    _check(got, ref, A8, W18, W28, sa, s1, s2, (variant, mode))
+
+
 @pytest.mark.parametrize("label", ["1", "3", "10"])
 def test_fp8_workload_full_size(sg, orc, label):
     """Full-size FP8 runs of the 1.5B prefill, 7B decode and 72B decode

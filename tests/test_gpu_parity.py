@@ -111,6 +111,60 @@ def test_forward_small_full_compare(sg, orc, monkeypatch, variant, M, N, K):
     assert_parity(got, want, (variant, M, N, K))
 
 
+SCHEDULE_MODES = ["dp", "split", "sk", "sk-tail"]
+
+
+@pytest.mark.parametrize("variant", ["1sm", "2sm"])
+@pytest.mark.parametrize("mode", SCHEDULE_MODES)
+def test_every_schedule_form_matches(sg, orc, monkeypatch, variant, mode):
+    """Each work split the scheduler can choose, forced on one shape with more
+    tiles than either kernel's grid (176 1-SM tiles, 96 pair tiles) and a
+    stream-K remainder of several k-blocks per CTA: whole tiles, the
+    column-split tail, stream-K over the last wave plus the remainder, and
+    stream-K over the remainder alone."""
+    monkeypatch.setenv("SWIGLU_FUSED_VARIANT", variant)
+    monkeypatch.setenv("SWIGLU_SCHEDULE", mode)
+    M, N, K = 1300, 2000, 2056
+    A, W1, W2 = workloads.random_case(M, N, K, seed=91)
+    got, _ = run_fused(sg, A, W1, W2)
+    want = orc.swiglu_up(A, W1, W2)["Y"]
+    assert_parity(got, want, (variant, mode))
+
+
+@pytest.mark.parametrize("variant,mode", [("1sm", "auto"), ("2sm", "auto"), ("1sm", "sk"),
+                                          ("2sm", "sk")])
+def test_cuda_graph_replay_matches_direct_calls(sg, monkeypatch, variant, mode):
+    """The forward captured in a CUDA graph (after one direct call has done
+    the per-device set-up) replays to the same bytes as direct calls,
+    including the stream-K path whose workspace counters must return to
+    zero after every launch."""
+    monkeypatch.setenv("SWIGLU_FUSED_VARIANT", variant)
+    if mode != "auto":
+        monkeypatch.setenv("SWIGLU_SCHEDULE", mode)
+    M, N, K = 520, 1160, 1032
+    A, W1, W2 = workloads.random_case(M, N, K, seed=17)
+    Ad = to_device_bf16(A, "cuda")
+    Wp = sg.swiglu_pack_weights(to_device_bf16(W1, "cuda"), to_device_bf16(W2, "cuda"))
+    ws_bytes = sg.swiglu_workspace_bytes(M, N, K)
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") if ws_bytes else None
+    Y_direct = sg.swiglu_up_forward(Ad, Wp, N, workspace=ws)
+    torch.cuda.synchronize()
+    Ys = [torch.zeros((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        for Y in Ys:
+            sg.swiglu_up_forward(Ad, Wp, N, Y=Y, workspace=ws, stream=cs)
+    for _ in range(2):
+        for Y in Ys:
+            Y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert sg.swiglu_check_device_status() == 0
+        for Y in Ys:
+            assert torch.equal(Y.view(torch.int16), Y_direct.view(torch.int16))
+
+
 def test_forward_saturating_inputs(sg, orc):
     # pre-activations with std ~8-16: SiLU at both saturated ends
     A, W1, W2 = workloads.random_case(200, 264, 512, seed=5, a_scale=12.0)

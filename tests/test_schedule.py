@@ -32,7 +32,10 @@ def _cases():
         cases.append((int(rng.integers(1, 40)), int(rng.integers(1, 40)), int(rng.integers(1, 30)),
                       int(rng.integers(1, 200)), int(rng.integers(1, 10)), int(rng.integers(0, 2))))
     cases += [(1, 1, 1, 152, 8, 1), (1, 1, 200, 152, 8, 0), (1, 152, 3, 152, 8, 1),
-              (2, 152, 5, 152, 8, 0), (1, 153, 7, 152, 1, 1), (64, 231, 128, 152, 8, 0)]
+              (2, 152, 5, 152, 8, 0), (1, 153, 7, 152, 1, 1), (64, 231, 128, 152, 8, 0),
+              # the forced-schedule GPU parity shape (M=1300, N=2000; BF16 and FP8 k-blocks)
+              (11, 16, 33, 152, 4, 0), (6, 16, 33, 76, 4, 0), (11, 16, 17, 152, 4, 0),
+              (6, 16, 17, 76, 4, 0)]
     return cases
 
 

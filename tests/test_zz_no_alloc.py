@@ -59,9 +59,10 @@ def test_noalloc_matches_forward_on_two_calls(sg, M, N, K):
 
 def test_noalloc_rejects_problems_over_its_scratch(sg):
     lib = sg.load_library()
-    # 200 rows, 100 column tiles, K = 8192: whole tiles would fill only 66% of
-    # two waves, so K is split and the workspace exceeds the 32 MiB scratch.
-    M, N, K = 200, 12800, 8192
+    # 200 rows, 30 column tiles, K = 8192: 60 tiles, or their column
+    # sub-tiles, would leave most of the SMs idle, so K is split over every SM
+    # and the workspace exceeds the 32 MiB scratch.
+    M, N, K = 200, 3840, 8192
     need = sg.swiglu_workspace_bytes(M, N, K)
     assert need > 32 * 1024 * 1024
     fake = 1 << 20   # 16-byte aligned, never dereferenced: the call is rejected first

@@ -136,9 +136,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
-// 2-SM variants: the destination is this CTA's shared memory, the
-// completion is signalled on `bar`, a shared::cluster address that may be
-// the leader (even) CTA's barrier of the pair.
 // L2 prefetch of one tensor-map box (no shared memory, no barrier): a hint
 // that only moves data from device memory into L2.
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *m, int32_t x, int32_t y) {
@@ -155,6 +152,9 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int32_t x,
                  : "memory");
 }
 
+// 2-SM variants: the destination is this CTA's shared memory, the
+// completion is signalled on `bar`, a shared::cluster address that may be
+// the leader (even) CTA's barrier of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *m, uint32_t bar,
                                                  int32_t x, int32_t y) {
     asm volatile(
@@ -172,12 +172,17 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *m, uint32_t bar,
-                                                 int32_t x, int32_t y, uint64_t policy) {
+// 2-SM multicast: the box lands at the same shared-memory offset in every
+// CTA of `cta_mask`, and each destination's completion is signalled on the
+// barrier at `bar`'s offset in the even (leader) CTA of that destination's
+// pair; `bar` is given as the issuing pair's leader barrier.
+__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                                    int32_t x, int32_t y, int32_t z,
+                                                    uint16_t cta_mask) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(cta_mask)
         : "memory");
 }
 
@@ -208,18 +213,6 @@ __device__ __forceinline__ void bulk_wait_group0() {
 // async-proxy (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// L2 eviction-priority policies for cache hints.
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
 }
 
 // ---------------------------------------------------------------- tcgen05

@@ -24,6 +24,10 @@ constexpr int kMinStreamKIters = 8;  // k-blocks per CTA share, at least
 constexpr int kAssumedMaxSms = 256;  // workspace sizing when no device answers
 constexpr int kPairStages = 6;
 constexpr int64_t kPairMinM = 256;   // from this many tokens on, the 2-SM kernel
+constexpr int64_t kQuadRows = 512;   // rows of a tile of two CTA pairs sharing weight tiles
+// Whether the automatic choice may take clusters of two pairs (multicast
+// weight tiles); SWIGLU_FUSED_VARIANT=4sm always can.
+constexpr bool kQuadAuto = false;
 using FusedC = FusedCfg<kFusedStages>;
 using PairC = PairCfg<kPairStages>;
 
@@ -31,14 +35,16 @@ using PairC = PairCfg<kPairStages>;
 int g_test_skip_first_fill = 0;  // set by swiglu_test_set_fault_injection
 #endif
 
-// Which kernel serves a call: the 2-SM (CTA pair) kernel for M >= 256, the
-// 1-SM kernel below. SWIGLU_FUSED_VARIANT=1sm|2sm overrides the choice (for
-// ablations and tests); it is read on every call.
-bool use_pair_kernel(int64_t M) {
+// SWIGLU_FUSED_VARIANT=1sm|2sm|4sm forces the 1-SM kernel, the CTA-pair
+// kernel, or clusters of two pairs that share weight tiles (for ablations
+// and tests); it is read on every call. 0: the automatic choice.
+int variant_override() {
     const char *v = std::getenv("SWIGLU_FUSED_VARIANT");
-    if (v && std::strcmp(v, "1sm") == 0) return false;
-    if (v && std::strcmp(v, "2sm") == 0) return true;
-    return M >= kPairMinM;
+    if (!v) return 0;
+    if (std::strcmp(v, "1sm") == 0) return 1;
+    if (std::strcmp(v, "2sm") == 0) return 2;
+    if (std::strcmp(v, "4sm") == 0) return 4;
+    return 0;
 }
 
 struct DeviceState {
@@ -46,6 +52,7 @@ struct DeviceState {
     int status = SWIGLU_OK;  // result of the one-time setup
     int sm_count = 0;
     int pair_clusters = 0;   // CTA pairs of the 2-SM kernel that can run at once
+    int quad_clusters = 0;   // clusters of two pairs that can run at once
 };
 
 DeviceState g_devices[kMaxDevices];
@@ -95,40 +102,50 @@ int device_setup(int *dev_out, DeviceState **st_out) {
         if (cudaFuncSetAttribute(fused_up_kernel<kFusedStages, ElemBF16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  FusedC::SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16>,
+            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16, 1>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PairC::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16, 2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairC::SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(fused_up_kernel<kFusedStages, ElemE4M3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  FusedC::SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemE4M3>,
+            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemE4M3, 1>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PairC::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemE4M3, 2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairC::SMEM_BYTES) != cudaSuccess) {
             cudaGetLastError();
             st.status = SWIGLU_ERR_CUDA;
             return;
         }
-        // how many CTA pairs fit at once (clusters must sit on SM pairs)
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(static_cast<unsigned>(sms / 2 * 2));
-        cfg.blockDim = dim3(PairC::THREADS);
-        cfg.dynamicSmemBytes = PairC::SMEM_BYTES;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, fused_up_pair_kernel<kPairStages, ElemBF16>,
-                                           &cfg) !=
-                cudaSuccess ||
-            clusters < 1) {
-            cudaGetLastError();
-            clusters = sms / 2;
-        }
-        st.pair_clusters = std::min(clusters, sms / 2);
+        // how many clusters of 2 and of 4 CTAs fit at once (a cluster sits
+        // inside one GPC, so not every SM count divides evenly)
+        auto max_clusters = [sms](int ctas, auto kernel) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(ctas);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(sms / ctas * ctas));
+            cfg.blockDim = dim3(PairC::THREADS);
+            cfg.dynamicSmemBytes = PairC::SMEM_BYTES;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                return -1;
+            }
+            return std::min(clusters, sms / ctas);
+        };
+        const int pairs = max_clusters(2, fused_up_pair_kernel<kPairStages, ElemBF16, 1>);
+        st.pair_clusters = pairs >= 1 ? pairs : sms / 2;
+        const int quads = max_clusters(4, fused_up_pair_kernel<kPairStages, ElemBF16, 2>);
+        st.quad_clusters = quads >= 1 ? quads : 0;   // 0: never use two-pair clusters
         st.sm_count = sms;
         st.status = SWIGLU_OK;
     });
@@ -164,15 +181,40 @@ int schedule_mode() {
     return kSchedAuto;
 }
 
-WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, bool pair, int kbk = 64) {
-    const int rows = pair ? PairC::UMMA_M : FusedC::BM;
+// Schedule for a kernel whose clusters hold `ctas` CTAs (1, 2 or 4: tiles of
+// 128, 256 or 512 rows), `workers` of them running at once.
+WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, int ctas, int kbk, int mode) {
+    const int rows = FusedC::BM * ctas;
     const int m_tiles = static_cast<int>((M + rows - 1) / rows);
     const int n_tiles = static_cast<int>((N + FusedC::BN - 1) / FusedC::BN);
     const int k_blocks = static_cast<int>((K + kbk - 1) / kbk);
     // few token rows: the kernel streams weights (HBM-bound), see plan_schedule
     const bool weight_bound = M <= 128;
-    return plan_schedule(m_tiles, n_tiles, k_blocks, workers, pair ? kGroupM / 2 : kGroupM,
-                         kMinStreamKIters, weight_bound, schedule_mode());
+    return plan_schedule(m_tiles, n_tiles, k_blocks, workers, kGroupM / ctas, kMinStreamKIters,
+                         weight_bound, mode);
+}
+
+// Which kernel serves a call, and its schedule: the 1-SM kernel below 256
+// rows, the CTA-pair kernel from there on. Clusters of two pairs (weight
+// tiles multicast to both) run whole tiles only; they are taken when forced,
+// or (if enabled) for multiples of 512 rows whose plan is whole tiles.
+struct LaunchPlan {
+    int ctas;        // CTAs per cluster: 1, 2 or 4
+    WorkSched sched;
+};
+LaunchPlan choose_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters,
+                       int quad_clusters, int kbk) {
+    const int v = variant_override();
+    const int mode = schedule_mode();
+    if (v == 1 || (v == 0 && M < kPairMinM)) return {1, plan_for(M, N, K, sms, 1, kbk, mode)};
+    if (v == 4 && quad_clusters > 0)
+        return {4, plan_for(M, N, K, quad_clusters, 4, kbk, kSchedDataParallel)};
+    if (v == 0 && kQuadAuto && quad_clusters > 0 && M % kQuadRows == 0 &&
+        (mode == kSchedAuto || mode == kSchedDataParallel)) {
+        const LaunchPlan q{4, plan_for(M, N, K, quad_clusters, 4, kbk, mode)};
+        if (q.sched.sk_iters == 0 && q.sched.n_split == 1) return q;
+    }
+    return {2, plan_for(M, N, K, pair_clusters, 2, kbk, mode)};
 }
 
 // Workspace layout: a counter region at offset 0 whose size depends only on
@@ -338,16 +380,16 @@ size_t workspace_bytes_impl(int64_t M, int64_t N, int64_t K) {
     if (M < 1 || N < 1 || K < 1 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
         K >= (int64_t(1) << 31))
         return 0;
-    const bool pair = use_pair_kernel(M);
     int dev;
     DeviceState *st;
-    if (device_setup(&dev, &st) == SWIGLU_OK)  // the same plan the forward will use
-        return workspace_bytes_for(
-            plan_for(M, N, K, pair ? st->pair_clusters : st->sm_count, pair, E::kBK), M, pair,
-            st->sm_count);
+    if (device_setup(&dev, &st) == SWIGLU_OK) {  // the same plan the forward will use
+        const LaunchPlan lp = choose_plan(M, N, K, st->sm_count, st->pair_clusters,
+                                          st->quad_clusters, E::kBK);
+        return workspace_bytes_for(lp.sched, M, lp.ctas == 2, st->sm_count);
+    }
     const int sms = current_sm_count();         // no usable device: a size for its SM count
-    return workspace_bytes_for(plan_for(M, N, K, pair ? sms / 2 : sms, pair, E::kBK), M, pair,
-                               sms);
+    const LaunchPlan lp = choose_plan(M, N, K, sms, sms / 2, 0, E::kBK);
+    return workspace_bytes_for(lp.sched, M, lp.ctas == 2, sms);
 }
 
 // The fused forward for element type E (BF16, or FP8 E4M3 with per-tensor
@@ -376,10 +418,11 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
     const int s = device_setup(&dev, &st);
     if (s != SWIGLU_OK) return s;
 
-    const bool pair = use_pair_kernel(M);
-    const WorkSched sched =
-        plan_for(M, N, K, pair ? st->pair_clusters : st->sm_count, pair, E::kBK);
-    const size_t ws_need = workspace_bytes_for(sched, M, pair, st->sm_count);
+    const LaunchPlan lp =
+        choose_plan(M, N, K, st->sm_count, st->pair_clusters, st->quad_clusters, E::kBK);
+    const WorkSched &sched = lp.sched;
+    const bool pair = lp.ctas >= 2;
+    const size_t ws_need = workspace_bytes_for(sched, M, lp.ctas == 2, st->sm_count);
     if (ws_need > 0) {
         if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
             workspace_bytes < ws_need)
@@ -435,15 +478,19 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
     cudaError_t err;
     if (pair) {
         attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(lp.ctas);
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
-        cfg.gridDim = dim3(static_cast<unsigned>(2 * sched.grid));
+        cfg.gridDim = dim3(static_cast<unsigned>(lp.ctas * sched.grid));
         cfg.blockDim = dim3(PairC::THREADS);
         cfg.dynamicSmemBytes = PairC::SMEM_BYTES;
-        err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages, E>, tmA, tmB, tmB64,
-                                 tmB32, tmY, args);
+        if (lp.ctas == 4)
+            err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages, E, 2>, tmA, tmB,
+                                     tmB64, tmB32, tmY, args);
+        else
+            err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages, E, 1>, tmA, tmB,
+                                     tmB64, tmB32, tmY, args);
     } else {
         cfg.numAttrs = 1;
         cfg.gridDim = dim3(static_cast<unsigned>(sched.grid));

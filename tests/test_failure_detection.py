@@ -60,7 +60,8 @@ def _run(lib, A, Wp, M, N, K, stream):
     return Y, status, raw.value
 
 
-@pytest.mark.parametrize("variant,M,N,K", [("1sm", 128, 256, 512), ("2sm", 512, 256, 512)])
+@pytest.mark.parametrize("variant,M,N,K", [("1sm", 128, 256, 512), ("2sm", 512, 256, 512),
+                                           ("4sm", 1024, 256, 512)])
 def test_wait_timeout_is_reported_and_context_survives(fi_lib, monkeypatch, variant, M, N, K):
     monkeypatch.setenv("SWIGLU_FUSED_VARIANT", variant)
     import oracle

@@ -56,6 +56,11 @@ constexpr int kKSteps = 4;       // UMMAs per k-block (32 bytes of each row apie
 // a warp (32 consecutive rows) touch 128 contiguous bytes per column.
 // slot_rows = min(128, M rounded up to 32): rows past it are never live.
 constexpr int kSlotCols = 256;
+// Stages whose loads a CTA asks L2 for while it waits on the previous
+// launch. Each TMA instruction takes ~0.1 us to issue, and the wait may
+// already be over (a launch that follows an evenly finishing one), so only
+// the first two.
+constexpr int kPrefetchStages = 2;
 
 __host__ __device__ __forceinline__ int slot_rows_for(long long M) {
     return M >= 128 ? 128 : static_cast<int>((M + 31) / 32 * 32);
@@ -152,6 +157,41 @@ __device__ __forceinline__ void tmem_ld_gu(uint32_t tbase, int c, float (&g)[32]
     for (int i = 0; i < 32; ++i) {
         g[i] = __uint_as_float(gr[i]);
         u[i] = __uint_as_float(ur[i]);
+    }
+}
+
+// Whole-tile epilogue into the warp's staging buffer: the four 32-column
+// chunks of Gate|Up are read from TMEM one chunk ahead of the arithmetic, so
+// each tcgen05.ld's latency hides behind the previous chunk's activation.
+// (tcgen05.wait::ld waits for all of the thread's loads, so the next chunk
+// is issued right after the wait that completes the current one.)
+__device__ __forceinline__ void epilogue_stage_tile(uint32_t tbase, uint32_t ybuf, int lane,
+                                                    float gs, float us) {
+    uint32_t gr[2][32], ur[2][32];
+    tmem_ld_32x32b_x32(tbase, gr[0]);
+    tmem_ld_32x32b_x32(tbase + 128, ur[0]);
+    tmem_ld_wait();
+    reg_fence32(gr[0]);
+    reg_fence32(ur[0]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int cur = i & 1;
+        if (i + 1 < 4) {
+            tmem_ld_32x32b_x32(tbase + 32 * (i + 1), gr[cur ^ 1]);
+            tmem_ld_32x32b_x32(tbase + 128 + 32 * (i + 1), ur[cur ^ 1]);
+        }
+        float g[32], u[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            g[k] = __uint_as_float(gr[cur][k]);
+            u[k] = __uint_as_float(ur[cur][k]);
+        }
+        stage_y32(ybuf, lane, 32 * i, g, u, gs, us);
+        if (i + 1 < 4) {
+            tmem_ld_wait();
+            reg_fence32(gr[cur ^ 1]);
+            reg_fence32(ur[cur ^ 1]);
+        }
     }
 }
 

@@ -46,19 +46,25 @@
 
 namespace swiglu {
 
-template <int STAGES>
+// BROWS = weight rows a stage holds: 256 (a whole tile's Gate and Up rows),
+// or, for launches made only of column sub-tiles of BROWS / 2 columns (the
+// narrow configurations), 128 or 64: smaller stages, so more of them fit
+// and more loads are in flight per SM. Sub-tiles store Y straight from
+// registers, so the narrow configurations have no Y staging buffer.
+template <int STAGES, int BROWS = 256>
 struct FusedCfg {
     static constexpr int BM = 128;                // token rows per tile = UMMA M
     static constexpr int BN = 128;                // output columns per tile
     static constexpr int BK = 64;                 // BF16 elements per 128-byte row
     static constexpr int UMMA_N = 2 * BN;         // Gate | Up
     static constexpr int UMMA_K = 16;
+    static constexpr bool NARROW = BROWS < UMMA_N;
     static constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-    static constexpr int B_BYTES = UMMA_N * BK * 2;  // 32 KB
+    static constexpr int B_BYTES = BROWS * BK * 2;  // 32 KB for a whole tile
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int EPI_WARPS = 4;
     static constexpr int Y_HALF_BYTES = 32 * 64 * 2;      // 32 rows x 64 cols, 4 KB
-    static constexpr int Y_WARP_BYTES = 2 * Y_HALF_BYTES;  // 32 rows x 128 cols
+    static constexpr int Y_WARP_BYTES = NARROW ? 0 : 2 * Y_HALF_BYTES;  // 32 rows x 128 cols
     static constexpr int TMEM_COLS = 2 * UMMA_N;          // two accumulator stages
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -73,14 +79,14 @@ struct FusedCfg {
     static_assert(UMMA_N == kSlotCols, "workspace slot shape");
 };
 
-template <int STAGES, typename E>
-__global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
+template <int STAGES, int BROWS, typename E>
+__global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
     fused_up_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB64,
                     const __grid_constant__ CUtensorMap tmB32,
                     const __grid_constant__ CUtensorMap tmY, const FusedArgs args) {
-    using C = FusedCfg<STAGES>;
+    using C = FusedCfg<STAGES, BROWS>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -139,7 +145,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
         if (it.next(u)) {
             int mb, nb;
             sched.order.coords(u.tile, mb, nb);
-            const int kend = (u.kb1 - u.kb0 < STAGES) ? u.kb1 : u.kb0 + STAGES;
+            const int kend = (u.kb1 - u.kb0 < kPrefetchStages) ? u.kb1 : u.kb0 + kPrefetchStages;
             for (int kb = u.kb0; kb < kend; ++kb) {
                 const int wtile = nb * sched.k_blocks + kb;
                 tma_prefetch_2d(&tmA, kb * E::kBK, mb * C::BM);
@@ -147,8 +153,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                     tma_prefetch_3d(&tmB, 0, 0, wtile);
                 } else {
                     const CUtensorMap *tmBn = (u.width == 64) ? &tmB64 : &tmB32;
-                    tma_prefetch_3d(tmBn, 0, u.sub * u.width, wtile);
-                    tma_prefetch_3d(tmBn, 0, C::BN + u.sub * u.width, wtile);
+                    tma_prefetch_4d(tmBn, 0, u.sub * u.width, 0, wtile);
                 }
             }
         }
@@ -186,6 +191,10 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                         continue;
                     }
 #endif
+                    if (2 * u.width > BROWS) {  // never planned: a unit wider than a stage
+                        ok = false;
+                        break;
+                    }
                     const uint32_t b_dst = sbase + C::OFF_B + stage * C::B_BYTES;
                     const int wtile = nb * sched.k_blocks + kb;
                     if (u.width == C::BN) {
@@ -194,15 +203,14 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                                     kb * E::kBK, mb * C::BM);
                         tma_load_3d(b_dst, &tmB, full_bar(stage), 0, 0, wtile);
                     } else {
-                        // column sub-tile: its Gate rows, then the matching Up rows
+                        // column sub-tile: its Gate rows, then the matching Up rows,
+                        // in one 4-D box (both halves of the packed tile)
                         const CUtensorMap *tmBn = (u.width == 64) ? &tmB64 : &tmB32;
                         mbar_arrive_expect_tx(full_bar(stage),
                                               args.a_tx_bytes + 2 * u.width * kRowBytes);
                         tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
                                     kb * E::kBK, mb * C::BM);
-                        tma_load_3d(b_dst, tmBn, full_bar(stage), 0, u.sub * u.width, wtile);
-                        tma_load_3d(b_dst + u.width * kRowBytes, tmBn, full_bar(stage), 0,
-                                    C::BN + u.sub * u.width, wtile);
+                        tma_load_4d(b_dst, tmBn, full_bar(stage), 0, u.sub * u.width, 0, wtile);
                     }
                     issued_mask |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -316,16 +324,19 @@ __global__ void __launch_bounds__(FusedCfg<STAGES>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty_bar(acc));
                 store_y = false;
+            } else if (C::NARROW) {
+                // unreachable: a narrow launch holds only column sub-tiles (the
+                // producer refuses anything wider), and it has no Y staging
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                store_y = false;
             } else if (!split) {
                 if (rows_live) {
                     if (lane == 0) bulk_wait_group_read0();  // last store has read ybuf
                     __syncwarp();
-#pragma unroll 1
-                    for (int c = 0; c < C::BN; c += 32) {
-                        float g[32], v[32];
-                        tmem_ld_gu(tbase, c, g, v);
-                        stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
-                    }
+                    static_assert(C::BN == 128, "four 32-column chunks");
+                    epilogue_stage_tile(tbase, ybuf, lane, args.gate_scale, args.up_scale);
                 }
                 tc_fence_before();
                 __syncwarp();

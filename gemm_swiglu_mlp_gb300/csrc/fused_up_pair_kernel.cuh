@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
             sched.order.coords(u.tile, tm, nb);
             const int pm = tm * PAIRS + pic;
             const CUtensorMap *tmBu = (u.width == C::BN) ? &tmB : (u.width == 64 ? &tmB64 : &tmB32);
-            const int kend = (u.kb1 - u.kb0 < STAGES) ? u.kb1 : u.kb0 + STAGES;
+            const int kend = (u.kb1 - u.kb0 < kPrefetchStages) ? u.kb1 : u.kb0 + kPrefetchStages;
             for (int kb = u.kb0; kb < kend; ++kb) {
                 tma_prefetch_2d(&tmA, kb * E::kBK, pm * C::UMMA_M + C::BM * static_cast<int>(half));
                 if (PAIRS == 2)
@@ -331,12 +331,8 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                 if (rows_live) {
                     if (lane == 0) bulk_wait_group_read0();
                     __syncwarp();
-#pragma unroll 1
-                    for (int c = 0; c < C::BN; c += 32) {
-                        float g[32], v[32];
-                        tmem_ld_gu(tbase, c, g, v);
-                        stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
-                    }
+                    static_assert(C::BN == 128, "four 32-column chunks");
+                    epilogue_stage_tile(tbase, ybuf, lane, args.gate_scale, args.up_scale);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -433,22 +429,27 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
 
     // ---- teardown
     __syncthreads();
-    cluster_sync();  // both CTAs out of their loops; abort flags final
-    if (*abort_flag && is_leader) {
-        if (warp == 0 && lane == 0) {
-            // every load of the pair completes on the leader's full barriers
-            for (int s = 0; s < STAGES; ++s)
-                if ((issued_mask >> s) & 1u)
-                    if (!mbar_wait_drain(full_bar(s), (last_parity >> s) & 1u))
-                        atomicOr(&g_status_word, kStatusDrainTimeout);
+    cluster_sync();  // every CTA out of its loops; abort flags final
+    // An abort sets the flag in every CTA of the cluster before this barrier,
+    // so all CTAs take the same branch. Without one, every issued load was
+    // consumed and every MMA completed before its accumulator was read.
+    if (*abort_flag) {
+        if (is_leader) {
+            if (warp == 0 && lane == 0) {
+                // every load into the pair completes on the leader's full barriers
+                for (int s = 0; s < STAGES; ++s)
+                    if ((issued_mask >> s) & 1u)
+                        if (!mbar_wait_drain(full_bar(s), (last_parity >> s) & 1u))
+                            atomicOr(&g_status_word, kStatusDrainTimeout);
+            }
+            if (warp == 1 && lane == 0) {
+                umma_commit_pair_mc(drain_bar, static_cast<uint16_t>(1u << leader_rank));
+                if (!mbar_wait_drain(drain_bar, 0)) atomicOr(&g_status_word, kStatusDrainTimeout);
+            }
         }
-        if (warp == 1 && lane == 0) {
-            umma_commit_pair_mc(drain_bar, 0x1);
-            if (!mbar_wait_drain(drain_bar, 0)) atomicOr(&g_status_word, kStatusDrainTimeout);
-        }
+        __syncthreads();
+        cluster_sync();  // the other CTAs stay until each leader has drained
     }
-    __syncthreads();
-    cluster_sync();  // the peer stays until the leader has drained
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();

@@ -152,6 +152,23 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int32_t x,
                  : "memory");
 }
 
+// 4-D tiled load global -> shared (x innermost).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z, int32_t w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *m, int32_t x, int32_t y,
+                                                int32_t z, int32_t w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
 // 2-SM variants: the destination is this CTA's shared memory, the
 // completion is signalled on `bar`, a shared::cluster address that may be
 // the leader (even) CTA's barrier of the pair.

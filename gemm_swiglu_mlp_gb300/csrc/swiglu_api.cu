@@ -19,6 +19,10 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kFusedStages = 4;
+// narrow 1-SM configurations (launches made only of column sub-tiles):
+// weight rows per stage and the stages that fit
+constexpr int kNarrow64Stages = 7;   // 64-column sub-tiles: 16 KB A + 16 KB weights
+constexpr int kNarrow32Stages = 9;   // 32-column sub-tiles: 16 KB A + 8 KB weights
 constexpr int kGroupM = 16;          // row-tiles per L2 group in the tile order
 constexpr int kMinStreamKIters = 8;  // k-blocks per CTA share, at least
 constexpr int kAssumedMaxSms = 256;  // workspace sizing when no device answers
@@ -29,6 +33,8 @@ constexpr int64_t kQuadRows = 512;   // rows of a tile of two CTA pairs sharing 
 // weight tiles); SWIGLU_FUSED_VARIANT=4sm always can.
 constexpr bool kQuadAuto = false;
 using FusedC = FusedCfg<kFusedStages>;
+using Narrow64C = FusedCfg<kNarrow64Stages, 128>;
+using Narrow32C = FusedCfg<kNarrow32Stages, 64>;
 using PairC = PairCfg<kPairStages>;
 
 #ifdef SWIGLU_TEST_FAULT_INJECTION
@@ -99,16 +105,28 @@ int device_setup(int *dev_out, DeviceState **st_out) {
             st.status = SWIGLU_ERR_UNSUPPORTED;
             return;
         }
-        if (cudaFuncSetAttribute(fused_up_kernel<kFusedStages, ElemBF16>,
+        if (cudaFuncSetAttribute(fused_up_kernel<kFusedStages, 256, ElemBF16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  FusedC::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_kernel<kNarrow64Stages, 128, ElemBF16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Narrow64C::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_kernel<kNarrow32Stages, 64, ElemBF16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Narrow32C::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_kernel<kNarrow64Stages, 128, ElemE4M3>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Narrow64C::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_kernel<kNarrow32Stages, 64, ElemE4M3>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Narrow32C::SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16, 1>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairC::SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16, 2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairC::SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(fused_up_kernel<kFusedStages, ElemE4M3>,
+            cudaFuncSetAttribute(fused_up_kernel<kFusedStages, 256, ElemE4M3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  FusedC::SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemE4M3, 1>,
@@ -259,6 +277,24 @@ bool encode_packed_weights(CUtensorMap *m, const void *base, uint64_t tiles, uin
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(elems), box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same packed weights as 4-D [tiles][2 halves][128 rows][row], with a box
+// of `box_rows` rows from BOTH halves: the Gate rows and the matching Up rows
+// of a column sub-tile in one load (they land back to back in shared memory).
+bool encode_packed_weight_halves(CUtensorMap *m, const void *base, uint64_t tiles,
+                                 uint32_t box_rows, bool fp8) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    const uint64_t elems = fp8 ? 128 : 64;
+    const cuuint64_t dims[4] = {elems, 128, 2, tiles};
+    const cuuint64_t strides[3] = {128, 128 * 128, 256 * 128};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(elems), box_rows, 2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -441,8 +477,12 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
     CUtensorMap tmA, tmB, tmB64, tmB32, tmY;
     if (!encode_2d(&tmA, A, K, M, E::kBK, a_rows, E::kFp8) ||
         !encode_packed_weights(&tmB, Wpacked, weight_tiles, pair ? 128u : 256u, E::kFp8) ||
-        !encode_packed_weights(&tmB64, Wpacked, weight_tiles, 64u, E::kFp8) ||
-        !encode_packed_weights(&tmB32, Wpacked, weight_tiles, 32u, E::kFp8) ||
+        // sub-tile maps: the pair kernels load one half (Gate or Up) per CTA,
+        // the 1-SM kernel both halves in one 4-D box
+        !(pair ? encode_packed_weights(&tmB64, Wpacked, weight_tiles, 64u, E::kFp8)
+               : encode_packed_weight_halves(&tmB64, Wpacked, weight_tiles, 64u, E::kFp8)) ||
+        !(pair ? encode_packed_weights(&tmB32, Wpacked, weight_tiles, 32u, E::kFp8)
+               : encode_packed_weight_halves(&tmB32, Wpacked, weight_tiles, 32u, E::kFp8)) ||
         !encode_2d(&tmY, Y, N, M, 64, 32))
         return SWIGLU_ERR_CUDA;
 
@@ -495,9 +535,22 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
         cfg.numAttrs = 1;
         cfg.gridDim = dim3(static_cast<unsigned>(sched.grid));
         cfg.blockDim = dim3(FusedC::THREADS);
-        cfg.dynamicSmemBytes = FusedC::SMEM_BYTES;
-        err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kFusedStages, E>, tmA, tmB, tmB64, tmB32,
-                                 tmY, args);
+        // A launch made only of column sub-tiles takes a narrow configuration:
+        // stages sized for its sub-tile, so more loads are in flight per SM.
+        const bool all_sub = sched.n_split > 1 && sched.dp_tiles == 0 && sched.sk_iters == 0;
+        if (all_sub && sched.n_split == 2) {
+            cfg.dynamicSmemBytes = Narrow64C::SMEM_BYTES;
+            err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kNarrow64Stages, 128, E>, tmA, tmB,
+                                     tmB64, tmB32, tmY, args);
+        } else if (all_sub && sched.n_split == 4) {
+            cfg.dynamicSmemBytes = Narrow32C::SMEM_BYTES;
+            err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kNarrow32Stages, 64, E>, tmA, tmB,
+                                     tmB64, tmB32, tmY, args);
+        } else {
+            cfg.dynamicSmemBytes = FusedC::SMEM_BYTES;
+            err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kFusedStages, 256, E>, tmA, tmB, tmB64,
+                                     tmB32, tmY, args);
+        }
     }
     if (err != cudaSuccess) {
         cudaGetLastError();

@@ -419,7 +419,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
             }
         }
         if (lane == 0) {
-            bulk_wait_group0();
+            // the last store has read its staging buffer; its writes to
+            // global memory complete with the grid (what the next launch's
+            // griddepcontrol.wait and stream order wait for)
+            bulk_wait_group_read0();
             if (!ok && !*abort_flag) {
                 atomicOr(&g_status_word, kStatusEpilogueTimeout);
                 set_abort_both();

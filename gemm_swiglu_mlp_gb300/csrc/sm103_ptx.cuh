@@ -221,11 +221,6 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-// Wait until all committed bulk stores have completed.
-__device__ __forceinline__ void bulk_wait_group0() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -11,7 +11,11 @@
 //                 shared-memory ring. Each A tile feeds both products. When
 //                 M < 128 the A box has only ceil(M/8)*8 rows: the rows past
 //                 it keep stale shared-memory data, which reaches only
-//                 accumulator rows >= M, and those are never stored.
+//                 accumulator rows >= M, and those are never stored. A
+//                 column sub-tile (64 or 32 output columns) loads its Gate
+//                 rows and the matching Up rows in one 4-D box; a launch made
+//                 only of sub-tiles uses narrow stages (BROWS weight rows),
+//                 so more of them fit.
 //   warp 1        MMA issuer: one tcgen05.mma (M=128, N=256, K=16) per K
 //                 step puts Gate in TMEM columns [0,128) and Up in [128,256)
 //                 of one accumulator stage; two stages (512 columns) let the
@@ -20,8 +24,9 @@
 //                 y = SiLU(g) * u in FP32, round to BF16, stage in 128-byte
 //                 swizzled shared memory, TMA store (clipped at M and N).
 //
-// Work is split by schedule.cuh: whole tiles first, then an even stream-K
-// split of the remaining k-block iterations. A tile cut between CTAs is
+// Work is split by schedule.cuh: whole tiles, column sub-tiles for the last
+// wave, or (for a handful of tiles) an even stream-K split of the k-block
+// iterations. A tile cut between CTAs is
 // finished without any inter-CTA waiting: every contributor writes its FP32
 // Gate/Up partial to a workspace slot and increments the tile's counter; the
 // one that brings the counter to the number of contributors sums all

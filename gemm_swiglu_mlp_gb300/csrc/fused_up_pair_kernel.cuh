@@ -19,8 +19,9 @@
 //     both CTAs' epilogue warps arrive on the leader's accumulator-empty
 //     barrier.
 //
-// Work split: schedule.cuh over pairs (data-parallel pair tiles, then
-// stream-K). Split tiles are summed per CTA half through the workspace as in
+// Work split: schedule.cuh over pairs (whole pair tiles, column sub-tiles
+// for the last wave, or stream-K for a handful of tiles). Split tiles are
+// summed per CTA half through the workspace as in
 // the 1-SM kernel (slot = (2 * pair + first/last) * 2 + half, counter =
 // 2 * stream-K tile + half, half = 0 for the leader CTA, 1 for its peer).
 //

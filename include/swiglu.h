@@ -94,8 +94,9 @@ int swiglu_pack_weights_nk(const void *W1, const void *W2, int64_t N, int64_t K,
  * the current device (the split of K over CTAs depends on its SM count).
  * 0 means none: pass workspace = NULL, workspace_bytes = 0. The workspace
  * holds FP32 Gate/Up partial tiles for tiles whose K range is split between
- * CTAs (balancing the last wave of tiles, or all tiles when there are fewer
- * tiles than SMs), plus one counter per such tile.
+ * CTAs, plus one counter per such tile. K is split only for problems of a
+ * handful of output tiles (whole tiles or column sub-tiles would leave most
+ * SMs idle), or when SWIGLU_SCHEDULE forces it (see swiglu_up_forward).
  */
 size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
@@ -116,10 +117,18 @@ size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * strides), M, N, K < 2^31; A, Wpacked, Y 16-byte aligned; Y must not overlap
  * A, Wpacked or the workspace. M, N and K need not be multiples of any tile
  * size. The schedule (tile shape, CTA count) is chosen from M, N, K and the
- * device's SM count; the result is bit-identical from run to run.
- * Errors: SWIGLU_ERR_INVALID_ARG, SWIGLU_ERR_UNSUPPORTED (device is not
- * sm_103 / sm_100-family with tcgen05), SWIGLU_ERR_CUDA (tensor-map encode
- * or launch failure). Device-side timeouts are reported later by
+ * device's SM count; the result is bit-identical from run to run. Two
+ * environment variables, read on every call, force a choice for ablations:
+ * SWIGLU_FUSED_VARIANT=1sm|2sm|4sm (1-SM kernel, CTA pairs, or clusters of
+ * two pairs sharing weight tiles) and SWIGLU_SCHEDULE=dp|split|sk|sk-tail
+ * (whole tiles, column sub-tiles in the last wave, split K over the last wave
+ * and the remainder, or over the remainder only); swiglu_workspace_bytes
+ * follows them too.
+ * The first call on a device does one-time set-up (kernel attributes); after
+ * it, calls may be captured into CUDA graphs and replayed.
+ * Errors: SWIGLU_ERR_INVALID_ARG, SWIGLU_ERR_UNSUPPORTED (the current device
+ * is not an sm_103 part), SWIGLU_ERR_CUDA (tensor-map encode or launch
+ * failure). Device-side timeouts are reported later by
  * swiglu_check_device_status.
  */
 int swiglu_up_forward(const void *A, const void *Wpacked, void *Y,

@@ -20,10 +20,17 @@
 //     barrier.
 //
 // Work split: schedule.cuh over pairs (whole pair tiles, column sub-tiles
-// for the last wave, or stream-K for a handful of tiles). Split tiles are
-// summed per CTA half through the workspace as in
-// the 1-SM kernel (slot = (2 * pair + first/last) * 2 + half, counter =
-// 2 * stream-K tile + half, half = 0 for the leader CTA, 1 for its peer).
+// for the last wave, or stream-K). A tile split over the K ranges of pairs
+// c_lo..c_hi (k order) is finished by its owner c_lo, whose range ends in
+// it, so it is always the owner's last unit: the other contributors write
+// their FP32 partials to workspace slots (slot = (2 * pair + first/last) * 2
+// + half, half = 0 for the leader CTA, 1 for its peer) and count themselves
+// in (counter = 2 * stream-K tile + half); the owner waits for the count
+// (bounded), brings the partials into its now idle operand ring with bulk
+// copies, adds them to its own accumulators in k order, activates, stores Y
+// and resets the counter. Only the owner waits, on CTAs that never wait for
+// it, and they finish their parts of the tile first (their range starts in
+// it).
 //
 // PAIRS = 2 (clusters of four CTAs, two pairs): the two pairs work on the
 // tiles of two vertically adjacent 256-row blocks with the same output
@@ -63,7 +70,8 @@ struct PairCfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_Y = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_BAR = OFF_Y + EPI_WARPS * Y_WARP_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull x2, tempty x2, drain
+    // full, empty, tfull x2, tempty x2, drain, fixup (split-tile partials)
+    static constexpr int NUM_BARS = 2 * STAGES + 6;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
@@ -102,6 +110,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     auto tfull_bar = [&](int a) { return sbase + C::OFF_BAR + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return sbase + C::OFF_BAR + 8u * (2 * STAGES + 2 + a); };
     const uint32_t drain_bar = sbase + C::OFF_BAR + 8u * (2 * STAGES + 4);
+    const uint32_t fix_bar = sbase + C::OFF_BAR + 8u * (2 * STAGES + 5);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     volatile int *last_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);
@@ -122,6 +131,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
             mbar_init(tempty_bar(a), 2 * C::EPI_WARPS);  // epilogue warps of both CTAs
         }
         mbar_init(drain_bar, 1);
+        mbar_init(fix_bar, 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_barrier_init();
@@ -345,62 +355,156 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                            static_cast<size_t>((2 * p + sched.sk_slot(p, u.sk)) * 2 + half) *
                                slot_floats;
                 };
-                float *slot = slot_of(pair);
-                if (rows_live) {
-#pragma unroll 1
-                    for (int c = 0; c < C::BN; c += 32) {
-                        float g[32], v[32];
-                        tmem_ld_gu(tbase, c, g, v);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            __stcg(slot + static_cast<size_t>(c + i) * args.slot_rows + row_in_tile,
-                                   g[i]);
-                            __stcg(slot + static_cast<size_t>(C::BN + c + i) * args.slot_rows +
-                                       row_in_tile,
-                                   v[i]);
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(tempty_leader);
-                __threadfence();
-                epilogue_bar();
                 unsigned int *counter = args.counters + 2 * u.sk + half;
-                if (lead_thread) {
-                    const unsigned int prev = atomicAdd(counter, 1u);
-                    *last_flag = (prev == static_cast<unsigned int>(c_hi - c_lo)) ? 1 : 0;
-                }
-                epilogue_bar();
-                store_y = *last_flag != 0;
-                if (store_y) {
-                    __threadfence();
+                const int others = c_hi - c_lo;
+                // column group width G (Gate and Up columns) whose partials of
+                // every other contributor fit in the operand ring at once
+                const uint32_t col_bytes = static_cast<uint32_t>(args.slot_rows) * 4u;
+                const uint32_t ring_bytes = STAGES * (C::A_BYTES + C::B_BYTES);
+                int G = 128;
+                while (G > 32 && static_cast<uint32_t>(others) * 2u * G * col_bytes > ring_bytes)
+                    G >>= 1;
+                const bool staged = static_cast<uint32_t>(others) * 2u * G * col_bytes <= ring_bytes;
+                if (pair != c_lo || !staged) {
+                    // a contributor (or an owner with too many partners to
+                    // stage): this CTA's FP32 partial -> its workspace slot
+                    float *slot = slot_of(pair);
                     if (rows_live) {
-                        if (lane == 0) bulk_wait_group_read0();
-                        __syncwarp();
 #pragma unroll 1
                         for (int c = 0; c < C::BN; c += 32) {
                             float g[32], v[32];
+                            tmem_ld_gu(tbase, c, g, v);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
-                                g[i] = 0.0f;
-                                v[i] = 0.0f;
+                                __stcg(slot + static_cast<size_t>(c + i) * args.slot_rows +
+                                           row_in_tile,
+                                       g[i]);
+                                __stcg(slot + static_cast<size_t>(C::BN + c + i) * args.slot_rows +
+                                           row_in_tile,
+                                       v[i]);
                             }
-                            for (int p = c_lo; p <= c_hi; ++p) {
-                                const float *src = slot_of(p);
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) {
-                                    const float pg = __ldcg(src + static_cast<size_t>(c + i) *
-                                                                      args.slot_rows + row_in_tile);
-                                    const float pu = __ldcg(src + static_cast<size_t>(C::BN + c + i) *
-                                                                      args.slot_rows + row_in_tile);
-                                    g[i] = (p == c_lo) ? pg : g[i] + pg;
-                                    v[i] = (p == c_lo) ? pu : v[i] + pu;
-                                }
-                            }
-                            stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
                         }
                     }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(tempty_leader);
+                    __threadfence();
+                    epilogue_bar();
+                    if (lead_thread) {
+                        const unsigned int prev = atomicAdd(counter, 1u);
+                        *last_flag = (prev == static_cast<unsigned int>(others)) ? 1 : 0;
+                    }
+                    epilogue_bar();
+                    store_y = *last_flag != 0;
+                    if (store_y) {
+                        // the last to count itself in (only when the owner
+                        // could not stage): sum every slot in k order
+                        __threadfence();
+                        if (rows_live) {
+                            if (lane == 0) bulk_wait_group_read0();
+                            __syncwarp();
+#pragma unroll 1
+                            for (int c = 0; c < C::BN; c += 32) {
+                                float g[32], v[32];
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    g[i] = 0.0f;
+                                    v[i] = 0.0f;
+                                }
+                                for (int p = c_lo; p <= c_hi; ++p) {
+                                    const float *src = slot_of(p);
+#pragma unroll
+                                    for (int i = 0; i < 32; ++i) {
+                                        const float pg = __ldcg(src + static_cast<size_t>(c + i) *
+                                                                          args.slot_rows +
+                                                                row_in_tile);
+                                        const float pu = __ldcg(
+                                            src + static_cast<size_t>(C::BN + c + i) * args.slot_rows +
+                                            row_in_tile);
+                                        g[i] = (p == c_lo) ? pg : g[i] + pg;
+                                        v[i] = (p == c_lo) ? pu : v[i] + pu;
+                                    }
+                                }
+                                stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
+                            }
+                        }
+                        if (lead_thread) *counter = 0u;
+                    }
+                } else {
+                    // the owner: wait until the `others` contributors have
+                    // written their partials, then add them to its own
+                    // accumulators, column group by column group, through
+                    // the idle operand ring
+                    bool got = true;
+                    if (lead_thread) {
+                        got = wait_counter_geq(counter, static_cast<unsigned int>(others));
+                        fence_proxy_async_global();
+                    }
+                    ok = epilogue_all(got);
+                    if (!ok) {
+                        if (lead_thread && !*abort_flag) {
+                            atomicOr(&g_status_word, kStatusEpilogueTimeout);
+                            set_abort_both();
+                        }
+                        break;
+                    }
+                    if (rows_live) {
+                        if (lane == 0) bulk_wait_group_read0();
+                        __syncwarp();
+                    }
+                    const uint32_t part_bytes = static_cast<uint32_t>(G) * col_bytes;
+                    uint32_t fix_phase = 0;
+#pragma unroll 1
+                    for (int g0 = 0; g0 < C::BN; g0 += G) {
+                        epilogue_bar();  // everyone is done reading the ring
+                        if (lead_thread) {
+                            mbar_arrive_expect_tx(fix_bar, static_cast<uint32_t>(others) * 2u *
+                                                               part_bytes);
+                            for (int q = 0; q < others; ++q) {
+                                const float *src = slot_of(c_lo + 1 + q);
+                                const uint32_t dst = sbase + static_cast<uint32_t>(q) * 2u * part_bytes;
+                                bulk_copy_g2s(dst, src + static_cast<size_t>(g0) * args.slot_rows,
+                                              part_bytes, fix_bar);
+                                bulk_copy_g2s(dst + part_bytes,
+                                              src + static_cast<size_t>(C::BN + g0) * args.slot_rows,
+                                              part_bytes, fix_bar);
+                            }
+                        }
+                        ok = epilogue_all(mbar_wait(fix_bar, fix_phase, abort_flag));
+                        fix_phase ^= 1u;
+                        if (!ok) break;
+                        if (rows_live) {
+                            const float *ring = reinterpret_cast<const float *>(smem);
+#pragma unroll 1
+                            for (int c = g0; c < g0 + G; c += 32) {
+                                float g[32], v[32];
+                                tmem_ld_gu(tbase, c, g, v);  // own part: first in k order
+                                for (int q = 0; q < others; ++q) {
+                                    const float *pg = ring + static_cast<size_t>(q) * 2u * G *
+                                                                 args.slot_rows;
+                                    const float *pu = pg + static_cast<size_t>(G) * args.slot_rows;
+#pragma unroll
+                                    for (int i = 0; i < 32; ++i) {
+                                        const size_t off = static_cast<size_t>(c - g0 + i) *
+                                                               args.slot_rows + row_in_tile;
+                                        g[i] += pg[off];
+                                        v[i] += pu[off];
+                                    }
+                                }
+                                stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
+                            }
+                        }
+                    }
+                    if (!ok) {
+                        if (lead_thread && !*abort_flag) {
+                            atomicOr(&g_status_word, kStatusEpilogueTimeout);
+                            set_abort_both();
+                        }
+                        break;
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(tempty_leader);
                     if (lead_thread) *counter = 0u;
                 }
             }

@@ -203,6 +203,37 @@ __device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensor
         : "memory");
 }
 
+// 1-D bulk copy global -> this CTA's shared memory (both addresses 16-byte
+// aligned, size a multiple of 16), completion signalled on `bar` as
+// transaction bytes.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to global memory
+// (including what an acquire made visible) before its later async-proxy
+// (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bounded wait until the 32-bit counter at `p` (global memory) reaches
+// `target`, with acquire semantics at GPU scope. False on timeout.
+__device__ __forceinline__ bool wait_counter_geq(const unsigned int *p, unsigned int target) {
+    const long long t0 = clock64();
+    while (true) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) return true;
+        if (clock64() - t0 > kWaitLimitCycles) return false;
+    }
+}
+
 // 2-D tiled store shared -> global (out-of-range rows/columns are clipped).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src, int32_t x,
                                              int32_t y) {

@@ -241,6 +241,11 @@ def _default_workspace(device, nbytes: int, stream) -> torch.Tensor:
     key = (dev.index, int(s.cuda_stream))
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
+        if torch.cuda.is_current_stream_capturing():
+            # an allocation made during capture belongs to the graph's pool
+            raise SwigluError(SWIGLU_ERR_INVALID_ARG,
+                              "this shape needs a workspace of %d bytes: allocate it before "
+                              "capturing (swiglu_workspace_bytes) and pass workspace=" % nbytes)
         with torch.cuda.stream(s):
             ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         _workspaces[key] = ws

@@ -27,3 +27,30 @@ def test_fusion_efficiency_by_hand():
     assert abs(bench.fusion_efficiency(w, 10e-6 + removed_s, 10e-6, 5000.0) - 1.0) < 1e-12
     assert abs(bench.fusion_efficiency(w, 10e-6 + 2 * removed_s, 10e-6, 5000.0) - 2.0) < 1e-12
     assert bench.fusion_efficiency(w, 10e-6, 10e-6, 5000.0) == 0.0
+
+
+def test_reference_arm_prints_one_contract_line(monkeypatch, capsys):
+    """The reference arm (the CPU oracle) on the small workload, one step:
+    one JSON line with the contract's keys, on this host's cores."""
+    import json
+    import oracle
+    oracle.build()
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+
+    class Args:
+        steps, warmup, dtype = 1, 3, "bf16"
+
+    monkeypatch.setattr(bench, "REFERENCE_BUDGET_S", 2.0)
+    assert bench.run_reference(Args(), workloads.BY_LABEL["0"]) == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    r = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e", "gpu_launches"):
+        assert key in r, key
+    assert r["impl"] == "reference" and r["metric"] == bench.METRIC and r["unit"] == "TFLOP/s"
+    assert r["value"] > 0 and r["cpu_baseline"]["kind"] == "oracle"
+    assert r["e2e"]["h2d_bytes_per_step"] == 0 and r["gpu_launches"] == 0
+    assert r["config"]["M"] == 128 and r["config"]["N"] == 4864 and r["config"]["K"] == 896

@@ -1,0 +1,41 @@
+"""bench.py on the GPU: the JSON line the benchmark contract asks for."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_bench_prints_one_contract_line(dtype):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "0", "--steps", "50",
+           "--warmup", "3", "--no-cpu-baseline", "--no-context", "--dtype", dtype]
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    r = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "e2e", "gpu_launches", "clocks"):
+        assert key in r, key
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in r["roofline"], key
+    for key in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"):
+        assert key in r["e2e"], key
+    for key in ("sm_mhz", "sm_max_mhz", "reasons"):
+        assert key in r["clocks"], key
+    assert r["value"] > 0 and r["e2e"]["value"] > 0 and r["gpu_launches"] == 50
+    assert r["roofline"]["bound"] == "hbm"          # the 0.5B shape streams weights
+    assert r["dtype"] == ("fp8-e4m3" if dtype == "fp8" else "bf16")
+    assert r["e2e"]["h2d_bytes_per_step"] == 128 * 896 * (1 if dtype == "fp8" else 2)
+    assert r["e2e"]["d2h_bytes_per_step"] == 128 * 4864 * 2

@@ -11,11 +11,19 @@ Activation Overlap for Efficient LLM Inference", Section 1 Introduction
 (Gate = A x W1, Up = A x W2, Y = SiLU(Gate) (.) Up) and the technical
 summary's problem statement; SiLU(x) = x / (1 + e^-x).
 
+``matmul`` is the plain product C = A x B (binary64 sums, one BF16 rounding),
+the down-projection out = Y x W3 that completes the gated MLP (the MLP whose
+run time the paper's Figure 1 splits; the paper defines only Gate, Up and
+Y); ``swiglu_mlp`` composes the two with Y rounded to BF16 in between, as
+the fused kernel stores it.
+
 Parity status: pinned (brute force with exact rationals on tiny shapes,
 closed forms W1 = 0 / W2 = 0 / rank-1, SiLU identities and textbook values,
 BF16 rounding on hand-built bit patterns including ties; FP8 E4M3 decoding
 on hand-derived patterns and an exact field-by-field decoder, and the FP8
-definition by exact-rational brute force with scales).
+definition by exact-rational brute force with scales; the plain product and
+the MLP composition by exact-rational brute force, column-selection and
+scaling closed forms).
 """
 from __future__ import annotations
 
@@ -77,6 +85,10 @@ def _load():
                                          i64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                          u16p, f64p, f64p, f64p, ctypes.c_int]
     lib.oracle_swiglu_up_fp8.restype = ctypes.c_int
+    lib.oracle_matmul.argtypes = [u16p, u16p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                  i64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                  u16p, f64p, ctypes.c_int]
+    lib.oracle_matmul.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -191,3 +203,45 @@ def swiglu_up_fp8(A8: np.ndarray, W18: np.ndarray, W28: np.ndarray, s_a: float, 
         out["G"] = G
         out["U"] = U
     return out
+
+
+def matmul(A: np.ndarray, B: np.ndarray, rows=None, cols=None, want_unrounded: bool = False,
+           nthreads: int = 0):
+    """Oracle C = A x B for BF16 bit patterns (A [M, K], B [K, N]): binary64
+    sums in increasing k, one BF16 RNE rounding. Returns {"C": [R, C] uint16}
+    and, on request, "Cd" (the unrounded sums). ``rows`` / ``cols`` as in
+    swiglu_up."""
+    lib = _load()
+    A = np.ascontiguousarray(A, dtype=np.uint16)
+    B = np.ascontiguousarray(B, dtype=np.uint16)
+    M, K = A.shape
+    K1, N = B.shape
+    if K1 != K:
+        raise ValueError("shape mismatch: A %s B %s" % (A.shape, B.shape))
+    if rows is None:
+        rows_arr, R = None, M
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        R = rows_arr.shape[0]
+    n0, n1 = (0, N) if cols is None else (int(cols[0]), int(cols[1]))
+    C = np.empty((R, max(0, n1 - n0)), dtype=np.uint16)
+    Cd = np.empty(C.shape, dtype=np.float64) if want_unrounded else None
+    rc = lib.oracle_matmul(_ptr(A, ctypes.c_uint16), _ptr(B, ctypes.c_uint16), M, N, K,
+                           _ptr(rows_arr, ctypes.c_int64), R, n0, n1,
+                           _ptr(C, ctypes.c_uint16), _ptr(Cd, ctypes.c_double), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_matmul failed (status %d)" % rc)
+    out = {"C": C}
+    if want_unrounded:
+        out["Cd"] = Cd
+    return out
+
+
+def swiglu_mlp(A: np.ndarray, W1: np.ndarray, W2: np.ndarray, W3: np.ndarray, rows=None,
+               nthreads: int = 0):
+    """The whole gated MLP, out = Y x W3 with Y = SiLU(A x W1) (.) (A x W2)
+    rounded to BF16 (as the fused up-projection stores it) and W3 [N, H].
+    Output row m needs only row m of Y, so ``rows`` limits both products.
+    Returns {"Y": [R, N], "out": [R, H]} (BF16 bits)."""
+    up = swiglu_up(A, W1, W2, rows=rows, nthreads=nthreads)
+    return {"Y": up["Y"], "out": matmul(up["Y"], W3, nthreads=nthreads)["C"]}

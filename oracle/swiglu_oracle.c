@@ -22,6 +22,10 @@
  * round-to-nearest-even, straight from the double (going through binary32
  * first could round twice).
  *
+ * oracle_matmul computes the plain product C = A x B the same way (one
+ * binary64 sum per element, one BF16 rounding): the down-projection
+ * out = Y x W3 that completes the gated MLP.
+ *
  * The loops are the definition written out: no blocking, no reordering of
  * the k sum, no fusion beyond the definition. Rows are split across threads;
  * each output element is computed by exactly one thread in the fixed order
@@ -108,6 +112,7 @@ typedef struct {
     const uint16_t *A, *W1, *W2;        /* BF16 inputs, or NULL when FP8 */
     const uint8_t *A8, *W18, *W28;      /* FP8 E4M3 inputs, or NULL when BF16 */
     double scale_gate, scale_up;        /* FP8: s_a * s_w1 and s_a * s_w2; BF16: 1 */
+    int plain;                          /* 1: out = A x W1 alone (no W2, no SiLU) */
     int64_t M, N, K;
     int64_t n0, n1;        /* output columns [n0, n1) */
     const int64_t *rows;   /* NULL: rows 0..nrows-1 */
@@ -143,11 +148,13 @@ static void *run_rows(void *arg)
             for (int64_t k = 0; k < K; ++k) {
                 const double a = oracle_bf16_to_double(a_row[k]);
                 const uint16_t *w1 = j->W1 + k * N + n0;
-                const uint16_t *w2 = j->W2 + k * N + n0;
-                for (int64_t i = 0; i < W; ++i) {
+                for (int64_t i = 0; i < W; ++i)
                     g[i] += a * oracle_bf16_to_double(w1[i]);
+                if (j->plain)
+                    continue;
+                const uint16_t *w2 = j->W2 + k * N + n0;
+                for (int64_t i = 0; i < W; ++i)
                     u[i] += a * oracle_bf16_to_double(w2[i]);
-                }
             }
         } else {
             /* FP8: the sums of the raw E4M3 values, then the per-tensor
@@ -167,9 +174,10 @@ static void *run_rows(void *arg)
                 u[i] *= j->scale_up;
             }
         }
-        /* Y = SiLU(Gate) (.) Up, rounded once to BF16. */
+        /* Y = SiLU(Gate) (.) Up (or, plain, the sum itself), rounded once
+         * to BF16. */
         for (int64_t i = 0; i < W; ++i) {
-            const double y = oracle_silu(g[i]) * u[i];
+            const double y = j->plain ? g[i] : oracle_silu(g[i]) * u[i];
             if (j->Y)
                 j->Y[r * W + i] = oracle_double_to_bf16(y);
             if (j->Yd)
@@ -294,5 +302,37 @@ int oracle_swiglu_up_fp8(const uint8_t *A8, const uint8_t *W18, const uint8_t *W
     proto.n0 = n0; proto.n1 = n1;
     proto.rows = rows; proto.nrows = nrows;
     proto.Y = Y; proto.Yd = Yd; proto.G = G; proto.U = U;
+    return run_jobs(&proto, nrows, nthreads);
+}
+
+/*
+ * Plain product C = A x B of BF16 bit patterns, A [M,K] and B [K,N]
+ * row-major: every product exact in binary64, the sum in increasing k, one
+ * BF16 round-to-nearest-even at the end. This is the down-projection that
+ * completes the gated MLP whose share of run time the paper measures
+ * ("Tile-Level Activation Overlap for Efficient LLM Inference", Section 1
+ * Introduction, Figure 1): out = Y x W3 with Y the BF16 output of the
+ * fused up-projection, W3 [N, H]. The paper defines only Gate, Up and Y;
+ * the down-projection is the usual completion of that MLP. Rows and
+ * columns as in oracle_swiglu_up; C_d (may be NULL) receives the unrounded
+ * binary64 sums.
+ */
+int oracle_matmul(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K,
+                  const int64_t *rows, int64_t nrows, int64_t n0, int64_t n1,
+                  uint16_t *C, double *C_d, int nthreads)
+{
+    if (!A || !B || check_rows(M, N, K, rows, nrows, n0, n1))
+        return 1;
+    if (nrows == 0 || n1 == n0)
+        return 0;
+    job_t proto;
+    memset(&proto, 0, sizeof proto);
+    proto.A = A; proto.W1 = B; proto.W2 = NULL;
+    proto.plain = 1;
+    proto.scale_gate = 1.0; proto.scale_up = 1.0;
+    proto.M = M; proto.N = N; proto.K = K;
+    proto.n0 = n0; proto.n1 = n1;
+    proto.rows = rows; proto.nrows = nrows;
+    proto.Y = C; proto.Yd = C_d;
     return run_jobs(&proto, nrows, nthreads);
 }

@@ -329,9 +329,11 @@ def time_mlp_context(w, W1, W2, sg, As, Wps, Ys, Wss, R, dev, stream, steps):
     """Context for the pages' Figure 1 ("Tile-Level Activation Overlap for
     Efficient LLM Inference", Section 1: SwiGLU and its intermediates as a
     share of MLP time): the whole gated MLP out = Y W3 with a synthetic
-    down-projection W3 [N, K]. Fused: this library's up-projection, then
-    torch.matmul (cuBLAS) for the down-projection. Eager: three cuBLAS GEMMs
-    and silu * mul, each also timed alone for the activation's share."""
+    down-projection W3 [N, K]. Fused: this library's whole-MLP call (the
+    fused up-projection, then its own down-projection kernel), and for
+    comparison the fused up-projection followed by torch.matmul (cuBLAS).
+    Eager: three cuBLAS GEMMs and silu * mul, each also timed alone for the
+    activation's share."""
     import numpy as np
     import torch
     import torch.nn.functional as F
@@ -346,6 +348,9 @@ def time_mlp_context(w, W1, W2, sg, As, Wps, Ys, Wss, R, dev, stream, steps):
     G = [torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
     U = [torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
     O = [torch.empty(w.M, w.K, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    W3ps = [sg.swiglu_pack_down_weights(W3s[j]) for j in range(R)]
+    mlp_ws = max(1, sg.swiglu_mlp_workspace_bytes(w.M, w.N, w.K))
+    MWs = [torch.zeros(mlp_ws, dtype=torch.uint8, device=dev) for _ in range(R)]
 
     def timed(fn):
         with torch.cuda.stream(stream):
@@ -375,21 +380,38 @@ def time_mlp_context(w, W1, W2, sg, As, Wps, Ys, Wss, R, dev, stream, steps):
 
     def fused(i):
         j = i % R
+        sg.swiglu_mlp_forward(As[j], Wps[j], W3ps[j], w.N, Y=Ys[j], out=O[j], workspace=MWs[j],
+                              stream=stream)
+
+    def fused_cublas_down(i):
+        j = i % R
         sg.swiglu_up_forward(As[j], Wps[j], w.N, Y=Ys[j], workspace=Wss[j], stream=stream)
         torch.matmul(Ys[j], W3s[j], out=O[j])
 
+    def down(i):
+        j = i % R
+        sg.swiglu_down_forward(Ys[j], W3ps[j], w.K, out=O[j], workspace=MWs[j], stream=stream)
+
     eager_ms = timed(eager)
     fused_ms = timed(fused)
+    fused_cublas_ms = timed(fused_cublas_down)
+    down_ms = timed(down)
     mlp_flops = w.flops + 2 * w.M * w.N * w.K
-    del W1s, W2s, W3s, G, U, O
+    down_flops = 2 * w.M * w.N * w.K
+    del W1s, W2s, W3s, W3ps, MWs, G, U, O
     return {"eager_mlp_ms": eager_ms, "fused_mlp_ms": fused_ms,
             "mlp_speedup": eager_ms / fused_ms,
             "fused_mlp_tflops": mlp_flops / (fused_ms * 1e-3) / 1e12,
+            "fused_up_cublas_down_mlp_ms": fused_cublas_ms,
+            "down_ms": down_ms, "down_tflops": down_flops / (down_ms * 1e-3) / 1e12,
+            "down_cublas_ms": op_ms["down_gemm"],
             "eager_op_ms": op_ms,
             "activation_share_of_eager_mlp": op_ms["silu_mul"] / sum(op_ms.values()),
             "what": "out = (SiLU(A W1) * (A W2)) W3, W3 [N, K] ~ N(0, 1/N) synthetic; fused = this "
-                    "library's up-projection + cuBLAS down-projection; eager = 3 cuBLAS GEMMs + "
-                    "silu*mul (Figure 1 of the pages measures this share on H100)"}
+                    "library's swiglu_mlp_forward (fused up-projection + its down-projection "
+                    "kernel); eager = 3 cuBLAS GEMMs + silu*mul (Figure 1 of the pages measures "
+                    "this share on H100); down_* = the down-projection alone, this library's "
+                    "kernel and cuBLAS"}
 
 
 def config_of(w, l2_note, dtype: str = "bf16"):

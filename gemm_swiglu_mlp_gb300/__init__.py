@@ -34,7 +34,9 @@ __all__ = [
     "swiglu_workspace_bytes",
     "swiglu_up_forward", "swiglu_up_forward_noalloc", "swiglu_check_device_status",
     "swiglu_packed_weight_bytes_fp8", "swiglu_pack_weights_fp8", "swiglu_workspace_bytes_fp8",
-    "swiglu_up_forward_fp8", "EXPORTED_SYMBOLS",
+    "swiglu_up_forward_fp8", "swiglu_down_packed_weight_bytes", "swiglu_pack_down_weights",
+    "swiglu_pack_down_weights_nk", "swiglu_down_workspace_bytes", "swiglu_down_forward",
+    "swiglu_mlp_workspace_bytes", "swiglu_mlp_forward", "EXPORTED_SYMBOLS",
 ]
 
 SWIGLU_OK = 0
@@ -48,13 +50,15 @@ EXPORTED_SYMBOLS = (
     "swiglu_pack_weights", "swiglu_pack_weights_nk", "swiglu_workspace_bytes",
     "swiglu_up_forward", "swiglu_up_forward_noalloc", "swiglu_check_device_status",
     "swiglu_packed_weight_bytes_fp8", "swiglu_pack_weights_fp8", "swiglu_workspace_bytes_fp8",
-    "swiglu_up_forward_fp8",
+    "swiglu_up_forward_fp8", "swiglu_down_packed_weight_bytes", "swiglu_pack_down_weights",
+    "swiglu_pack_down_weights_nk", "swiglu_down_workspace_bytes", "swiglu_down_forward",
+    "swiglu_mlp_workspace_bytes", "swiglu_mlp_forward",
 )
 
 _lock = threading.Lock()
 _lib = None
 _workspaces = {}   # (device index, stream handle) -> zero-initialised uint8 tensor
-_ws_bytes = {}     # (device index, M, N, K, kernel and schedule overrides) -> workspace bytes
+_ws_bytes = {}     # ([entry,] device index, M, N, K, kernel and schedule overrides) -> bytes
 
 
 class SwigluError(RuntimeError):
@@ -100,6 +104,20 @@ def load_library(path: str = LIB_PATH):
         f32 = ctypes.c_float
         lib.swiglu_up_forward_fp8.argtypes = [vp, vp, vp, i64, i64, i64, f32, f32, f32, vp, sz, vp]
         lib.swiglu_up_forward_fp8.restype = ctypes.c_int
+        lib.swiglu_down_packed_weight_bytes.argtypes = [i64, i64]
+        lib.swiglu_down_packed_weight_bytes.restype = sz
+        lib.swiglu_pack_down_weights.argtypes = [vp, i64, i64, vp, vp]
+        lib.swiglu_pack_down_weights.restype = ctypes.c_int
+        lib.swiglu_pack_down_weights_nk.argtypes = [vp, i64, i64, vp, vp]
+        lib.swiglu_pack_down_weights_nk.restype = ctypes.c_int
+        lib.swiglu_down_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.swiglu_down_workspace_bytes.restype = sz
+        lib.swiglu_down_forward.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+        lib.swiglu_down_forward.restype = ctypes.c_int
+        lib.swiglu_mlp_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.swiglu_mlp_workspace_bytes.restype = sz
+        lib.swiglu_mlp_forward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, sz, vp]
+        lib.swiglu_mlp_forward.restype = ctypes.c_int
         lib.swiglu_check_device_status.argtypes = [vp, u32p]
         lib.swiglu_check_device_status.restype = ctypes.c_int
         _lib = lib
@@ -268,6 +286,143 @@ def swiglu_up_forward_noalloc(A: torch.Tensor, Wpacked: torch.Tensor, N: int,
                                              M, N, K, _stream_handle(stream)),
                "swiglu_up_forward_noalloc")
     return Y
+
+
+def _workspace_args(kind: str, fn, dev: int, M: int, N: int, K: int, device, workspace, stream):
+    """(pointer, bytes) of the workspace for one call: the caller's, or this
+    module's per-(device, stream) default, sized by the library's own query."""
+    key = (kind, dev, M, N, K, os.environ.get("SWIGLU_FUSED_VARIANT"),
+           os.environ.get("SWIGLU_SCHEDULE"))
+    need = _ws_bytes.get(key)
+    if need is None:
+        need = _ws_bytes[key] = int(fn(M, N, K))
+    if not need:
+        return None, 0
+    if workspace is None:
+        workspace = _default_workspace(device, need, stream)
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+class _OnDevice:
+    """Makes `device` current for the duration of a call."""
+
+    def __init__(self, device):
+        self.dev = device.index
+
+    def __enter__(self):
+        self.prev = torch.cuda.current_device()
+        if self.dev != self.prev:
+            torch.cuda.set_device(self.dev)
+
+    def __exit__(self, *exc):
+        if self.dev != self.prev:
+            torch.cuda.set_device(self.prev)
+
+
+def swiglu_down_packed_weight_bytes(N: int, K: int) -> int:
+    return int(load_library().swiglu_down_packed_weight_bytes(int(N), int(K)))
+
+
+def swiglu_down_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().swiglu_down_workspace_bytes(int(M), int(N), int(K)))
+
+
+def swiglu_mlp_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().swiglu_mlp_workspace_bytes(int(M), int(N), int(K)))
+
+
+def _pack_down(fn_name: str, W: torch.Tensor, N: int, K: int, W3packed, stream) -> torch.Tensor:
+    lib = load_library()
+    nbytes = swiglu_down_packed_weight_bytes(N, K)
+    if W3packed is None:
+        W3packed = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    elif W3packed.numel() * W3packed.element_size() < nbytes or not W3packed.is_contiguous():
+        raise ValueError("W3packed must be contiguous with at least %d bytes" % nbytes)
+    a, b = (N, K) if fn_name == "swiglu_pack_down_weights" else (K, N)
+    with torch.cuda.device(W.device):
+        _check(getattr(lib, fn_name)(W.data_ptr(), a, b, W3packed.data_ptr(),
+                                     _stream_handle(stream)), fn_name)
+    return W3packed
+
+
+def swiglu_pack_down_weights(W3: torch.Tensor, W3packed: torch.Tensor = None,
+                             stream=None) -> torch.Tensor:
+    """Pack the down-projection weight W3 ([N, K] BF16, out = Y x W3)."""
+    _require_bf16_cuda(W3, "W3")
+    if W3.dim() != 2:
+        raise ValueError("W3 must be [N, K]")
+    N, K = W3.shape
+    return _pack_down("swiglu_pack_down_weights", W3, N, K, W3packed, stream)
+
+
+def swiglu_pack_down_weights_nk(W3t: torch.Tensor, W3packed: torch.Tensor = None,
+                                stream=None) -> torch.Tensor:
+    """Pack an nn.Linear-layout down-projection weight W3t ([K, N] BF16,
+    out = Y x W3t^T): the same packed result as swiglu_pack_down_weights(W3t.T)."""
+    _require_bf16_cuda(W3t, "W3t")
+    if W3t.dim() != 2:
+        raise ValueError("W3t must be [K, N]")
+    K, N = W3t.shape
+    return _pack_down("swiglu_pack_down_weights_nk", W3t, N, K, W3packed, stream)
+
+
+def _out_tensor(t, shape, device, name):
+    if t is None:
+        return torch.empty(shape, dtype=torch.bfloat16, device=device)
+    _require_bf16_cuda(t, name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must be %s" % (name, list(shape)))
+    return t
+
+
+def swiglu_down_forward(Y: torch.Tensor, W3packed: torch.Tensor, K: int, out: torch.Tensor = None,
+                        workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """out[M, K] = Y x W3 from Y [M, N] BF16 and packed W3 (plain product,
+    FP32 accumulation, BF16 out)."""
+    lib = load_library()
+    _require_bf16_cuda(Y, "Y")
+    if Y.dim() != 2:
+        raise ValueError("Y must be [M, N]")
+    M, N = Y.shape
+    K = int(K)
+    need = swiglu_down_packed_weight_bytes(N, K)
+    if not W3packed.is_cuda or W3packed.numel() * W3packed.element_size() < need:
+        raise ValueError("W3packed must be a CUDA buffer of at least %d bytes" % need)
+    out = _out_tensor(out, (M, K), Y.device, "out")
+    with _OnDevice(Y.device):
+        ws_ptr, ws_bytes = _workspace_args("down", swiglu_down_workspace_bytes, Y.device.index,
+                                           M, N, K, Y.device, workspace, stream)
+        _check(lib.swiglu_down_forward(Y.data_ptr(), W3packed.data_ptr(), out.data_ptr(), M, N, K,
+                                       ws_ptr, ws_bytes, _stream_handle(stream)),
+               "swiglu_down_forward")
+    return out
+
+
+def swiglu_mlp_forward(A: torch.Tensor, Wpacked: torch.Tensor, W3packed: torch.Tensor, N: int,
+                       Y: torch.Tensor = None, out: torch.Tensor = None,
+                       workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """The whole gated MLP, out[M, K] = (SiLU(A W1) (.) (A W2)) W3: the fused
+    up-projection into Y [M, N] (caller's or a new buffer), then the
+    down-projection. Returns out; Y holds the up-projection's output."""
+    lib = load_library()
+    _require_bf16_cuda(A, "A")
+    if A.dim() != 2:
+        raise ValueError("A must be [M, K]")
+    M, K = A.shape
+    N = int(N)
+    for buf, nbytes, name in ((Wpacked, swiglu_packed_weight_bytes(N, K), "Wpacked"),
+                              (W3packed, swiglu_down_packed_weight_bytes(N, K), "W3packed")):
+        if not buf.is_cuda or buf.numel() * buf.element_size() < nbytes:
+            raise ValueError("%s must be a CUDA buffer of at least %d bytes" % (name, nbytes))
+    Y = _out_tensor(Y, (M, N), A.device, "Y")
+    out = _out_tensor(out, (M, K), A.device, "out")
+    with _OnDevice(A.device):
+        ws_ptr, ws_bytes = _workspace_args("mlp", swiglu_mlp_workspace_bytes, A.device.index,
+                                           M, N, K, A.device, workspace, stream)
+        _check(lib.swiglu_mlp_forward(A.data_ptr(), Wpacked.data_ptr(), W3packed.data_ptr(),
+                                      Y.data_ptr(), out.data_ptr(), M, N, K, ws_ptr, ws_bytes,
+                                      _stream_handle(stream)), "swiglu_mlp_forward")
+    return out
 
 
 def _require_u8_cuda(t: torch.Tensor, name: str):

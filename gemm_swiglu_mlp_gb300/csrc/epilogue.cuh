@@ -217,6 +217,37 @@ __device__ __forceinline__ void store_y32_global(int row, int col, const float (
     }
 }
 
+// 32 consecutive output columns [col, col+32) of one row of a plain product
+// (no activation): FP32 rounded to BF16 (nearest, ties to even) and stored
+// to global memory in 16-byte pieces. Rows >= M and columns >= N are
+// skipped; N is a multiple of 8, so a piece is wholly inside or outside.
+__device__ __forceinline__ void store_plain32(int row, int col, const float (&x)[32],
+                                              const FusedArgs &args) {
+    if (row >= args.M) return;
+    uint16_t *dst = args.Y + static_cast<size_t>(row) * args.N + col;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (col + 8 * j >= args.N) break;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(x[8 * j + 2 * e], x[8 * j + 2 * e + 1]);
+        *reinterpret_cast<uint4 *>(dst + 8 * j) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Plain-product epilogue of a whole pair tile: the 256 accumulator columns
+// of this thread's row are output columns [col0, col0 + 256).
+__device__ __forceinline__ void epilogue_plain_tile(uint32_t tbase, int row, int col0,
+                                                    const FusedArgs &args) {
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+        float a[32], b[32];
+        tmem_ld_gu(tbase, c, a, b);   // columns c.. and 128 + c..
+        store_plain32(row, col0 + c, a, args);
+        store_plain32(row, col0 + 128 + c, b, args);
+    }
+}
+
 // Epilogue of a column sub-tile (width 64 or 32), or of a whole tile stored
 // without shared-memory staging (width 128): TMEM holds Gate in columns
 // [0, width) and Up in [width, 2*width). Each thread owns one output row.

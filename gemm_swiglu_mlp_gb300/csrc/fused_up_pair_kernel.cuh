@@ -41,6 +41,14 @@
 // Both pairs' MMA commits free a stage in all four CTAs (a multicast load
 // may refill it only when both pairs are done with it). Whole tiles only.
 //
+// PLAIN = true: the same kernel computes a plain product out = A x W (no
+// activation), the down-projection out = Y x W3 that completes the gated
+// MLP. The packed weight tile then holds 256 output columns (one CTA loads
+// 128 of them), the accumulator's 256 columns are those output columns, and
+// the epilogue rounds them to BF16 and stores them straight from registers.
+// Whole tiles and stream-K only (no column sub-tiles); split tiles are summed
+// exactly as above.
+//
 // Every wait is bounded. An abort sets the abort flag of every CTA of the
 // cluster; after a cluster barrier each leader drains the loads and MMAs in
 // flight (all loads into a pair complete on its leader's barriers), a second
@@ -80,7 +88,7 @@ struct PairCfg {
     static_assert(UMMA_N == kSlotCols, "workspace slot shape");
 };
 
-template <int STAGES, typename E, int PAIRS>
+template <int STAGES, typename E, int PAIRS, bool PLAIN = false>
 __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     fused_up_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
@@ -89,6 +97,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                          const __grid_constant__ CUtensorMap tmY, const FusedArgs args) {
     using C = PairCfg<STAGES>;
     static_assert(PAIRS == 1 || PAIRS == 2, "one pair, or two pairs sharing weight tiles");
+    static_assert(!PLAIN || (PAIRS == 1 && !E::kFp8), "plain product: BF16 CTA pairs");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -328,9 +337,18 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                 c_hi = sched.sk_owner(first + sched.k_blocks - 1);
             }
             const bool split = c_hi > c_lo;
-            bool store_y = true;
+            bool store_y = !PLAIN;   // a staged Y tile waits for its TMA store
+            // 32 summed columns of each accumulator half, at column c of the half
+            auto emit32 = [&](int c, const float (&g)[32], const float (&v)[32]) {
+                if constexpr (PLAIN) {
+                    store_plain32(row0 + lane, nb * C::UMMA_N + c, g, args);
+                    store_plain32(row0 + lane, nb * C::UMMA_N + C::BN + c, v, args);
+                } else {
+                    stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
+                }
+            };
 
-            if (u.width != C::BN) {
+            if (!PLAIN && u.width != C::BN) {
                 if (rows_live)
                     epilogue_subtile_store(tbase, u.width, row0 + lane, nb * C::BN + u.sub * u.width,
                                            args);
@@ -340,10 +358,14 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                 store_y = false;
             } else if (!split) {
                 if (rows_live) {
-                    if (lane == 0) bulk_wait_group_read0();
-                    __syncwarp();
                     static_assert(C::BN == 128, "four 32-column chunks");
-                    epilogue_stage_tile(tbase, ybuf, lane, args.gate_scale, args.up_scale);
+                    if constexpr (PLAIN) {
+                        epilogue_plain_tile(tbase, row0 + lane, nb * C::UMMA_N, args);
+                    } else {
+                        if (lane == 0) bulk_wait_group_read0();
+                        __syncwarp();
+                        epilogue_stage_tile(tbase, ybuf, lane, args.gate_scale, args.up_scale);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -395,8 +417,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                         *last_flag = (prev == static_cast<unsigned int>(others)) ? 1 : 0;
                     }
                     epilogue_bar();
-                    store_y = *last_flag != 0;
-                    if (store_y) {
+                    const bool last = *last_flag != 0;
+                    store_y = store_y && last;
+                    if (last) {
                         // the last to count itself in (only when the owner
                         // could not stage): sum every slot in k order
                         __threadfence();
@@ -425,7 +448,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                                         v[i] = (p == c_lo) ? pu : v[i] + pu;
                                     }
                                 }
-                                stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
+                                emit32(c, g, v);
                             }
                         }
                         if (lead_thread) *counter = 0u;
@@ -491,7 +514,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                                         v[i] += pu[off];
                                     }
                                 }
-                                stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
+                                emit32(c, g, v);
                             }
                         }
                     }

@@ -81,4 +81,57 @@ __global__ void __launch_bounds__(256) pack_weights_nk_kernel(const uint16_t *__
     }
 }
 
+// Down-projection weights, for the plain product out = Y x W3 that
+// completes the gated MLP: W3 [N, K] row-major (N, the intermediate size, is
+// the product's reduction; K, the hidden size, its output columns) ->
+// W3packed [KT][NB][256][64], KT = ceil(K/256) tiles of 256 output columns,
+// NB = ceil(N/64) k-blocks: element (j, b, r, nn) is W3[64b + nn][256j + r],
+// zero where the column is >= K or the k index is >= N. The same
+// tile-contiguous K-major form as the up-projection's packed weights, with
+// 256 output columns per tile in place of 128 Gate + 128 Up rows; the packed
+// row index 256j + r is the output column itself. A permutation plus zero
+// padding: bit-exact.
+__global__ void __launch_bounds__(256) pack_down_kernel(const uint16_t *__restrict__ W3,
+                                                         uint16_t *__restrict__ Wp, int N, int K,
+                                                         int NB) {
+    __shared__ uint16_t tile[kPackTile][kPackTile + 2];
+    const int b = blockIdx.x;                 // k-block (over N)
+    const int n0 = b * kPackTile;
+    const int p0 = blockIdx.y * kPackTile;    // first packed row = first output column
+    const int j = p0 / 256;
+    const int r0 = p0 % 256;
+    for (int i = threadIdx.x; i < kPackTile * kPackTile; i += blockDim.x) {
+        const int nn = i / kPackTile, cc = i % kPackTile;
+        const int n = n0 + nn, col = p0 + cc;
+        tile[nn][cc] = (n < N && col < K) ? W3[static_cast<int64_t>(n) * K + col] : uint16_t(0);
+    }
+    __syncthreads();
+    uint16_t *__restrict__ out = Wp + ((static_cast<int64_t>(j) * NB + b) * 256 + r0) * kPackTile;
+    for (int i = threadIdx.x; i < kPackTile * kPackTile; i += blockDim.x) {
+        const int cc = i / kPackTile, nn = i % kPackTile;
+        out[cc * kPackTile + nn] = tile[nn][cc];
+    }
+}
+
+// The same from the nn.Linear layout of the down-projection weight, W3t
+// [K, N] row-major (row c holds output column c's N weights, already
+// K-major): a row gather, packed row 256j + r = W3t[256j + r][64b .. 64b+63].
+__global__ void __launch_bounds__(256) pack_down_nk_kernel(const uint16_t *__restrict__ W3t,
+                                                            uint16_t *__restrict__ Wp, int N,
+                                                            int K, int NB) {
+    const int b = blockIdx.x;
+    const int p0 = blockIdx.y * kPackTile;
+    const int j = p0 / 256;
+    const int r0 = p0 % 256;
+    uint16_t *__restrict__ out = Wp + ((static_cast<int64_t>(j) * NB + b) * 256 + r0) * kPackTile;
+    for (int i = threadIdx.x; i < kPackTile * kPackTile / 8; i += blockDim.x) {
+        const int rr = i / (kPackTile / 8), c8 = (i % (kPackTile / 8)) * 8;
+        const int col = p0 + rr, n = b * kPackTile + c8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (col < K && n < N)   // N % 8 == 0: an 8-element piece is wholly in or out
+            v = *reinterpret_cast<const uint4 *>(W3t + static_cast<int64_t>(col) * N + n);
+        *reinterpret_cast<uint4 *>(out + rr * kPackTile + c8) = v;
+    }
+}
+
 }  // namespace swiglu

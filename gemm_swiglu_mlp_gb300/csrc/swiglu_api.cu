@@ -27,6 +27,7 @@ constexpr int kGroupM = 16;          // row-tiles per L2 group in the tile order
 constexpr int kMinStreamKIters = 8;  // k-blocks per CTA share, at least
 constexpr int kAssumedMaxSms = 256;  // workspace sizing when no device answers
 constexpr int kPairStages = 6;
+constexpr int kDownTileCols = 256;   // output columns of a plain-product (down) tile
 constexpr int64_t kPairMinM = 256;   // from this many tokens on, the 2-SM kernel
 constexpr int64_t kQuadRows = 512;   // rows of a tile of two CTA pairs sharing weight tiles
 // Whether the automatic choice may take clusters of two pairs (multicast
@@ -126,6 +127,9 @@ int device_setup(int *dev_out, DeviceState **st_out) {
             cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16, 2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairC::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16, 1, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PairC::SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(fused_up_kernel<kFusedStages, 256, ElemE4M3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  FusedC::SMEM_BYTES) != cudaSuccess ||
@@ -210,6 +214,30 @@ WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, int ctas, int k
     const bool weight_bound = M <= 128;
     return plan_schedule(m_tiles, n_tiles, k_blocks, workers, kGroupM / ctas, kMinStreamKIters,
                          weight_bound, mode);
+}
+
+// Schedule of the plain product out = Y x W3 (Y [M, N], W3 [N, K]): CTA
+// pairs on tiles of 256 rows x 256 output columns, k-blocks over N. Its
+// output has few tiles against a long reduction (the hidden size is a few
+// times smaller than the intermediate size), so whole tiles are kept only
+// when they fill at least 90% of the last wave and stream-K splits the
+// k-blocks otherwise (a split tile's partial sums cost a few k-blocks of
+// time against tiles of a hundred). Column sub-tiles do not apply.
+WorkSched plan_down(int64_t M, int64_t N, int64_t K, int workers) {
+    const int rows = FusedC::BM * 2;
+    const int m_tiles = static_cast<int>((M + rows - 1) / rows);
+    const int n_tiles = static_cast<int>((K + kDownTileCols - 1) / kDownTileCols);
+    const int k_blocks = static_cast<int>((N + ElemBF16::kBK - 1) / ElemBF16::kBK);
+    int mode = schedule_mode();
+    if (mode == kSchedColumnSplit) mode = kSchedAuto;
+    if (mode == kSchedAuto) {
+        const long long T = static_cast<long long>(m_tiles) * n_tiles;
+        const long long waves = (T + workers - 1) / workers;
+        const double eff = static_cast<double>(T) / (static_cast<double>(waves) * workers);
+        mode = eff >= 0.9 ? kSchedDataParallel : kSchedStreamK;
+    }
+    return plan_schedule(m_tiles, n_tiles, k_blocks, workers, kGroupM / 2, kMinStreamKIters,
+                         false, mode);
 }
 
 // Which kernel serves a call, and its schedule: the 1-SM kernel below 256
@@ -619,6 +647,210 @@ int swiglu_up_forward_fp8(const void *A8, const void *Wpacked8, void *Y, int64_t
         return SWIGLU_ERR_INVALID_ARG;   // also rejects NaN, and products that leave FP32
     return forward_impl<ElemE4M3>(A8, Wpacked8, Y, M, N, K, gs, us, workspace, workspace_bytes, stream,
                                   swiglu_packed_weight_bytes_fp8(N, K));
+}
+
+}  // extern "C"
+
+namespace swiglu {
+namespace {
+
+size_t down_workspace_bytes_impl(int64_t M, int64_t N, int64_t K) {
+    if (M < 1 || N < 1 || K < 1 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
+        K >= (int64_t(1) << 31))
+        return 0;
+    int dev;
+    DeviceState *st;
+    if (device_setup(&dev, &st) == SWIGLU_OK)
+        return workspace_bytes_for(plan_down(M, N, K, st->pair_clusters), M, true, st->sm_count);
+    const int sms = current_sm_count();
+    return workspace_bytes_for(plan_down(M, N, K, sms / 2), M, true, sms);
+}
+
+// Argument checks of the plain product out [M, K] = Y [M, N] x W3 [N, K].
+int down_checks(const void *Y, const void *W3packed, const void *out, int64_t M, int64_t N,
+                int64_t K) {
+    if (!Y || !W3packed || !out) return SWIGLU_ERR_INVALID_ARG;
+    if (M < 1 || N < 8 || K < 8 || (N % 8) != 0 || (K % 8) != 0) return SWIGLU_ERR_INVALID_ARG;
+    const int64_t lim = int64_t(1) << 31;
+    if (M >= lim || N >= lim || K >= lim) return SWIGLU_ERR_INVALID_ARG;
+    if (!aligned16(Y) || !aligned16(W3packed) || !aligned16(out)) return SWIGLU_ERR_INVALID_ARG;
+    const size_t obytes = static_cast<size_t>(M) * K * 2;
+    if (overlaps(out, obytes, Y, static_cast<size_t>(M) * N * 2) ||
+        overlaps(out, obytes, W3packed, swiglu_down_packed_weight_bytes(N, K)))
+        return SWIGLU_ERR_INVALID_ARG;
+    return SWIGLU_OK;
+}
+
+// out [M, K] = Y [M, N] x W3 [N, K] (W3 packed by swiglu_pack_down_weights),
+// BF16 in and out, FP32 accumulation: the CTA-pair kernel in its plain mode.
+int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M, int64_t N,
+                      int64_t K, void *workspace, size_t workspace_bytes, void *stream) {
+    const int c = down_checks(Y, W3packed, out, M, N, K);
+    if (c != SWIGLU_OK) return c;
+    const size_t obytes = static_cast<size_t>(M) * K * 2;
+    const size_t ybytes = static_cast<size_t>(M) * N * 2;
+    const size_t pbytes = swiglu_down_packed_weight_bytes(N, K);
+
+    int dev;
+    DeviceState *st;
+    const int s = device_setup(&dev, &st);
+    if (s != SWIGLU_OK) return s;
+    const WorkSched sched = plan_down(M, N, K, st->pair_clusters);
+    const size_t ws_need = workspace_bytes_for(sched, M, true, st->sm_count);
+    if (ws_need > 0) {
+        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+            workspace_bytes < ws_need)
+            return SWIGLU_ERR_INVALID_ARG;
+        if (overlaps(workspace, ws_need, out, obytes) || overlaps(workspace, ws_need, Y, ybytes) ||
+            overlaps(workspace, ws_need, W3packed, pbytes))
+            return SWIGLU_ERR_INVALID_ARG;
+    }
+    const uint64_t weight_tiles =
+        static_cast<uint64_t>(sched.order.n_tiles) * static_cast<uint64_t>(sched.k_blocks);
+    // the sub-tile maps are never used in the plain mode: the whole-tile map
+    // stands in for them
+    CUtensorMap tmA, tmB, tmOut;
+    if (!encode_2d(&tmA, Y, N, M, ElemBF16::kBK, FusedC::BM) ||
+        !encode_packed_weights(&tmB, W3packed, weight_tiles, 128u, false) ||
+        !encode_2d(&tmOut, out, K, M, 64, 32))
+        return SWIGLU_ERR_CUDA;
+
+    FusedArgs args;
+    args.M = static_cast<int>(M);
+    args.N = static_cast<int>(K);   // output columns
+    args.K = static_cast<int>(N);   // reduction
+    args.stage_tx_bytes = FusedC::BM * kRowBytes + FusedC::B_BYTES;
+    args.a_tx_bytes = FusedC::BM * kRowBytes;
+    args.Y = static_cast<uint16_t *>(out);
+    args.gate_scale = 1.0f;
+    args.up_scale = 1.0f;
+    args.slot_rows = slot_rows_for(M);
+    args.sched = sched;
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+    args.skip_first_fill = g_test_skip_first_fill;
+#endif
+    args.counters = ws_need ? static_cast<unsigned int *>(workspace) : nullptr;
+    args.partials = ws_need ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                        counter_region_bytes(st->sm_count))
+                            : nullptr;
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * sched.grid));
+    cfg.blockDim = dim3(PairC::THREADS);
+    cfg.dynamicSmemBytes = PairC::SMEM_BYTES;
+    const cudaError_t err =
+        cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages, ElemBF16, 1, true>, tmA, tmB,
+                           tmB, tmB, tmOut, args);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SWIGLU_ERR_CUDA;
+    }
+    return SWIGLU_OK;
+}
+
+// Shared checks of the two down-weight packs; on success the launch grid.
+int pack_down_checks(const void *W, int64_t N, int64_t K, void *W3packed, dim3 *grid) {
+    if (!W || !W3packed) return SWIGLU_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0 || (N % 8) != 0 || (K % 8) != 0) return SWIGLU_ERR_INVALID_ARG;
+    if (N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return SWIGLU_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(W3packed)) return SWIGLU_ERR_INVALID_ARG;
+    if (overlaps(W3packed, swiglu_down_packed_weight_bytes(N, K), W, static_cast<size_t>(N) * K * 2))
+        return SWIGLU_ERR_INVALID_ARG;
+    const int64_t rows = round_up(K, kDownTileCols);
+    if (rows / kPackTile > 65535) return SWIGLU_ERR_UNSUPPORTED;
+    *grid = dim3(static_cast<unsigned>((N + kPackTile - 1) / kPackTile),
+                 static_cast<unsigned>(rows / kPackTile));
+    return SWIGLU_OK;
+}
+
+}  // namespace
+}  // namespace swiglu
+
+extern "C" {
+
+size_t swiglu_down_packed_weight_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0) return 0;
+    return static_cast<size_t>(round_up(K, kDownTileCols)) * static_cast<size_t>(round_up(N, 64)) *
+           2u;
+}
+
+int swiglu_pack_down_weights(const void *W3, int64_t N, int64_t K, void *W3packed, void *stream) {
+    dim3 grid;
+    int s = pack_down_checks(W3, N, K, W3packed, &grid);
+    if (s != SWIGLU_OK) return s;
+    int dev;
+    DeviceState *st;
+    s = device_setup(&dev, &st);
+    if (s != SWIGLU_OK) return s;
+    pack_down_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(W3), static_cast<uint16_t *>(W3packed), static_cast<int>(N),
+        static_cast<int>(K), static_cast<int>(grid.x));
+    if (cudaGetLastError() != cudaSuccess) return SWIGLU_ERR_CUDA;
+    return SWIGLU_OK;
+}
+
+int swiglu_pack_down_weights_nk(const void *W3t, int64_t K, int64_t N, void *W3packed,
+                                void *stream) {
+    dim3 grid;
+    int s = pack_down_checks(W3t, N, K, W3packed, &grid);
+    if (s != SWIGLU_OK) return s;
+    int dev;
+    DeviceState *st;
+    s = device_setup(&dev, &st);
+    if (s != SWIGLU_OK) return s;
+    pack_down_nk_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(W3t), static_cast<uint16_t *>(W3packed), static_cast<int>(N),
+        static_cast<int>(K), static_cast<int>(grid.x));
+    if (cudaGetLastError() != cudaSuccess) return SWIGLU_ERR_CUDA;
+    return SWIGLU_OK;
+}
+
+size_t swiglu_down_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    return down_workspace_bytes_impl(M, N, K);
+}
+
+int swiglu_down_forward(const void *Y, const void *W3packed, void *out, int64_t M, int64_t N,
+                        int64_t K, void *workspace, size_t workspace_bytes, void *stream) {
+    return down_forward_impl(Y, W3packed, out, M, N, K, workspace, workspace_bytes, stream);
+}
+
+size_t swiglu_mlp_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    return std::max(swiglu_workspace_bytes(M, N, K), down_workspace_bytes_impl(M, N, K));
+}
+
+int swiglu_mlp_forward(const void *A, const void *Wpacked, const void *W3packed, void *Y,
+                       void *out, int64_t M, int64_t N, int64_t K, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+    // everything the two launches need is checked before the first one
+    if (!A || !Wpacked) return SWIGLU_ERR_INVALID_ARG;
+    const int c = down_checks(Y, W3packed, out, M, N, K);
+    if (c != SWIGLU_OK) return c;
+    const size_t obytes = static_cast<size_t>(M) * K * 2;
+    const size_t ybytes = static_cast<size_t>(M) * N * 2;
+    const size_t p3bytes = swiglu_down_packed_weight_bytes(N, K);
+    if (overlaps(out, obytes, A, obytes) ||
+        overlaps(out, obytes, Wpacked, swiglu_packed_weight_bytes(N, K)) ||
+        overlaps(Y, ybytes, W3packed, p3bytes))
+        return SWIGLU_ERR_INVALID_ARG;
+    const size_t need = swiglu_mlp_workspace_bytes(M, N, K);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return SWIGLU_ERR_INVALID_ARG;
+        if (overlaps(workspace, need, out, obytes) || overlaps(workspace, need, W3packed, p3bytes))
+            return SWIGLU_ERR_INVALID_ARG;
+    }
+    int s = swiglu_up_forward(A, Wpacked, Y, M, N, K, workspace, workspace_bytes, stream);
+    if (s != SWIGLU_OK) return s;
+    return down_forward_impl(Y, W3packed, out, M, N, K, workspace, workspace_bytes, stream);
 }
 
 int swiglu_check_device_status(void *stream, uint32_t *raw_word) {

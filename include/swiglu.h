@@ -216,6 +216,78 @@ int swiglu_up_forward_fp8(const void *A8, const void *Wpacked8, void *Y,
                           float scale_a, float scale_w1, float scale_w2,
                           void *workspace, size_t workspace_bytes, void *stream);
 
+/* ------------------------------------------------------------------------
+ * The whole gated MLP: out = Y x W3 after the fused up-projection. The paper
+ * defines Gate, Up and Y (Section 1 Introduction) and measures the
+ * activation's share of the whole MLP's run time (Figure 1), but gives no
+ * down-projection; out = Y x W3 with W3 [N, K] (N the intermediate size, K
+ * the hidden size) is the usual completion of that MLP, and these entry
+ * points are this library's extension. The down-projection is a plain
+ * product: BF16 Y and W3, FP32 accumulation in tensor memory, each output
+ * rounded once to BF16 (round to nearest even). It runs on the CTA-pair
+ * kernel in a plain mode (tiles of 256 rows x 256 output columns; stream-K
+ * over N when whole tiles would leave the last wave less than 90% full).
+ * ---------------------------------------------------------------------- */
+
+/* Packed down-projection weight bytes: [KT][NB][256][64] BF16 values,
+ * KT = ceil(K/256) tiles of 256 output columns, NB = ceil(N/64) k-blocks.
+ * Returns 0 if N <= 0 or K <= 0. */
+size_t swiglu_down_packed_weight_bytes(int64_t N, int64_t K);
+
+/* Packs W3 (device, BF16, [N, K] row-major: out = Y x W3) into W3packed
+ * (device, swiglu_down_packed_weight_bytes(N, K) bytes, any prior content):
+ * element (j, b, r, i) = W3[64b + i][256j + r], zero padded. A permutation:
+ * bit-exact. Requirements: N > 0, K > 0, N % 8 == 0, K % 8 == 0, pointers
+ * non-null and 16-byte aligned, no overlap. Asynchronous on `stream`. */
+int swiglu_pack_down_weights(const void *W3, int64_t N, int64_t K, void *W3packed,
+                             void *stream);
+
+/* The same from the nn.Linear layout of the down-projection weight: W3t
+ * (device, BF16, [K, N] row-major, W3t[c][n] = W3[n][c]). Note the argument
+ * order (K, N), the order of W3t's dimensions. Same packed result. */
+int swiglu_pack_down_weights_nk(const void *W3t, int64_t K, int64_t N, void *W3packed,
+                                void *stream);
+
+/* Workspace bytes of swiglu_down_forward for (M, N, K) on the current device
+ * (0: none needed). Same rules and layout as swiglu_workspace_bytes. */
+size_t swiglu_down_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * out = Y x W3, the down-projection alone.
+ *   Y         device, BF16, [M, N] row-major (e.g. swiglu_up_forward's Y)
+ *   W3packed  device, output of swiglu_pack_down_weights for this (N, K)
+ *   out       device, BF16, [M, K] row-major; fully overwritten
+ *   workspace: as swiglu_up_forward, sized by swiglu_down_workspace_bytes
+ * Requirements: M >= 1, N >= 8, K >= 8, N % 8 == 0, K % 8 == 0, M, N, K <
+ * 2^31; pointers 16-byte aligned; out must not overlap Y, W3packed or the
+ * workspace. SWIGLU_SCHEDULE=dp|sk|sk-tail forces a work split as for
+ * swiglu_up_forward (split is not offered here and means the automatic
+ * choice); SWIGLU_FUSED_VARIANT does not apply. Errors as swiglu_up_forward.
+ */
+int swiglu_down_forward(const void *Y, const void *W3packed, void *out,
+                        int64_t M, int64_t N, int64_t K,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of swiglu_mlp_forward: the larger of the two products'. */
+size_t swiglu_mlp_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * out = (SiLU(A x W1) (.) (A x W2)) x W3: swiglu_up_forward into Y, then
+ * swiglu_down_forward from Y, two launches on `stream` (the second starts
+ * while the first finishes and waits for its results before reading Y).
+ *   A, Wpacked  as swiglu_up_forward; W3packed as swiglu_down_forward
+ *   Y           device, BF16, [M, N]: the intermediate, caller-owned,
+ *               overwritten (it holds the up-projection's output afterwards)
+ *   out         device, BF16, [M, K]; fully overwritten
+ *   workspace   shared by both launches, at least swiglu_mlp_workspace_bytes
+ * Every argument of both launches is checked before the first is made.
+ * Requirements: those of both entry points; out must not overlap A or
+ * Wpacked, and Y must not overlap W3packed.
+ */
+int swiglu_mlp_forward(const void *A, const void *Wpacked, const void *W3packed, void *Y,
+                       void *out, int64_t M, int64_t N, int64_t K,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
 /*
  * Synchronizes `stream`, then reads and clears the current device's status
  * word. Every wait inside the kernels is bounded (about a second); a kernel

@@ -75,6 +75,17 @@ def fp32_accumulation_bound(A_bits, W1_bits, W2_bits, G, U, values=None):
     return scale * (np.abs(dsilu) * np.abs(U) * n1 + np.abs(G * sig) * n2)
 
 
+def plain_accumulation_bound(A_bits, B_bits):
+    """The same FP32 accumulation scale for a plain product C = A x B (no
+    activation): c 2^-24 sqrt(K) ||a (.) b||_2 per output element, for the
+    rows of A_bits [R, K] and B_bits [K, N]."""
+    A_v, B_v = bits_to_f64(A_bits), bits_to_f64(B_bits)
+    K = A_v.shape[1]
+    scale = ACCUM_C * 2.0 ** -24 * np.sqrt(K)
+    a2 = np.square(A_v).astype(np.float32)
+    return scale * np.sqrt((a2 @ np.square(B_v).astype(np.float32)).astype(np.float64))
+
+
 def compare(got_bits: np.ndarray, want_bits: np.ndarray, accum_bound=None) -> dict:
     got = bits_to_f64(got_bits)
     want = bits_to_f64(want_bits)
@@ -145,6 +156,22 @@ def unpack_reference(P: np.ndarray, K: int, N: int):
     w1 = T[:, :, :128, :].transpose(1, 3, 0, 2).reshape(KB * 64, NB * 128)
     w2 = T[:, :, 128:, :].transpose(1, 3, 0, 2).reshape(KB * 64, NB * 128)
     return w1[:K, :N], w2[:K, :N]
+
+
+def pack_down_reference(W3: np.ndarray) -> np.ndarray:
+    """The packed down-projection layout, written out with numpy slicing:
+    [KT][NB][256][64] with KT = ceil(K/256), NB = ceil(N/64) for W3 [N, K];
+    tile (j, b) = W3[64b:64b+64, 256j:256j+256] transposed; zero outside N
+    and K. Returned as a flat uint16 array."""
+    N, K = W3.shape
+    KT, NB = -(-K // 256), -(-N // 64)
+    w = np.zeros((NB * 64, KT * 256), np.uint16)
+    w[:N, :K] = W3
+    P = np.zeros((KT, NB, 256, 64), np.uint16)
+    for j in range(KT):
+        for b in range(NB):
+            P[j, b] = w[64 * b:64 * b + 64, 256 * j:256 * j + 256].T
+    return P.reshape(-1)
 
 
 def pack_reference_fp8(W1: np.ndarray, W2: np.ndarray) -> np.ndarray:

@@ -179,3 +179,34 @@ def test_parity_criteria_by_hand():
     got = workloads.f32_to_bf16_bits(np.array([1.0, 5e-6, 100.0, 1e-4], np.float32))
     r = parity.compare(got, want)
     assert r["mismatches"] == 0 and r["over_bound"] == 0 and r["literal_rel_mismatches"] == 1
+
+
+def test_down_sizes_and_host_validation(lib):
+    """The down-projection / whole-MLP entry points: packed size and
+    argument checks made on the host before anything is launched."""
+    import gemm_swiglu_mlp_gb300 as sg
+    assert sg.swiglu_down_packed_weight_bytes(8960, 1536) == 1536 * 8960 * 2
+    assert sg.swiglu_down_packed_weight_bytes(4864, 896) == 1024 * 4864 * 2   # K -> 4 x 256
+    assert sg.swiglu_down_packed_weight_bytes(72, 8) == 256 * 128 * 2         # N -> 128
+    assert sg.swiglu_down_packed_weight_bytes(0, 8) == 0
+    assert sg.swiglu_down_workspace_bytes(2048, 8960, 1536) >= 0
+    assert sg.swiglu_mlp_workspace_bytes(2048, 8960, 1536) >= max(
+        sg.swiglu_workspace_bytes(2048, 8960, 1536), sg.swiglu_down_workspace_bytes(2048, 8960, 1536))
+    d = lib.swiglu_down_forward
+    for bad in [(0, Q, R, 4, 8, 8), (P, 0, R, 4, 8, 8), (P, Q, 0, 4, 8, 8),   # null pointers
+                (P, Q, R, 0, 8, 8), (P, Q, R, 4, 12, 8), (P, Q, R, 4, 8, 12),  # M, N, K
+                (P + 8, Q, R, 4, 8, 8), (P, Q, R + 2, 4, 8, 8),                # misaligned
+                (P, Q, P, 4, 8, 8), (P, Q, Q, 4, 8, 8)]:                       # out aliases Y, W3
+        assert d(*bad, None, 0, None) == 1, bad
+    m = lib.swiglu_mlp_forward
+    S = 0xC0000000
+    for bad in [(0, Q, R, S, P + 0x100000, 4, 8, 8),                          # null A
+                (P, Q, R, S, S, 4, 8, 8),                                     # out aliases Y
+                (P, Q, R, S, P, 4, 8, 8),                                     # out aliases A
+                (P, Q, R, R, S, 4, 8, 8),                                     # Y aliases W3packed
+                (P, Q, R, S, P + 0x100000, 4, 12, 8)]:                        # N % 8 != 0
+        assert m(*bad, None, 0, None) == 1, bad
+    for bad in [(0, 64, 64, R), (P, 60, 64, R), (P, 64, 4, R), (P + 2, 64, 64, R), (P, 64, 64, P)]:
+        W, N, K, Wp = bad
+        assert lib.swiglu_pack_down_weights(W, N, K, Wp, None) == 1, bad
+        assert lib.swiglu_pack_down_weights_nk(W, K, N, Wp, None) == 1, bad

@@ -235,17 +235,47 @@ __device__ __forceinline__ void store_plain32(int row, int col, const float (&x)
     }
 }
 
-// Plain-product epilogue of a whole pair tile: the 256 accumulator columns
-// of this thread's row are output columns [col0, col0 + 256).
-__device__ __forceinline__ void epilogue_plain_tile(uint32_t tbase, int row, int col0,
-                                                    const FusedArgs &args) {
+// 32 values rounded to BF16 into a warp's staging buffer at output column
+// `col` (a multiple of 32): boxes of 64 columns x 32 rows (4 KB each, one
+// 128-byte row per lane, 16-byte chunks XOR-swizzled by row), the layout a
+// 128-byte-swizzled TMA store of 64 x 32 reads.
+__device__ __forceinline__ void stage_bf16x32(uint32_t stg, int lane, int col,
+                                              const float (&x)[32]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(x[8 * j + 2 * e], x[8 * j + 2 * e + 1]);
+        const int cc = col + 8 * j;
+        const uint32_t addr = stg + (cc >> 6) * (32 * 64 * 2) + lane * 128 +
+                              (static_cast<uint32_t>(((cc & 63) >> 3) ^ (lane & 7)) << 4);
+        st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+    }
+}
+
+// 128 accumulator columns [tcol, tcol+128) of this thread's row, rounded to
+// BF16 into the warp's staging buffer (columns 0..127).
+__device__ __forceinline__ void stage_plain_128(uint32_t tbase, uint32_t stg, int lane) {
 #pragma unroll 1
     for (int c = 0; c < 128; c += 32) {
-        float a[32], b[32];
-        tmem_ld_gu(tbase, c, a, b);   // columns c.. and 128 + c..
-        store_plain32(row, col0 + c, a, args);
-        store_plain32(row, col0 + 128 + c, b, args);
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tbase + c, r);
+        tmem_ld_wait();
+        reg_fence32(r);
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+        stage_bf16x32(stg, lane, c, x);
     }
+}
+
+// TMA stores of `boxes` staged 64 x 32 boxes to output columns x0, x0+64,
+// ... of rows [row0, row0+32); boxes wholly past column n are skipped (TMA
+// clips the rest at the tensor's edges). One thread; the caller commits.
+__device__ __forceinline__ void store_staged_boxes(const CUtensorMap *tm, uint32_t stg, int x0,
+                                                   int row0, int boxes, int n) {
+    for (int q = 0; q < boxes; ++q)
+        if (x0 + 64 * q < n) tma_store_2d(tm, stg + q * (32 * 64 * 2), x0 + 64 * q, row0);
 }
 
 // Epilogue of a column sub-tile (width 64 or 32), or of a whole tile stored

@@ -45,9 +45,11 @@
 // activation), the down-projection out = Y x W3 that completes the gated
 // MLP. The packed weight tile then holds 256 output columns (one CTA loads
 // 128 of them), the accumulator's 256 columns are those output columns, and
-// the epilogue rounds them to BF16 and stores them straight from registers.
-// Whole tiles and stream-K only (no column sub-tiles); split tiles are summed
-// exactly as above.
+// the epilogue rounds them to BF16 and stores them with TMA: a whole tile in
+// two passes of 128 columns through the Y staging buffer, a split tile's sum
+// (its owner's last unit, when the operand ring is idle) through the last
+// 64 KB of the ring. Whole tiles and stream-K only (no column sub-tiles);
+// split tiles are summed exactly as above.
 //
 // Every wait is bounded. An abort sets the abort flag of every CTA of the
 // cluster; after a cluster barrier each leader drains the loads and MMAs in
@@ -338,7 +340,8 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
             }
             const bool split = c_hi > c_lo;
             bool store_y = !PLAIN;   // a staged Y tile waits for its TMA store
-            // 32 summed columns of each accumulator half, at column c of the half
+            // 32 summed columns of each accumulator half, at column c of the
+            // half (plain product: straight to global memory)
             auto emit32 = [&](int c, const float (&g)[32], const float (&v)[32]) {
                 if constexpr (PLAIN) {
                     store_plain32(row0 + lane, nb * C::UMMA_N + c, g, args);
@@ -360,7 +363,19 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                 if (rows_live) {
                     static_assert(C::BN == 128, "four 32-column chunks");
                     if constexpr (PLAIN) {
-                        epilogue_plain_tile(tbase, row0 + lane, nb * C::UMMA_N, args);
+                        // two passes of 128 output columns through the staging buffer
+                        for (int p = 0; p < 2; ++p) {
+                            if (lane == 0) bulk_wait_group_read0();
+                            __syncwarp();
+                            stage_plain_128(tbase + 128 * p, ybuf, lane);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                store_staged_boxes(&tmY, ybuf, nb * C::UMMA_N + 128 * p, row0, 2,
+                                                   args.N);
+                                bulk_commit_group();
+                            }
+                        }
                     } else {
                         if (lane == 0) bulk_wait_group_read0();
                         __syncwarp();
@@ -382,11 +397,14 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                 // column group width G (Gate and Up columns) whose partials of
                 // every other contributor fit in the operand ring at once
                 const uint32_t col_bytes = static_cast<uint32_t>(args.slot_rows) * 4u;
-                const uint32_t ring_bytes = STAGES * (C::A_BYTES + C::B_BYTES);
+                // (plain product: the ring's last 64 KB stage the owner's output)
+                constexpr uint32_t kPlainStage = PLAIN ? C::EPI_WARPS * 4u * 32u * 64u * 2u : 0u;
+                const uint32_t ring_bytes = STAGES * (C::A_BYTES + C::B_BYTES) - kPlainStage;
                 int G = 128;
                 while (G > 32 && static_cast<uint32_t>(others) * 2u * G * col_bytes > ring_bytes)
                     G >>= 1;
                 const bool staged = static_cast<uint32_t>(others) * 2u * G * col_bytes <= ring_bytes;
+                const uint32_t pstg = sbase + ring_bytes + (warp - 2) * (4u * 32u * 64u * 2u);
                 if (pair != c_lo || !staged) {
                     // a contributor (or an owner with too many partners to
                     // stage): this CTA's FP32 partial -> its workspace slot
@@ -514,7 +532,12 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                                         v[i] += pu[off];
                                     }
                                 }
-                                emit32(c, g, v);
+                                if constexpr (PLAIN) {
+                                    stage_bf16x32(pstg, lane, c, g);
+                                    stage_bf16x32(pstg, lane, C::BN + c, v);
+                                } else {
+                                    emit32(c, g, v);
+                                }
                             }
                         }
                     }
@@ -524,6 +547,16 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                             set_abort_both();
                         }
                         break;
+                    }
+                    if constexpr (PLAIN) {
+                        if (rows_live) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                store_staged_boxes(&tmY, pstg, nb * C::UMMA_N, row0, 4, args.N);
+                                bulk_commit_group();
+                            }
+                        }
                     }
                     tc_fence_before();
                     __syncwarp();

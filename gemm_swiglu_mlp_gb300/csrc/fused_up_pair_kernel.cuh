@@ -352,13 +352,27 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
             };
 
             if (!PLAIN && u.width != C::BN) {
-                if (rows_live)
-                    epilogue_subtile_store(tbase, u.width, row0 + lane, nb * C::BN + u.sub * u.width,
-                                           args);
+                // a 64-column sub-tile is one staged TMA box; a 32-column one
+                // (half a box) is stored from registers
+                if (rows_live) {
+                    if (u.width == 64) {
+                        if (lane == 0) bulk_wait_group_read0();
+                        __syncwarp();
+#pragma unroll 1
+                        for (int c = 0; c < 64; c += 32) {
+                            float g[32], v[32];
+                            tmem_ld_gu(tbase, c, g, v, 64);
+                            stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
+                        }
+                    } else {
+                        epilogue_subtile_store(tbase, u.width, row0 + lane,
+                                               nb * C::BN + u.sub * u.width, args);
+                    }
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(tempty_leader);
-                store_y = false;
+                store_y = u.width == 64;
             } else if (!split) {
                 if (rows_live) {
                     static_assert(C::BN == 128, "four 32-column chunks");
@@ -568,9 +582,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    const int x0 = nb * C::BN;
-                    tma_store_2d(&tmY, ybuf, x0, row0);
-                    if (x0 + 64 < args.N) tma_store_2d(&tmY, ybuf + C::Y_HALF_BYTES, x0 + 64, row0);
+                    const int x0 = nb * C::BN + u.sub * u.width;   // whole tiles: sub = 0
+                    if (x0 < args.N) tma_store_2d(&tmY, ybuf, x0, row0);
+                    if (u.width == C::BN && x0 + 64 < args.N)
+                        tma_store_2d(&tmY, ybuf + C::Y_HALF_BYTES, x0 + 64, row0);
                     bulk_commit_group();
                 }
             }

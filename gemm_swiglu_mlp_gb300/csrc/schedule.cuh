@@ -134,8 +134,11 @@ struct UnitIter {
 //     column sub-tiles (64 or 32 columns: smaller UMMA N, same k loop), which
 //     shortens the last wave without any workspace. A sub-tile still loads a
 //     whole A tile per k-block for a fraction of the MMA work, so where the
-//     MMA feed is the limit (compute-bound shapes) this only pays when SMs
-//     would otherwise idle outright: fewer tiles than half the grid. For
+//     MMA feed is the limit (compute-bound shapes) a sub-tile takes nearly
+//     as long as a whole tile. So on compute-bound shapes the split is taken
+//     when SMs would otherwise idle outright (fewer tiles than half the
+//     grid), or as halves when the halved tail still fits in one wave, where
+//     it cannot lose (1.5B prefill shape: 73.5 against 73.9 us). For
 //     weight-streaming shapes (`weight_bound`: few token rows, the bytes per
 //     unit scale with its width) it is taken whenever it reaches 0.9.
 //   * otherwise, whole tiles whenever they fill at least half the grid;
@@ -200,7 +203,11 @@ inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_co
                 best_eff = e;
             }
         }
-        const bool take = weight_bound ? best_eff >= 0.9 : (best_eff >= 0.85 && 2 * T < G);
+        bool take = weight_bound ? best_eff >= 0.9 : (best_eff >= 0.85 && 2 * T < G);
+        if (!weight_bound && !take && mode == kSchedAuto && full > 0 && 2 * tail <= G) {
+            best = 2;   // the halved tail fits in one wave
+            take = true;
+        }
         if (mode == kSchedColumnSplit && best == 1) best = 2;
         if (best > 1 && (take || mode == kSchedColumnSplit)) {
             s.grid = G;

@@ -53,6 +53,14 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def device_info(dev) -> dict:
+    """Name, SM count and L2 size of the GPU the step ran on."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    return {"name": torch.cuda.get_device_name(dev), "sm_count": props.multi_processor_count,
+            "l2_bytes": getattr(props, "L2_cache_size", None)}
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gemm_swiglu_mlp_gb300", "csrc")
@@ -664,6 +672,7 @@ def run_gb300(args, w):
                 "how": "pinned host A -> device, forward, device Y -> pinned host, every step; "
                        "copy-in, compute and copy-out of consecutive steps overlap on 3 streams"},
         "gpu_launches": K, "clocks": sampler.summary(), "context_l2_warm": l2_warm,
+        "device": device_info(dev),
     }
     if unfused is not None:
         line["context_unfused_torch"] = unfused

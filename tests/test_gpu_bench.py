@@ -34,6 +34,7 @@ def test_bench_prints_one_contract_line(dtype):
         assert key in r["e2e"], key
     for key in ("sm_mhz", "sm_max_mhz", "reasons"):
         assert key in r["clocks"], key
+    assert r["device"]["sm_count"] > 0 and r["device"]["name"]
     assert r["value"] > 0 and r["e2e"]["value"] > 0 and r["gpu_launches"] == 50
     assert r["roofline"]["bound"] == "hbm"          # the 0.5B shape streams weights
     assert r["dtype"] == ("fp8-e4m3" if dtype == "fp8" else "bf16")

@@ -202,3 +202,20 @@ def test_mlp_workload_full_size(sg, orc, label, full):
     Yg, outg = _run_mlp(sg, A, W1, W2, W3)
     rows = np.arange(w.M, dtype=np.int64) if full else _sample_rows(w.M, 4 if w.M > 64 else 8)
     _check_mlp(orc, A, W1, W2, W3, Yg, outg, rows, w.name)
+
+
+@pytest.mark.parametrize("mode", ["auto", "sk", "dp"])
+def test_down_deterministic_bitwise(sg, monkeypatch, mode):
+    """Stream-K partial sums are added in a fixed order: repeated calls give
+    bit-identical results (the 1.5B down-projection shape, and a ragged one)."""
+    if mode != "auto":
+        monkeypatch.setenv("SWIGLU_SCHEDULE", mode)
+    for M, N, K in [(2048, 8960, 1536), (1300, 2056, 2000)]:
+        Yb, W3b = _down_case(M, N, K, 55)
+        Wd = sg.swiglu_pack_down_weights(to_device_bf16(W3b, "cuda"))
+        Yd = to_device_bf16(Yb, "cuda")
+        first = sg.swiglu_down_forward(Yd, Wd, K)
+        for _ in range(3):
+            again = sg.swiglu_down_forward(Yd, Wd, K)
+            assert torch.equal(first.view(torch.int16), again.view(torch.int16)), (mode, M, N, K)
+        sg.swiglu_check_device_status()

@@ -192,11 +192,12 @@ def test_mlp_in_a_cuda_graph(sg, orc):
     _check_mlp(orc, A, W1, W2, W3, Yg, outg, np.arange(M, dtype=np.int64), "graph")
 
 
-@pytest.mark.parametrize("label,full", [("0", True), ("1", False), ("10", False)])
+@pytest.mark.parametrize("label,full", [("0", True), ("1", False), ("6", False), ("10", False)])
 def test_mlp_workload_full_size(sg, orc, label, full):
-    """The whole MLP at the 0.5B (every row), 1.5B prefill and 72B decode
-    shapes (rows sampled from every 128-row block; each sampled row compared
-    in every column)."""
+    """The whole MLP at the 0.5B (every row), 1.5B and 7B prefill and 72B
+    decode shapes (rows sampled from every 128-row block; each sampled row
+    compared in every column). The 7B down-projection (112 output tiles on
+    the CTA pairs) runs whole tiles plus stream-K over the tail."""
     w = workloads.BY_LABEL[label]
     A, W1, W2, W3 = _mlp_inputs(w)
     Yg, outg = _run_mlp(sg, A, W1, W2, W3)

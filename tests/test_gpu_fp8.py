@@ -95,12 +95,12 @@ def test_fp8_every_schedule_form_matches(sg, orc, monkeypatch, variant, mode):
     _check(got, ref, A8, W18, W28, sa, s1, s2, (variant, mode))
 
 
-@pytest.mark.parametrize("label", ["1", "1s", "3", "8", "10"])
+@pytest.mark.parametrize("label", ["1", "1s", "3", "6", "8", "10"])
 def test_fp8_workload_full_size(sg, orc, label):
     """Full-size FP8 runs of the 1.5B prefill (also with the x8 stress input,
-    pre-activations that saturate SiLU), 7B decode, 32B decode (1% outlier
-    channels, which set the per-tensor scale) and 72B decode shapes, every
-    output element compared."""
+    pre-activations that saturate SiLU), 7B decode and prefill (M=2048),
+    32B decode (1% outlier channels, which set the per-tensor scale) and 72B
+    decode shapes, every output element compared."""
     w = workloads.BY_LABEL[label]
     A8, W18, W28, sa, s1, s2 = workloads.make_inputs_fp8(w)
     got = _run(sg, A8, W18, W28, sa, s1, s2)

@@ -210,3 +210,39 @@ def test_down_sizes_and_host_validation(lib):
         W, N, K, Wp = bad
         assert lib.swiglu_pack_down_weights(W, N, K, Wp, None) == 1, bad
         assert lib.swiglu_pack_down_weights_nk(W, K, N, Wp, None) == 1, bad
+
+
+def test_binding_rejects_host_tensors_for_the_mlp_calls(lib):
+    """The Python binding checks dtype, device and shape before any launch:
+    CPU tensors or wrong shapes raise instead of reaching the C ABI."""
+    import torch
+    import gemm_swiglu_mlp_gb300 as sg
+    Y = torch.zeros(4, 8, dtype=torch.bfloat16)
+    W = torch.zeros(8, 8, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        sg.swiglu_pack_down_weights(W)
+    with pytest.raises(TypeError):
+        sg.swiglu_pack_down_weights_nk(W)
+    with pytest.raises(TypeError):
+        sg.swiglu_down_forward(Y, torch.zeros(16, dtype=torch.uint8), 8)
+    with pytest.raises(TypeError):
+        sg.swiglu_mlp_forward(Y, torch.zeros(16, dtype=torch.uint8),
+                              torch.zeros(16, dtype=torch.uint8), 8)
+    with pytest.raises(TypeError):
+        sg.swiglu_down_forward(torch.zeros(4, 8, dtype=torch.float32),
+                               torch.zeros(16, dtype=torch.uint8), 8)
+
+
+def test_pack_down_reference_layout_by_hand():
+    # N=2 (reduction), K=3 (outputs): one tile [256][64]; packed row r < 3
+    # holds W3[:, r] in its first 2 entries; everything else is zero padding
+    from tests.parity import pack_down_reference
+    W3 = np.arange(6, dtype=np.uint16).reshape(2, 3)
+    P = pack_down_reference(W3).reshape(1, 1, 256, 64)
+    assert P.shape == (1, 1, 256, 64)
+    for r in range(3):
+        assert list(P[0, 0, r, :2]) == [W3[0, r], W3[1, r]]
+        assert not P[0, 0, r, 2:].any()
+    assert not P[0, 0, 3:].any()
+    import gemm_swiglu_mlp_gb300 as sg
+    assert sg.swiglu_down_packed_weight_bytes(2, 3) == P.size * 2

@@ -93,3 +93,52 @@ def test_wait_timeout_is_reported_and_context_survives(fi_lib, monkeypatch, vari
     assert status == 0 and raw == 0
     r = compare(from_device_bf16(Y), oracle.swiglu_up(A, W1, W2)["Y"])
     assert r["mismatches"] == 0 and r["over_bound"] == 0, r
+
+
+@pytest.mark.parametrize("mode,M,N,K", [("auto", 512, 2048, 512), ("dp", 512, 512, 512)])
+def test_down_projection_wait_timeout(fi_lib, monkeypatch, mode, M, N, K):
+    """The same for the down-projection (the CTA-pair kernel's plain mode),
+    with stream-K split tiles (auto: 4 output tiles on all pairs) and with
+    whole tiles: the timeout is reported and the next call is correct."""
+    if mode != "auto":
+        monkeypatch.setenv("SWIGLU_SCHEDULE", mode)
+    import oracle
+    lib = fi_lib
+    vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    lib.swiglu_pack_down_weights.argtypes = [vp, i64, i64, vp, vp]
+    lib.swiglu_down_packed_weight_bytes.argtypes = [i64, i64]
+    lib.swiglu_down_packed_weight_bytes.restype = sz
+    lib.swiglu_down_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.swiglu_down_workspace_bytes.restype = sz
+    lib.swiglu_down_forward.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+    rng = np.random.Generator(np.random.PCG64(78))
+    Yb = workloads.f32_to_bf16_bits(rng.standard_normal(size=(M, N), dtype=np.float32))
+    W3 = workloads.f32_to_bf16_bits(
+        rng.standard_normal(size=(N, K), dtype=np.float32) * np.float32(N ** -0.5))
+    Yd, W3d = to_device_bf16(Yb, "cuda"), to_device_bf16(W3, "cuda")
+    W3p = torch.empty(lib.swiglu_down_packed_weight_bytes(N, K), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert lib.swiglu_pack_down_weights(W3d.data_ptr(), N, K, W3p.data_ptr(), stream) == 0
+    ws_bytes = lib.swiglu_down_workspace_bytes(M, N, K)
+    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+
+    def run():
+        out = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+        assert lib.swiglu_down_forward(Yd.data_ptr(), W3p.data_ptr(), out.data_ptr(), M, N, K,
+                                       ws.data_ptr() if ws_bytes else None, ws_bytes,
+                                       stream) == 0
+        raw = ctypes.c_uint32(0)
+        return out, lib.swiglu_check_device_status(stream, ctypes.byref(raw)), raw.value
+
+    lib.swiglu_test_set_fault_injection(1)
+    try:
+        _, status, raw = run()
+    finally:
+        lib.swiglu_test_set_fault_injection(0)
+    assert status == TIMEOUT_STATUS and raw & (MMA_TIMEOUT_BIT | PRODUCER_TIMEOUT_BIT), raw
+    # an aborted launch may leave partial counts behind: zero the workspace again
+    ws.zero_()
+    out, status, raw = run()
+    assert status == 0 and raw == 0
+    r = compare(from_device_bf16(out), oracle.matmul(Yb, W3)["C"])
+    assert r["mismatches"] == 0 and r["over_bound"] == 0, r

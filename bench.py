@@ -702,9 +702,8 @@ def main(argv=None):
                    help="timed region: replay CUDA graphs of the calls (default) or call K times")
     p.add_argument("--dtype", choices=("bf16", "fp8"), default="bf16",
                    help="input type: bf16, or fp8 (E4M3 with per-tensor scales)")
-    p.add_argument("--variant", choices=("auto", "1sm", "2sm", "4sm"), default="auto",
-                   help="fused kernel: auto (2-SM pairs for M >= 256), or force one (ablation; "
-                        "4sm = clusters of two pairs sharing weight tiles)")
+    p.add_argument("--variant", choices=("auto", "1sm", "2sm"), default="auto",
+                   help="fused kernel: auto (2-SM pairs for M >= 256), or force one (ablation)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

@@ -467,12 +467,14 @@ def swiglu_up_forward_fp8(A: torch.Tensor, Wpacked: torch.Tensor, N: int, scale_
     packed FP8 weights standing for scale_w1*W1_8 and scale_w2*W2_8."""
     lib = load_library()
     _require_u8_cuda(A, "A")
+    if A.dim() != 2:
+        raise ValueError("A must be [M, K]")
     M, K = A.shape
     N = int(N)
-    if Y is None:
-        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    else:
-        _require_bf16_cuda(Y, "Y")
+    need = swiglu_packed_weight_bytes_fp8(N, K)
+    if not Wpacked.is_cuda or Wpacked.numel() * Wpacked.element_size() < need:
+        raise ValueError("Wpacked must be a CUDA buffer of at least %d bytes" % need)
+    Y = _out_tensor(Y, (M, N), A.device, "Y")
     with torch.cuda.device(A.device):
         ws_need = swiglu_workspace_bytes_fp8(M, N, K)
         ws_ptr, ws_bytes = None, 0

@@ -32,15 +32,6 @@
 // it, and they finish their parts of the tile first (their range starts in
 // it).
 //
-// PAIRS = 2 (clusters of four CTAs, two pairs): the two pairs work on the
-// tiles of two vertically adjacent 256-row blocks with the same output
-// columns, so they need the same weight tile. Each CTA then loads half of
-// its half of the weight tile (64 rows) and multicasts it to the CTA that
-// holds the same half in the other pair: every CTA still receives 32 KB
-// per k-block, but reads only 24 KB of it from L2 (A 16 KB, weights 8 KB).
-// Both pairs' MMA commits free a stage in all four CTAs (a multicast load
-// may refill it only when both pairs are done with it). Whole tiles only.
-//
 // PLAIN = true: the same kernel computes a plain product out = A x W (no
 // activation), the down-projection out = Y x W3 that completes the gated
 // MLP. The packed weight tile then holds 256 output columns (one CTA loads
@@ -90,7 +81,7 @@ struct PairCfg {
     static_assert(UMMA_N == kSlotCols, "workspace slot shape");
 };
 
-template <int STAGES, typename E, int PAIRS, bool PLAIN = false>
+template <int STAGES, typename E, bool PLAIN = false>
 __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     fused_up_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
@@ -98,8 +89,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                          const __grid_constant__ CUtensorMap tmB32,
                          const __grid_constant__ CUtensorMap tmY, const FusedArgs args) {
     using C = PairCfg<STAGES>;
-    static_assert(PAIRS == 1 || PAIRS == 2, "one pair, or two pairs sharing weight tiles");
-    static_assert(!PLAIN || (PAIRS == 1 && !E::kFp8), "plain product: BF16 CTA pairs");
+    static_assert(!PLAIN || !E::kFp8, "plain product: BF16 CTA pairs");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -107,14 +97,11 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();      // 0 .. 2 * PAIRS - 1
+    const uint32_t rank = cluster_ctarank();      // 0 or 1
     const uint32_t half = rank & 1u;               // 0: leader (Gate rows), 1: Up rows
-    const int pic = static_cast<int>(rank >> 1);   // which pair of the cluster
-    const uint32_t leader_rank = rank & ~1u;
+    constexpr uint32_t leader_rank = 0;
     const bool is_leader = half == 0;
-    const int pair = blockIdx.x / (2 * PAIRS);     // schedule worker: one cluster
-    // a CTA's multicast partner: the CTA holding the same half in the other pair
-    const uint16_t wmask = static_cast<uint16_t>((1u << half) | (1u << (half + 2)));
+    const int pair = blockIdx.x / 2;               // schedule worker: one cluster
 
     auto full_bar = [&](int s) { return sbase + C::OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sbase + C::OFF_BAR + 8u * (STAGES + s); };
@@ -125,17 +112,16 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     volatile int *last_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);
-    // the same flag in every other CTA of the cluster
+    // the same flag in the other CTA of the pair
     auto set_abort_both = [&]() {
         *abort_flag = 1;
-        for (uint32_t r = 0; r < 2u * PAIRS; ++r)
-            if (r != rank) st_cluster_u32(mapa_shared(sbase + C::OFF_MISC + 4, r), 1u);
+        st_cluster_u32(mapa_shared(sbase + C::OFF_MISC + 4, rank ^ 1u), 1u);
     };
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), PAIRS);   // one commit from each pair's MMA
+            mbar_init(empty_bar(s), 1);       // one commit from the pair's MMA
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
@@ -174,17 +160,12 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
         if (it.next(u)) {
             int tm, nb;
             sched.order.coords(u.tile, tm, nb);
-            const int pm = tm * PAIRS + pic;
             const CUtensorMap *tmBu = (u.width == C::BN) ? &tmB : (u.width == 64 ? &tmB64 : &tmB32);
             const int kend = (u.kb1 - u.kb0 < kPrefetchStages) ? u.kb1 : u.kb0 + kPrefetchStages;
             for (int kb = u.kb0; kb < kend; ++kb) {
-                tma_prefetch_2d(&tmA, kb * E::kBK, pm * C::UMMA_M + C::BM * static_cast<int>(half));
-                if (PAIRS == 2)
-                    tma_prefetch_3d(&tmB64, 0, C::BN * static_cast<int>(half) + 64 * pic,
-                                    nb * sched.k_blocks + kb);
-                else
-                    tma_prefetch_3d(tmBu, 0, C::BN * static_cast<int>(half) + u.sub * u.width,
-                                    nb * sched.k_blocks + kb);
+                tma_prefetch_2d(&tmA, kb * E::kBK, tm * C::UMMA_M + C::BM * static_cast<int>(half));
+                tma_prefetch_3d(tmBu, 0, C::BN * static_cast<int>(half) + u.sub * u.width,
+                                nb * sched.k_blocks + kb);
             }
         }
     }
@@ -203,7 +184,6 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
             while (ok && it.next(u)) {
                 int tm, nb;
                 sched.order.coords(u.tile, tm, nb);
-                const int pm = tm * PAIRS + pic;
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                         ok = false;
@@ -228,21 +208,12 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                         mbar_arrive_expect_tx(full_bar(stage), 2 * (C::A_BYTES + brows * kRowBytes));
                     const uint32_t bar = mapa_shared(full_bar(stage), leader_rank);
                     tma_load_2d_pair(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, bar, kb * E::kBK,
-                                     pm * C::UMMA_M + C::BM * static_cast<int>(half));
-                    if (PAIRS == 2) {
-                        // rows [64 * pic, 64 * pic + 64) of this CTA's half, to
-                        // both pairs (whole tiles only: brows == C::BN)
-                        tma_load_3d_pair_mc(
-                            sbase + C::OFF_B + stage * C::B_BYTES + 64 * pic * kRowBytes, &tmB64, bar,
-                            0, C::BN * static_cast<int>(half) + 64 * pic, nb * sched.k_blocks + kb,
-                            wmask);
-                    } else {
-                        const CUtensorMap *tmBu =
-                            (brows == C::BN) ? &tmB : (brows == 64 ? &tmB64 : &tmB32);
-                        tma_load_3d_pair(sbase + C::OFF_B + stage * C::B_BYTES, tmBu, bar, 0,
-                                         C::BN * static_cast<int>(half) + u.sub * brows,
-                                         nb * sched.k_blocks + kb);
-                    }
+                                     tm * C::UMMA_M + C::BM * static_cast<int>(half));
+                    const CUtensorMap *tmBu =
+                        (brows == C::BN) ? &tmB : (brows == 64 ? &tmB64 : &tmB32);
+                    tma_load_3d_pair(sbase + C::OFF_B + stage * C::B_BYTES, tmBu, bar, 0,
+                                     C::BN * static_cast<int>(half) + u.sub * brows,
+                                     nb * sched.k_blocks + kb);
                     issued_mask |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -288,16 +259,15 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                     for (int k = 0; k < kKSteps; ++k)
                         E::mma_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc_u,
                                     (kb != u.kb0 || k != 0) ? 1u : 0u);
-                    // frees the stage in both CTAs of this pair, and with two
-                    // pairs also in the other pair (its multicast loads refill it)
-                    umma_commit_pair_mc(empty_bar(stage), PAIRS == 2 ? 0xF : 0x3);
+                    // frees the stage in both CTAs of the pair
+                    umma_commit_pair_mc(empty_bar(stage), 0x3);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair_mc(tfull_bar(acc), static_cast<uint16_t>(0x3u << (2 * pic)));
+                umma_commit_pair_mc(tfull_bar(acc), 0x3);
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -322,11 +292,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
         while (it.next(u)) {
             int tm, nb;
             sched.order.coords(u.tile, tm, nb);
-            const int pm = tm * PAIRS + pic;
             ok = epilogue_all(mbar_wait(tfull_bar(acc), acc_phase, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const int row0 = pm * C::UMMA_M + C::BM * static_cast<int>(half) + 32 * quad;
+            const int row0 = tm * C::UMMA_M + C::BM * static_cast<int>(half) + 32 * quad;
             const bool rows_live = row0 < args.M;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) +
                                    static_cast<uint32_t>(acc * C::UMMA_N);

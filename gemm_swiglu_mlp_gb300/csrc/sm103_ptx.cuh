@@ -189,20 +189,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// 2-SM multicast: the box lands at the same shared-memory offset in every
-// CTA of `cta_mask`, and each destination's completion is signalled on the
-// barrier at `bar`'s offset in the even (leader) CTA of that destination's
-// pair; `bar` is given as the issuing pair's leader barrier.
-__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap *m, uint32_t bar,
-                                                    int32_t x, int32_t y, int32_t z,
-                                                    uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(cta_mask)
-        : "memory");
-}
-
 // 1-D bulk copy global -> this CTA's shared memory (both addresses 16-byte
 // aligned, size a multiple of 16), completion signalled on `bar` as
 // transaction bytes.

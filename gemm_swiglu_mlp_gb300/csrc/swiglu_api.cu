@@ -29,10 +29,6 @@ constexpr int kAssumedMaxSms = 256;  // workspace sizing when no device answers
 constexpr int kPairStages = 6;
 constexpr int kDownTileCols = 256;   // output columns of a plain-product (down) tile
 constexpr int64_t kPairMinM = 256;   // from this many tokens on, the 2-SM kernel
-constexpr int64_t kQuadRows = 512;   // rows of a tile of two CTA pairs sharing weight tiles
-// Whether the automatic choice may take clusters of two pairs (multicast
-// weight tiles); SWIGLU_FUSED_VARIANT=4sm always can.
-constexpr bool kQuadAuto = false;
 using FusedC = FusedCfg<kFusedStages>;
 using Narrow64C = FusedCfg<kNarrow64Stages, 128>;
 using Narrow32C = FusedCfg<kNarrow32Stages, 64>;
@@ -42,15 +38,14 @@ using PairC = PairCfg<kPairStages>;
 int g_test_skip_first_fill = 0;  // set by swiglu_test_set_fault_injection
 #endif
 
-// SWIGLU_FUSED_VARIANT=1sm|2sm|4sm forces the 1-SM kernel, the CTA-pair
-// kernel, or clusters of two pairs that share weight tiles (for ablations
-// and tests); it is read on every call. 0: the automatic choice.
+// SWIGLU_FUSED_VARIANT=1sm|2sm forces the 1-SM kernel or the CTA-pair
+// kernel (for ablations and tests); it is read on every call. 0: the
+// automatic choice.
 int variant_override() {
     const char *v = std::getenv("SWIGLU_FUSED_VARIANT");
     if (!v) return 0;
     if (std::strcmp(v, "1sm") == 0) return 1;
     if (std::strcmp(v, "2sm") == 0) return 2;
-    if (std::strcmp(v, "4sm") == 0) return 4;
     return 0;
 }
 
@@ -59,7 +54,6 @@ struct DeviceState {
     int status = SWIGLU_OK;  // result of the one-time setup
     int sm_count = 0;
     int pair_clusters = 0;   // CTA pairs of the 2-SM kernel that can run at once
-    int quad_clusters = 0;   // clusters of two pairs that can run at once
 };
 
 DeviceState g_devices[kMaxDevices];
@@ -121,30 +115,24 @@ int device_setup(int *dev_out, DeviceState **st_out) {
             cudaFuncSetAttribute(fused_up_kernel<kNarrow32Stages, 64, ElemE4M3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Narrow32C::SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16, 1>,
+            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairC::SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16, 2>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 PairC::SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16, 1, true>,
+            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairC::SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(fused_up_kernel<kFusedStages, 256, ElemE4M3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  FusedC::SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemE4M3, 1>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 PairC::SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemE4M3, 2>,
+            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemE4M3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairC::SMEM_BYTES) != cudaSuccess) {
             cudaGetLastError();
             st.status = SWIGLU_ERR_CUDA;
             return;
         }
-        // how many clusters of 2 and of 4 CTAs fit at once (a cluster sits
-        // inside one GPC, so not every SM count divides evenly)
+        // how many CTA pairs fit at once (a cluster sits inside one GPC, so
+        // not every SM count divides evenly)
         auto max_clusters = [sms](int ctas, auto kernel) {
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute attr[1];
@@ -164,10 +152,8 @@ int device_setup(int *dev_out, DeviceState **st_out) {
             }
             return std::min(clusters, sms / ctas);
         };
-        const int pairs = max_clusters(2, fused_up_pair_kernel<kPairStages, ElemBF16, 1>);
+        const int pairs = max_clusters(2, fused_up_pair_kernel<kPairStages, ElemBF16>);
         st.pair_clusters = pairs >= 1 ? pairs : sms / 2;
-        const int quads = max_clusters(4, fused_up_pair_kernel<kPairStages, ElemBF16, 2>);
-        st.quad_clusters = quads >= 1 ? quads : 0;   // 0: never use two-pair clusters
         st.sm_count = sms;
         st.status = SWIGLU_OK;
     });
@@ -203,8 +189,8 @@ int schedule_mode() {
     return kSchedAuto;
 }
 
-// Schedule for a kernel whose clusters hold `ctas` CTAs (1, 2 or 4: tiles of
-// 128, 256 or 512 rows), `workers` of them running at once.
+// Schedule for a kernel whose clusters hold `ctas` CTAs (1 or 2: tiles of
+// 128 or 256 rows), `workers` of them running at once.
 WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, int ctas, int kbk, int mode) {
     const int rows = FusedC::BM * ctas;
     const int m_tiles = static_cast<int>((M + rows - 1) / rows);
@@ -244,25 +230,15 @@ WorkSched plan_down(int64_t M, int64_t N, int64_t K, int workers) {
 }
 
 // Which kernel serves a call, and its schedule: the 1-SM kernel below 256
-// rows, the CTA-pair kernel from there on. Clusters of two pairs (weight
-// tiles multicast to both) run whole tiles only; they are taken when forced,
-// or (if enabled) for multiples of 512 rows whose plan is whole tiles.
+// rows, the CTA-pair kernel from there on.
 struct LaunchPlan {
-    int ctas;        // CTAs per cluster: 1, 2 or 4
+    int ctas;        // CTAs per cluster: 1 or 2
     WorkSched sched;
 };
-LaunchPlan choose_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters,
-                       int quad_clusters, int kbk) {
+LaunchPlan choose_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters, int kbk) {
     const int v = variant_override();
     const int mode = schedule_mode();
     if (v == 1 || (v == 0 && M < kPairMinM)) return {1, plan_for(M, N, K, sms, 1, kbk, mode)};
-    if (v == 4 && quad_clusters > 0)
-        return {4, plan_for(M, N, K, quad_clusters, 4, kbk, kSchedDataParallel)};
-    if (v == 0 && kQuadAuto && quad_clusters > 0 && M % kQuadRows == 0 &&
-        (mode == kSchedAuto || mode == kSchedDataParallel)) {
-        const LaunchPlan q{4, plan_for(M, N, K, quad_clusters, 4, kbk, mode)};
-        if (q.sched.sk_iters == 0 && q.sched.n_split == 1) return q;
-    }
     return {2, plan_for(M, N, K, pair_clusters, 2, kbk, mode)};
 }
 
@@ -450,12 +426,11 @@ size_t workspace_bytes_impl(int64_t M, int64_t N, int64_t K) {
     int dev;
     DeviceState *st;
     if (device_setup(&dev, &st) == SWIGLU_OK) {  // the same plan the forward will use
-        const LaunchPlan lp = choose_plan(M, N, K, st->sm_count, st->pair_clusters,
-                                          st->quad_clusters, E::kBK);
+        const LaunchPlan lp = choose_plan(M, N, K, st->sm_count, st->pair_clusters, E::kBK);
         return workspace_bytes_for(lp.sched, M, lp.ctas == 2, st->sm_count);
     }
     const int sms = current_sm_count();         // no usable device: a size for its SM count
-    const LaunchPlan lp = choose_plan(M, N, K, sms, sms / 2, 0, E::kBK);
+    const LaunchPlan lp = choose_plan(M, N, K, sms, sms / 2, E::kBK);
     return workspace_bytes_for(lp.sched, M, lp.ctas == 2, sms);
 }
 
@@ -485,11 +460,10 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
     const int s = device_setup(&dev, &st);
     if (s != SWIGLU_OK) return s;
 
-    const LaunchPlan lp =
-        choose_plan(M, N, K, st->sm_count, st->pair_clusters, st->quad_clusters, E::kBK);
+    const LaunchPlan lp = choose_plan(M, N, K, st->sm_count, st->pair_clusters, E::kBK);
     const WorkSched &sched = lp.sched;
-    const bool pair = lp.ctas >= 2;
-    const size_t ws_need = workspace_bytes_for(sched, M, lp.ctas == 2, st->sm_count);
+    const bool pair = lp.ctas == 2;
+    const size_t ws_need = workspace_bytes_for(sched, M, pair, st->sm_count);
     if (ws_need > 0) {
         if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
             workspace_bytes < ws_need)
@@ -556,12 +530,8 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
         cfg.gridDim = dim3(static_cast<unsigned>(lp.ctas * sched.grid));
         cfg.blockDim = dim3(PairC::THREADS);
         cfg.dynamicSmemBytes = PairC::SMEM_BYTES;
-        if (lp.ctas == 4)
-            err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages, E, 2>, tmA, tmB,
-                                     tmB64, tmB32, tmY, args);
-        else
-            err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages, E, 1>, tmA, tmB,
-                                     tmB64, tmB32, tmY, args);
+        err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages, E>, tmA, tmB, tmB64,
+                                 tmB32, tmY, args);
     } else {
         cfg.numAttrs = 1;
         cfg.gridDim = dim3(static_cast<unsigned>(sched.grid));
@@ -752,7 +722,7 @@ int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M,
     cfg.blockDim = dim3(PairC::THREADS);
     cfg.dynamicSmemBytes = PairC::SMEM_BYTES;
     const cudaError_t err =
-        cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages, ElemBF16, 1, true>, tmA, tmB,
+        cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages, ElemBF16, true>, tmA, tmB,
                            tmB, tmB, tmOut, args);
     if (err != cudaSuccess) {
         cudaGetLastError();

@@ -113,14 +113,25 @@ size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *            SWIGLU_ERR_DEVICE_TIMEOUT, zero it again. Calls that run at the
  *            same time on the GPU (different streams) need separate
  *            workspaces.
+ *            Why a workspace at all: the operation itself (the paper's
+ *            problem statement) needs only A, the weights and Y. The
+ *            workspace serves this library's K split for problems of a
+ *            handful of output tiles, whose FP32 partial sums are combined
+ *            through global memory before the activation (SiLU is not
+ *            linear). Combining them inside a thread-block cluster through
+ *            distributed shared memory instead needs no workspace, but was
+ *            measured slower on GB300 (0.5B-shaped problem: 9.0 against
+ *            8.2 us), so the interface keeps a caller-owned workspace, and
+ *            swiglu_up_forward_noalloc below serves callers that cannot
+ *            provide one.
  * Requirements: M >= 1, N >= 8, K >= 8, N % 8 == 0, K % 8 == 0 (16-byte row
  * strides), M, N, K < 2^31; A, Wpacked, Y 16-byte aligned; Y must not overlap
  * A, Wpacked or the workspace. M, N and K need not be multiples of any tile
  * size. The schedule (tile shape, CTA count) is chosen from M, N, K and the
  * device's SM count; the result is bit-identical from run to run. Two
  * environment variables, read on every call, force a choice for ablations:
- * SWIGLU_FUSED_VARIANT=1sm|2sm|4sm (1-SM kernel, CTA pairs, or clusters of
- * two pairs sharing weight tiles) and SWIGLU_SCHEDULE=dp|split|sk|sk-tail
+ * SWIGLU_FUSED_VARIANT=1sm|2sm (1-SM kernel or CTA pairs) and
+ * SWIGLU_SCHEDULE=dp|split|sk|sk-tail
  * (whole tiles, column sub-tiles in the last wave, split K over the last wave
  * and the remainder, or over the remainder only); swiglu_workspace_bytes
  * follows them too.
@@ -294,6 +305,9 @@ int swiglu_mlp_forward(const void *A, const void *Wpacked, const void *W3packed,
  * that gives up sets a bit in the word, releases its tensor memory and
  * exits instead of hanging. Returns SWIGLU_OK, SWIGLU_ERR_DEVICE_TIMEOUT
  * (and writes the raw word to *raw_word if non-NULL), or SWIGLU_ERR_CUDA.
+ * raw_word (optional, may be NULL) is a diagnostic output beyond the status:
+ * which role's wait ran out (bit 0 producer, 1 MMA issuer, 2 epilogue,
+ * 3 the drain after an abort).
  */
 int swiglu_check_device_status(void *stream, uint32_t *raw_word);
 

@@ -62,8 +62,7 @@ def _run(lib, A, Wp, M, N, K, stream):
     return Y, status, raw.value
 
 
-@pytest.mark.parametrize("variant,M,N,K", [("1sm", 128, 256, 512), ("2sm", 512, 256, 512),
-                                           ("4sm", 1024, 256, 512)])
+@pytest.mark.parametrize("variant,M,N,K", [("1sm", 128, 256, 512), ("2sm", 512, 256, 512)])
 def test_wait_timeout_is_reported_and_context_survives(fi_lib, monkeypatch, variant, M, N, K):
     monkeypatch.setenv("SWIGLU_FUSED_VARIANT", variant)
     import oracle
@@ -84,8 +83,7 @@ def test_wait_timeout_is_reported_and_context_survives(fi_lib, monkeypatch, vari
     assert status == TIMEOUT_STATUS
     # The MMA waits for the stage that is never filled; the producers then
     # wait for stages that its MMAs never free. Whichever bounded wait runs
-    # out first reports (with two pairs sharing loads the producers of the
-    # other pair start waiting within microseconds of the MMA).
+    # out first reports.
     assert raw & (MMA_TIMEOUT_BIT | PRODUCER_TIMEOUT_BIT)
 
     # 2) the word was cleared by the read, and the context still works

@@ -32,14 +32,27 @@ def sg():
     return mod
 
 
-# Shapes that split K across CTAs (so the scratch is used) and shapes that
-# run whole tiles (no scratch), on both the 1-SM and the 2-SM kernel.
-CASES = [(33, 264, 2000), (128, 4864, 896), (70, 520, 1000), (1, 136, 4096),
-         (300, 392, 200), (2048, 392, 520)]
+# (M, N, K, forced schedule or None). The first group splits K across CTAs
+# (stream-K), so the calls go through the shared scratch array: three by the
+# library's own choice on a 152-SM part, and two forced to stream-K (one per
+# kernel) so that the scratch path is run whatever the automatic choice
+# becomes. The last group runs whole tiles or column sub-tiles and needs no
+# scratch.
+SCRATCH_CASES = [(33, 264, 2000, None), (70, 520, 1000, None), (2048, 392, 520, None),
+                 (300, 392, 1000, "sk"), (128, 4864, 896, "sk")]
+PLAIN_CASES = [(128, 4864, 896, None), (512, 4864, 256, None), (1300, 2000, 256, None),
+               (200, 9728, 256, None)]
 
 
-@pytest.mark.parametrize("M,N,K", CASES)
-def test_noalloc_matches_forward_on_two_calls(sg, M, N, K):
+@pytest.mark.parametrize("M,N,K,mode,uses_scratch",
+                         [c + (True,) for c in SCRATCH_CASES] + [c + (False,) for c in PLAIN_CASES])
+def test_noalloc_matches_forward_on_two_calls(sg, monkeypatch, M, N, K, mode, uses_scratch):
+    """Two calls in a row give exactly the bytes of swiglu_up_forward on the
+    same inputs (the second call finds the first call's partial sums still
+    in the scratch array), and are within the oracle tolerance of it."""
+    if mode is not None:
+        monkeypatch.setenv("SWIGLU_SCHEDULE", mode)
+    assert (sg.swiglu_workspace_bytes(M, N, K) > 0) == uses_scratch
     lib = sg.load_library()
     A, W1, W2 = workloads.random_case(M, N, K, seed=4000 + M + N + K)
     Ad = to_device_bf16(A, "cuda")
@@ -52,9 +65,12 @@ def test_noalloc_matches_forward_on_two_calls(sg, M, N, K):
                                            M, N, K, stream)
         assert st == 0, sg.swiglu_status_string(st)
         assert sg.swiglu_check_device_status() == 0
-        r = compare(from_device_bf16(Y), ref)
+        got = from_device_bf16(Y)
+        r = compare(got, ref)
         assert r["nonfinite"] == 0, (call, r)
         assert r["mismatches"] == 0 and r["over_bound"] == 0, (call, r)
+        # same kernel, same schedule, same k order of the partial sums
+        assert np.array_equal(got, ref), (call, int(np.count_nonzero(got != ref)))
 
 
 def test_noalloc_rejects_problems_over_its_scratch(sg):

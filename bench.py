@@ -2,22 +2,39 @@
 """Benchmark of the fused SwiGLU up-projection Y = SiLU(A x W1) (.) (A x W2).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--workload LABEL] [--dtype bf16|fp8]
+                    [--workload LABEL] [--dtype bf16|fp8] [--split replicas|columns]
 
 One step = one call of swiglu_up_forward (the whole fused path: both GEMMs,
 the activation and the BF16 store) over one batch of M tokens. Default
-workload: the Qwen-2.5-1.5B-shaped up-projection, M=2048, K=1536, N=8960.
-Inputs are seeded synthetic data (workloads/), generated once and resident in
-HBM before the timed region. `--dtype fp8` runs swiglu_up_forward_fp8 on the
-E4M3 quantization of the same draws (per-tensor scales, BF16 Y); its tensor
-roofline is the measured BF16 peak times the nominal FP8/BF16 ratio of 2.
-Consecutive steps rotate over several copies of
-A, the packed weights and Y whose total exceeds twice the L2 size, so no step
-finds its operands in L2.
+workload: the largest single-GPU configuration, the Qwen-2.5-72B-shaped
+up-projection with M=8192 tokens (K=8192, N=29568). Its inputs are the
+seeded synthetic data of workloads/ (numpy PCG64), generated once and
+resident in HBM before the timed region. Consecutive steps rotate over
+several copies of A, the packed weights and Y whose total exceeds twice the
+L2 size, so no step finds its operands in L2. `--dtype fp8` runs
+swiglu_up_forward_fp8 on the E4M3 quantization of the same draws
+(per-tensor scales, BF16 Y); its tensor roofline is the measured BF16 peak
+times the nominal FP8/BF16 ratio of 2.
 
-Prints one JSON line (rank 0). Under torchrun each rank runs the same
-workload on its own GPU (independent replicas, no collective on the data
-path); `value` is the FLOP total of all ranks over the slowest rank's time.
+Besides the headline it measures, in the same process:
+  * `sweep`: every workload of workloads.WORKLOADS (the metric is "vs M"),
+    each timed over a window of graph-replayed launches with the clocks of
+    that window; inputs drawn on the GPU from torch's seeded generator with
+    the workloads' distributions;
+  * `context_sustained`: the headline launch replayed for >= 1 s, against
+    the sustained BF16 peak, with the clocks of that window;
+  * `e2e`: the same metric through the public call with a pinned-host copy
+    of A in and of Y out inside every step;
+  * context only: L2-warm launches, the unfused cuBLAS path, the whole gated
+    MLP, and the CPU oracle on a bounded row sample (`cpu_baseline`).
+
+Prints one JSON line (rank 0). `--gpus N` with N > 1 starts N ranks itself
+(torch.distributed.run on this node) unless it already runs under torchrun.
+`--split replicas` (default): every rank runs the whole workload on its own
+GPU (weak scaling); `--split columns`: rank r packs its slice of W1 and W2's
+columns and writes Y[:, slice] (column-parallel, strong scaling). Neither
+needs a collective on the data path; `value` is the FLOPs of all ranks over
+the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -25,6 +42,7 @@ import argparse
 import hashlib
 import json
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -37,9 +55,10 @@ if ROOT not in sys.path:
 
 METRIC = "fused SwiGLU up-proj TFLOP/s and % of GB300 BF16/HBM roofline vs M"
 UNIT = "TFLOP/s"
-DEFAULT_WORKLOAD = "1"
+DEFAULT_WORKLOAD = "11"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 REFERENCE_BUDGET_S = 120.0
+TILE_COLS = 128          # output columns of one tile: the column-split granule
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -101,8 +120,8 @@ def algorithmic_bytes(w, dtype: str) -> int:
     return w.roofline_bytes
 
 
-def roofline_us(w, peaks, dtype: str = "bf16"):
-    return max(w.flops / (tensor_peak(peaks, dtype) * 1e12),
+def roofline_us(w, peaks, dtype: str = "bf16", key: str = "bf16_tflops"):
+    return max(w.flops / (tensor_peak(peaks, dtype, key) * 1e12),
                algorithmic_bytes(w, dtype) / (peaks["hbm_gbs"] * 1e9)) * 1e6
 
 
@@ -112,17 +131,36 @@ def bound_of(w, peaks, dtype: str = "bf16") -> str:
     return "tensor" if t_tc >= t_hbm else "hbm"
 
 
+def roofline_entry(w, peaks, dtype: str, launch_s: float) -> dict:
+    """The roofline numbers of one launch duration: the binding resource, the
+    achieved rate against its measured peak (burst peak for a tensor-bound
+    launch, also against the sustained one), and the fraction of roofline
+    time (the slower of the tensor and HBM bounds)."""
+    bound = bound_of(w, peaks, dtype)
+    tflops = w.flops / launch_s / 1e12
+    gbs = algorithmic_bytes(w, dtype) / launch_s / 1e9
+    e = {"us_per_launch": launch_s * 1e6, "tflops": tflops, "bound": bound,
+         "achieved_gbs": gbs, "frac_of_roofline_time": roofline_us(w, peaks, dtype) * 1e-6 / launch_s}
+    if bound == "tensor":
+        e["frac"] = tflops / tensor_peak(peaks, dtype)
+        e["frac_of_sustained"] = tflops / tensor_peak(peaks, dtype, "bf16_tflops_sustained")
+    else:
+        e["frac"] = gbs / peaks["hbm_gbs"]
+    return e
+
+
 class ClockSampler:
-    """Samples SM clock, power and throttle reasons with nvidia-smi while running."""
+    """Samples SM clock, power and throttle reasons with nvidia-smi while
+    running; summaries are taken over any wall-clock window."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 100):
+    def __init__(self, gpu_index: int, period_ms: int = 25):
         self.samples = []
         self.proc = None
-        self.t_timed = None
+        self.period_ms = period_ms
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
@@ -146,9 +184,6 @@ class ClockSampler:
             except ValueError:
                 continue
 
-    def mark_timed(self, t0, t1):
-        self.t_timed = (t0, t1)
-
     def stop(self):
         if self.proc is not None:
             self.proc.terminate()
@@ -157,14 +192,17 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
-        if not self.samples:
+    def summary(self, t0=None, t1=None, min_samples: int = 3):
+        """Clocks over the wall-clock window [t0, t1]; with fewer than
+        `min_samples` samples inside it, over the run so far (and says so)."""
+        samples = list(self.samples)
+        if not samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
         window = "timed"
-        sel = [s for s in self.samples if self.t_timed and self.t_timed[0] <= s["t"] <= self.t_timed[1]]
-        if len(sel) < 3:
-            window = "warmup+timed"
-            sel = self.samples[1:] or self.samples
+        sel = [s for s in samples if t0 is not None and t0 <= s["t"] <= t1]
+        if len(sel) < min_samples:
+            window = "whole run (fewer than %d samples inside the timed window)" % min_samples
+            sel = samples[1:] or samples
         active = lambda v: v.lower() in ("active", "1", "yes")
         reasons = set()
         for s in sel:
@@ -175,7 +213,9 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(s["sm"] for s in sel),
                 "sm_max_mhz": max(s["sm_max"] for s in sel),
                 "power_w_median": statistics.median(s["power"] for s in sel),
-                "samples": len(sel), "window": window, "reasons": sorted(reasons)}
+                "power_w_max": max(s["power"] for s in sel),
+                "samples": len(sel), "period_ms": self.period_ms, "window": window,
+                "reasons": sorted(reasons)}
 
 
 def dist_env():
@@ -206,8 +246,36 @@ def barrier(world: int, device=None):
 
 
 def aggregate_value(flops_per_step: float, steps: int, world: int, elapsed_max_s: float) -> float:
-    """Whole-job TFLOP/s: every rank's FLOPs over the slowest rank's time."""
+    """Whole-job TFLOP/s of replicas: every rank's FLOPs over the slowest
+    rank's time."""
     return flops_per_step * steps * world / elapsed_max_s / 1e12
+
+
+def column_slice(N: int, world: int, rank: int, granule: int = TILE_COLS):
+    """Columns [c0, c1) of Y (and of W1, W2) that rank `rank` computes in the
+    column-parallel split: whole 128-column tiles dealt out as evenly as
+    possible, the last slice ending at N. Every slice width is a multiple of
+    8 (N is), so each rank's problem meets the library's requirements."""
+    tiles = -(-N // granule)
+    if world > tiles:
+        raise ValueError("column split: %d ranks for %d column tiles" % (world, tiles))
+    t0 = rank * tiles // world
+    t1 = (rank + 1) * tiles // world
+    return t0 * granule, min(t1 * granule, N)
+
+
+def free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def torchrun_command(n: int, argv) -> list:
+    """The command that starts n ranks of this script on this node, one
+    process per GPU (rendezvous on 127.0.0.1)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            "--nproc-per-node=%d" % n, "--master-addr", "127.0.0.1",
+            "--master-port", str(free_port()), os.path.abspath(__file__)] + list(argv)
 
 
 # ----------------------------------------------------------------------------- CPU oracle legs
@@ -291,17 +359,158 @@ def fusion_efficiency(w, t_unfused_s: float, t_fused_s: float, hbm_gbs: float) -
     return (t_unfused_s - t_fused_s) / (8.0 * w.M * w.N / (hbm_gbs * 1e9))
 
 
+# ----------------------------------------------------------------------------- GPU pieces
+class Problem:
+    """One workload resident on the GPU: R rotating sets of A, packed weights,
+    Y and workspace (R sized so the sets exceed twice the L2), and the
+    forward call over set j. `n_cols` < N: this rank's column slice."""
+
+    def __init__(self, sg, w, dtype, dev, A_d, Wp, scales=None, n_cols=None):
+        import torch
+        self.sg, self.w, self.dtype, self.dev = sg, w, dtype, dev
+        self.fp8 = dtype == "fp8"
+        self.N = w.N if n_cols is None else n_cols
+        self.scales = scales
+        a_elem = 1 if self.fp8 else 2
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        per_set = w.M * w.K * a_elem + Wp.numel() + w.M * self.N * 2
+        self.R = max(2, -(-2 * l2 // per_set))
+        self.As = [A_d] + [A_d.clone() for _ in range(self.R - 1)]
+        self.Wps = [Wp] + [Wp.clone() for _ in range(self.R - 1)]
+        self.Ys = [torch.empty(w.M, self.N, dtype=torch.bfloat16, device=dev) for _ in range(self.R)]
+        ws = (sg.swiglu_workspace_bytes_fp8 if self.fp8 else sg.swiglu_workspace_bytes)(
+            w.M, self.N, w.K)
+        self.Wss = [torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev) if ws else None
+                    for _ in range(self.R)]
+        self.l2_note = "rotating %d input sets (%.0f MB total, > 2x the %.0f MB L2)" % (
+            self.R, self.R * per_set / 1e6, l2 / 1e6)
+
+    def forward(self, j, stream):
+        j %= self.R
+        if self.fp8:
+            s_a, s_w1, s_w2 = self.scales
+            self.sg.swiglu_up_forward_fp8(self.As[j], self.Wps[j], self.N, s_a, s_w1, s_w2,
+                                          Y=self.Ys[j], workspace=self.Wss[j], stream=stream)
+        else:
+            self.sg.swiglu_up_forward(self.As[j], self.Wps[j], self.N, Y=self.Ys[j],
+                                      workspace=self.Wss[j], stream=stream)
+
+    def capture(self, n, dev):
+        """A CUDA graph of n forward calls over the rotating sets (the calls
+        go through the same public entry point)."""
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream(dev)
+            for i in range(n):
+                self.forward(i, cs)
+        return g
+
+
+def pack_problem(sg, w, dtype, dev, inputs, split=None):
+    """Device copies of the inputs, packed weights (of this rank's column
+    slice when `split` = (c0, c1)) and the rotating sets. `inputs` are host
+    arrays (workloads' recipe) or device tensors (make_inputs_device)."""
+    import numpy as np
+    import torch
+    from tests.parity import to_device_bf16
+    fp8 = dtype == "fp8"
+    c0, c1 = split if split else (0, w.N)
+    if fp8:
+        A, W1, W2, s_a, s_w1, s_w2 = inputs
+        if isinstance(A, np.ndarray):
+            A_d = torch.from_numpy(A).to(dev)
+            W1d, W2d = torch.from_numpy(W1).to(dev), torch.from_numpy(W2).to(dev)
+        else:
+            A_d, W1d, W2d = A, W1, W2
+        Wp = sg.swiglu_pack_weights_fp8(W1d[:, c0:c1].contiguous(), W2d[:, c0:c1].contiguous())
+        scales = (s_a, s_w1, s_w2)
+    else:
+        A, W1, W2 = inputs
+        if isinstance(A, np.ndarray):
+            A_d, W1d, W2d = to_device_bf16(A, dev), to_device_bf16(W1, dev), to_device_bf16(W2, dev)
+        else:
+            A_d, W1d, W2d = A, W1, W2
+        Wp = sg.swiglu_pack_weights(W1d[:, c0:c1].contiguous(), W2d[:, c0:c1].contiguous())
+        scales = None
+    del W1d, W2d
+    return Problem(sg, w, dtype, dev, A_d, Wp, scales, n_cols=c1 - c0)
+
+
+def replay_window(graphs, stream, dev, min_s: float):
+    """Replays `graphs` (a list replayed in order = one round) until at least
+    `min_s` seconds of GPU time have passed; the number of rounds is fixed
+    from one untimed round first. Returns (seconds, rounds, wall t0, wall t1)."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for g in graphs:
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    one = max(e0.elapsed_time(e1) * 1e-3, 1e-7)
+    rounds = max(1, int(-(-min_s // one)))
+    wall0 = time.time()
+    e0.record(stream)
+    for _ in range(rounds):
+        for g in graphs:
+            g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    return e0.elapsed_time(e1) * 1e-3, rounds, wall0, wall1
+
+
+def graph_launches(R: int, launch_s: float, target_s: float = 2e-3, cap: int = 256) -> int:
+    """Launches per captured graph: enough that one replay lasts about
+    `target_s`, a multiple of the R rotating sets, at most `cap`."""
+    n = max(1, int(target_s / max(launch_s, 1e-7)))
+    n = max(R, -(-n // R) * R)
+    return min(n, max(R, cap // R * R))
+
+
+def sweep(sg, peaks, dtype, dev, stream, sampler, window_s: float, labels):
+    """Every workload timed on its own: inputs drawn on the GPU (seeded, the
+    workloads' distributions), packed, R rotating sets, a CUDA graph of
+    launches replayed for `window_s` seconds; one entry per workload."""
+    import torch
+
+    import workloads
+    out = []
+    for label in labels:
+        w = workloads.BY_LABEL[label]
+        inputs = workloads.make_inputs_device(w, dev, fp8=dtype == "fp8")
+        p = pack_problem(sg, w, dtype, dev, inputs)
+        del inputs
+        for i in range(3):
+            p.forward(i, stream)
+        torch.cuda.synchronize(dev)
+        sg.swiglu_check_device_status(stream)
+        n = graph_launches(p.R, roofline_us(w, peaks, dtype) * 1e-6)
+        g = p.capture(n, dev)
+        el, rounds, t0, t1 = replay_window([g], stream, dev, window_s)
+        sg.swiglu_check_device_status(stream)
+        e = {"workload": label, "name": w.name, "M": w.M, "K": w.K, "N": w.N,
+             "variant": w.variant, "launches": n * rounds}
+        e.update(roofline_entry(w, peaks, dtype, el / (n * rounds)))
+        e["clocks"] = sampler.summary(t0, t1, min_samples=2)
+        out.append(e)
+        del g, p
+        torch.cuda.empty_cache()
+    return out
+
+
 def time_unfused_context(w, W1, W2, As, Ys, R, dev, stream, steps, fused_value, hbm_gbs):
     """Context only (not this library): the unfused PyTorch path the pages
     compare against ("Tile-Level Activation Overlap for Efficient LLM
     Inference", Section 1: two GEMMs that write Gate and Up to HBM, then the
     activation), timed on the same rotating inputs: torch.matmul x2 (cuBLAS),
     then silu(g) * u in BF16."""
-    import numpy as np
     import torch
     import torch.nn.functional as F
-    w1 = torch.from_numpy(W1.view(np.int16)).view(torch.bfloat16).to(dev)
-    w2 = torch.from_numpy(W2.view(np.int16)).view(torch.bfloat16).to(dev)
+    from tests.parity import to_device_bf16
+    w1 = to_device_bf16(W1, dev)
+    w2 = to_device_bf16(W2, dev)
     W1s = [w1] + [w1.clone() for _ in range(R - 1)]
     W2s = [w2] + [w2.clone() for _ in range(R - 1)]
 
@@ -333,7 +542,7 @@ def time_unfused_context(w, W1, W2, As, Ys, R, dev, stream, steps, fused_value, 
                     "in BF16), then silu(Gate) * Up in BF16; same rotating inputs"}
 
 
-def time_mlp_context(w, W1, W2, sg, As, Wps, Ys, Wss, R, dev, stream, steps):
+def time_mlp_context(w, W1, W2, sg, p, dev, stream, steps):
     """Context for the pages' Figure 1 ("Tile-Level Activation Overlap for
     Efficient LLM Inference", Section 1: SwiGLU and its intermediates as a
     share of MLP time): the whole gated MLP out = Y W3 with a synthetic
@@ -342,14 +551,15 @@ def time_mlp_context(w, W1, W2, sg, As, Wps, Ys, Wss, R, dev, stream, steps):
     comparison the fused up-projection followed by torch.matmul (cuBLAS).
     Eager: three cuBLAS GEMMs and silu * mul, each also timed alone for the
     activation's share."""
-    import numpy as np
     import torch
     import torch.nn.functional as F
 
     import workloads
-    w3 = torch.from_numpy(workloads.make_W3(w).view(np.int16)).view(torch.bfloat16).to(dev)
-    w1 = torch.from_numpy(W1.view(np.int16)).view(torch.bfloat16).to(dev)
-    w2 = torch.from_numpy(W2.view(np.int16)).view(torch.bfloat16).to(dev)
+    from tests.parity import to_device_bf16
+    R, As, Wps, Ys, Wss = p.R, p.As, p.Wps, p.Ys, p.Wss
+    w3 = to_device_bf16(workloads.make_W3(w), dev)
+    w1 = to_device_bf16(W1, dev)
+    w2 = to_device_bf16(W2, dev)
     W1s = [w1] + [w1.clone() for _ in range(R - 1)]
     W2s = [w2] + [w2.clone() for _ in range(R - 1)]
     W3s = [w3] + [w3.clone() for _ in range(R - 1)]
@@ -422,12 +632,15 @@ def time_mlp_context(w, W1, W2, sg, As, Wps, Ys, Wss, R, dev, stream, steps):
                     "kernel and cuBLAS"}
 
 
-def config_of(w, l2_note, dtype: str = "bf16"):
+def config_of(w, l2_note, dtype: str = "bf16", split: str = "replicas", world: int = 1):
     io = ("FP8 E4M3 in (per-tensor amax/448 scales), BF16 out" if dtype == "fp8"
           else "BF16 in/out")
     c = {"workload": "%s: M=%d tokens, K=%d, N=%d, A~N(0,1), W1/W2~N(0,1/K), %s, FP32 accumulate"
                      % (w.name, w.M, w.K, w.N, io),
-         "M": w.M, "K": w.K, "N": w.N, "parallelism": "replicas"}
+         "M": w.M, "K": w.K, "N": w.N,
+         "parallelism": ("column-parallel x%d (each rank packs and computes its slice of the N "
+                         "columns, no collective)" % world) if split == "columns" else
+                        "replicas (each rank runs the whole workload, no collective)"}
     if l2_note:
         c["l2"] = l2_note
     return c
@@ -435,6 +648,8 @@ def config_of(w, l2_note, dtype: str = "bf16"):
 
 # ----------------------------------------------------------------------------- GPU arm
 def run_gb300(args, w):
+    import dataclasses
+
     import numpy as np
     import torch
 
@@ -448,49 +663,22 @@ def run_gb300(args, w):
     from gemm_swiglu_mlp_gb300 import build as lib_build
     lib_build.build()
     import gemm_swiglu_mlp_gb300 as sg
-    import workloads
-    from tests.parity import to_device_bf16
 
     peaks, peaks_src = load_peaks()
     fp8 = args.dtype == "fp8"
+    columns = args.split == "columns" and world > 1
     inputs = oracle_inputs(w, args.dtype)
-    if fp8:
-        A, W18, W28, s_a, s_w1, s_w2 = inputs
-        A_d = torch.from_numpy(A).to(dev)
-        Wp = sg.swiglu_pack_weights_fp8(torch.from_numpy(W18).to(dev), torch.from_numpy(W28).to(dev))
-        a_elem = 1
-    else:
-        A, W1, W2 = inputs
-        A_d = to_device_bf16(A, dev)
-        Wp = sg.swiglu_pack_weights(to_device_bf16(W1, dev), to_device_bf16(W2, dev))
-        a_elem = 2
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    per_set = w.M * w.K * a_elem + Wp.numel() + w.M * w.N * 2
-    R = max(2, -(-2 * l2 // per_set))
-    As = [A_d] + [A_d.clone() for _ in range(R - 1)]
-    Wps = [Wp] + [Wp.clone() for _ in range(R - 1)]
-    Ys = [torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
-    ws = (sg.swiglu_workspace_bytes_fp8 if fp8 else sg.swiglu_workspace_bytes)(w.M, w.N, w.K)
-    Wss = [torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev) if ws else None for _ in range(R)]
-    l2_note = "rotating %d input sets (%.0f MB total, > 2x the %.0f MB L2)" % (
-        R, R * per_set / 1e6, l2 / 1e6)
+    split = column_slice(w.N, world, rank) if columns else None
+    p = pack_problem(sg, w, args.dtype, dev, inputs, split)
+    # this rank's share of the work (its column slice, or the whole workload)
+    w_rank = dataclasses.replace(w, N=p.N)
+    job_flops_per_step = w.flops if columns else w.flops * world
     stream = torch.cuda.current_stream(dev)
-
-    def forward(j, st=None):
-        st = stream if st is None else st
-        if fp8:
-            sg.swiglu_up_forward_fp8(As[j], Wps[j], w.N, s_a, s_w1, s_w2, Y=Ys[j],
-                                     workspace=Wss[j], stream=st)
-        else:
-            sg.swiglu_up_forward(As[j], Wps[j], w.N, Y=Ys[j], workspace=Wss[j], stream=st)
-
-    def step(i):
-        forward(i % R)
 
     sampler = ClockSampler(local)
     time.sleep(0.3)
     for i in range(args.warmup):
-        step(i)
+        p.forward(i, stream)
     torch.cuda.synchronize(dev)
     sg.swiglu_check_device_status(stream)
 
@@ -503,30 +691,22 @@ def run_gb300(args, w):
     # buffers), so that the host's per-call cost does not set the pace of
     # launches shorter than it; `--launch direct` issues K calls instead.
     K = args.steps
-    graphs, timing = [], "direct: %d calls" % K
+    R = p.R
+    graphs, timing, g_main, gl = [], "direct: %d calls" % K, None, 0
     if args.launch == "graph":
         try:
             gl = min(K, R * max(1, 256 // R))
-
-            def capture(n):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    cs = torch.cuda.current_stream(dev)
-                    for i in range(n):
-                        forward(i % R, cs)
-                return g
-
-            g_main = capture(gl)
+            g_main = p.capture(gl, dev)
             graphs = [g_main] * (K // gl)
             if K % gl:
-                graphs.append(capture(K % gl))
+                graphs.append(p.capture(K % gl, dev))
             g_main.replay()                      # one untimed replay
             torch.cuda.synchronize(dev)
             sg.swiglu_check_device_status(stream)
             timing = "CUDA graph of %d launches replayed %d times%s" % (
                 gl, K // gl, (" + one of %d" % (K % gl)) if K % gl else "")
         except Exception as exc:               # capture unavailable: direct calls
-            graphs, timing = [], "direct: %d calls (graph capture failed: %s)" % (K, exc)
+            graphs, timing, g_main = [], "direct: %d calls (graph capture failed: %s)" % (K, exc), None
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(world, dev)
@@ -538,17 +718,30 @@ def run_gb300(args, w):
             g.replay()
     else:
         for i in range(K):
-            step(i)
+            p.forward(i, stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
     barrier(world, dev)
-    sampler.mark_timed(wall0, wall1)
     elapsed = t_begin.elapsed_time(t_end) * 1e-3
     sg.swiglu_check_device_status(stream)
     elapsed_max = max_over_ranks(elapsed, world, dev)
-    value = aggregate_value(w.flops, K, world, elapsed_max)
+    value = job_flops_per_step * K / elapsed_max / 1e12
     avg_launch = elapsed / K
+    clocks_timed = sampler.summary(wall0, wall1)
+
+    # ---- sustained: the headline launch replayed for >= args.sustained_s
+    # seconds, so that the clocks settle under the power cap and the sampler
+    # sees the load; reported against the sustained BF16 peak as well.
+    sustained = None
+    if g_main is not None and args.sustained_s > 0:
+        el, rounds, s0, s1 = replay_window([g_main], stream, dev, args.sustained_s)
+        sg.swiglu_check_device_status(stream)
+        n_l = rounds * gl
+        sustained = roofline_entry(w_rank, peaks, args.dtype, el / n_l)
+        sustained.update({"launches": n_l, "seconds": el, "clocks": sampler.summary(s0, s1, 10),
+                          "what": "the timed region's CUDA graph replayed back to back for "
+                                  ">= %.1f s of GPU time" % args.sustained_s})
 
     # ---- L2-warm context: the same launches on one input set, so A and the
     # weights stay in L2 from call to call when they fit (not the headline).
@@ -556,14 +749,14 @@ def run_gb300(args, w):
     w0 = torch.cuda.Event(enable_timing=True)
     w1_ = torch.cuda.Event(enable_timing=True)
     for _ in range(3):
-        forward(0)
+        p.forward(0, stream)
     w0.record(stream)
     for _ in range(Kw):
-        forward(0)
+        p.forward(0, stream)
     w1_.record(stream)
     torch.cuda.synchronize(dev)
     warm_s = w0.elapsed_time(w1_) * 1e-3 / Kw
-    l2_warm = {"avg_launch_us": warm_s * 1e6, "tflops": w.flops / warm_s / 1e12, "steps": Kw,
+    l2_warm = {"avg_launch_us": warm_s * 1e6, "tflops": w_rank.flops / warm_s / 1e12, "steps": Kw,
                "what": "one input set reused every call (operands L2-resident when they fit)"}
 
     # ---- end to end through the public API, as a serving loop runs it: every
@@ -572,9 +765,10 @@ def run_gb300(args, w):
     # consecutive steps overlap on three streams; slot j's device buffers are
     # reused only after step j-R has finished with them (events).
     Ke = min(K, 2000)
-    A_h = (torch.from_numpy(A) if fp8 else
-           torch.from_numpy(A.view(np.int16)).view(torch.bfloat16)).pin_memory()
-    Y_h = [torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory() for _ in range(R)]
+    A_np = inputs[0]
+    A_h = (torch.from_numpy(A_np) if fp8 else
+           torch.from_numpy(A_np.view(np.int16)).view(torch.bfloat16)).pin_memory()
+    Y_h = [torch.empty((w.M, p.N), dtype=torch.bfloat16).pin_memory() for _ in range(R)]
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(R)]
@@ -587,16 +781,16 @@ def run_gb300(args, w):
         if used[j]:
             s_in.wait_event(ev_comp[j])          # A slot free once its compute is done
         with torch.cuda.stream(s_in):
-            As[j].copy_(A_h, non_blocking=True)
+            p.As[j].copy_(A_h, non_blocking=True)
         ev_in[j].record(s_in)
         stream.wait_event(ev_in[j])
         if used[j]:
             stream.wait_event(ev_out[j])         # Y slot free once its copy-out is done
-        forward(j)
+        p.forward(j, stream)
         ev_comp[j].record(stream)
         s_out.wait_event(ev_comp[j])
         with torch.cuda.stream(s_out):
-            Y_h[j].copy_(Ys[j], non_blocking=True)
+            Y_h[j].copy_(p.Ys[j], non_blocking=True)
         ev_out[j].record(s_out)
         used[j] = True
 
@@ -618,20 +812,32 @@ def run_gb300(args, w):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world, dev)
-    sampler.stop()
     e_el = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world, dev)
-    e2e_value = aggregate_value(w.flops, Ke, world, e_el)
+    e2e_value = job_flops_per_step * Ke / e_el / 1e12
     sg.swiglu_check_device_status(stream)
     # the pipelined loop returned the right bytes: the last Y equals the device result
     y_check = Y_h[(Ke - 1) % R]
-    if not torch.equal(y_check.to(dev), Ys[(Ke - 1) % R]):
+    if not torch.equal(y_check.to(dev), p.Ys[(Ke - 1) % R]):
         raise RuntimeError("e2e loop: copied-out Y differs from the device result")
+    del Y_h, A_h
 
     unfused = mlp = None
-    if not args.no_context and not fp8:
-        unfused = time_unfused_context(w, W1, W2, As, Ys, R, dev, stream, min(K, 2000), value,
-                                       peaks["hbm_gbs"])
-        mlp = time_mlp_context(w, W1, W2, sg, As, Wps, Ys, Wss, R, dev, stream, min(K, 500))
+    if not args.no_context and not fp8 and not columns:
+        _, W1, W2 = inputs
+        unfused = time_unfused_context(w, W1, W2, p.As, p.Ys, R, dev, stream, min(K, 2000),
+                                       w.flops / avg_launch / 1e12, peaks["hbm_gbs"])
+        mlp = time_mlp_context(w, W1, W2, sg, p, dev, stream, min(K, 500))
+        torch.cuda.empty_cache()
+
+    l2_note = p.l2_note
+    sweep_out = None
+    if world == 1 and not args.no_sweep:
+        del p
+        torch.cuda.empty_cache()
+        import workloads
+        labels = [x.c for x in workloads.WORKLOADS]
+        sweep_out = sweep(sg, peaks, args.dtype, dev, stream, sampler, args.sweep_window_s, labels)
+    sampler.stop()
 
     if rank != 0:
         if world > 1:
@@ -639,10 +845,12 @@ def run_gb300(args, w):
             dist.destroy_process_group()
         return 0
 
-    bound = bound_of(w, peaks, args.dtype)
-    abytes = algorithmic_bytes(w, args.dtype)
+    # the roofline of the kernel as launched: the whole workload, or (column
+    # split) this rank's slice of it
+    bound = bound_of(w_rank, peaks, args.dtype)
+    abytes = algorithmic_bytes(w_rank, args.dtype)
     if bound == "tensor":
-        achieved = w.flops / avg_launch / 1e12
+        achieved = w_rank.flops / avg_launch / 1e12
         peak = tensor_peak(peaks, args.dtype)
         src = ("%s burst bf16 x %g (nominal fp8/bf16 ratio)" % (peaks_src, FP8_OVER_BF16) if fp8
                else "%s burst bf16" % peaks_src)
@@ -655,25 +863,32 @@ def run_gb300(args, w):
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": "%s copy bandwidth" % peaks_src}
-    roof["traffic"] = recorded_traffic(w.c, args.dtype)
-    roof["algorithmic_per_launch"] = w.flops if bound == "tensor" else abytes
+    roof["traffic"] = recorded_traffic(w.c, args.dtype) if not columns else None
+    roof["algorithmic_per_launch"] = w_rank.flops if bound == "tensor" else abytes
     roof["avg_launch_us"] = avg_launch * 1e6
-    roof["frac_of_roofline_time"] = roofline_us(w, peaks, args.dtype) * 1e-6 / avg_launch
+    roof["frac_of_roofline_time"] = roofline_us(w_rank, peaks, args.dtype) * 1e-6 / avg_launch
 
+    a_elem = 1 if fp8 else 2
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": elapsed_max / K * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3" if fp8 else "bf16",
-        "data": "synthetic", "config": dict(config_of(w, l2_note, args.dtype), timing=timing),
+        "scaling": "strong" if columns else "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3" if fp8 else "bf16", "data": "synthetic",
+        "config": dict(config_of(w, l2_note, args.dtype, "columns" if columns else "replicas",
+                                 world), timing=timing),
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": w.M * w.K * a_elem,
-                "d2h_bytes_per_step": w.M * w.N * 2, "steps": Ke,
+                "d2h_bytes_per_step": w.M * w_rank.N * 2, "steps": Ke,
                 "ms_per_step": e_el / Ke * 1e3,
                 "how": "pinned host A -> device, forward, device Y -> pinned host, every step; "
                        "copy-in, compute and copy-out of consecutive steps overlap on 3 streams"},
-        "gpu_launches": K, "clocks": sampler.summary(), "context_l2_warm": l2_warm,
+        "gpu_launches": K, "clocks": clocks_timed, "context_l2_warm": l2_warm,
         "device": device_info(dev),
     }
+    if sustained is not None:
+        line["context_sustained"] = sustained
+    if sweep_out is not None:
+        line["sweep"] = sweep_out
     if unfused is not None:
         line["context_unfused_torch"] = unfused
     if mlp is not None:
@@ -688,25 +903,41 @@ def run_gb300(args, w):
 
 
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10000)
-    p.add_argument("--warmup", type=int, default=500)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                   help="workload label (workloads.WORKLOADS), default 1 = Qwen-2.5-1.5B M=2048")
+                   help="workload label (workloads.WORKLOADS), default 11 = Qwen-2.5-72B M=8192")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-context", action="store_true",
-                   help="skip timing the unfused PyTorch path (context only)")
+                   help="skip timing the unfused PyTorch path and the whole MLP (context only)")
+    p.add_argument("--no-sweep", action="store_true", help="skip the per-workload sweep")
+    p.add_argument("--sweep-window-s", type=float, default=0.25,
+                   help="GPU seconds of replayed launches per sweep workload")
+    p.add_argument("--sustained-s", type=float, default=1.0,
+                   help="GPU seconds of the sustained window (0: skip)")
     p.add_argument("--launch", choices=("graph", "direct"), default="graph",
                    help="timed region: replay CUDA graphs of the calls (default) or call K times")
     p.add_argument("--dtype", choices=("bf16", "fp8"), default="bf16",
                    help="input type: bf16, or fp8 (E4M3 with per-tensor scales)")
     p.add_argument("--variant", choices=("auto", "1sm", "2sm"), default="auto",
                    help="fused kernel: auto (2-SM pairs for M >= 256), or force one (ablation)")
+    p.add_argument("--split", choices=("replicas", "columns"), default="replicas",
+                   help="N > 1: every rank runs the whole workload (replicas), or its slice of "
+                        "the output columns (column-parallel)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
+    if args.gpus < 1:
+        p.error("--gpus must be at least 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return subprocess.call(torchrun_command(args.gpus, argv))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != args.gpus:
+        p.error("--gpus %d but WORLD_SIZE=%d" % (args.gpus, world))
     import workloads
     w = workloads.BY_LABEL[args.workload]
     if args.variant != "auto":

@@ -18,7 +18,10 @@ def test_bench_prints_one_contract_line(dtype):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "0", "--steps", "50",
-           "--warmup", "3", "--no-cpu-baseline", "--no-context", "--dtype", dtype]
+           "--warmup", "3", "--no-cpu-baseline", "--no-context", "--dtype", dtype,
+           "--sustained-s", "0.2", "--sweep-window-s", "0.05"]
+    if dtype == "fp8":
+        cmd.append("--no-sweep")
     out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
@@ -40,3 +43,21 @@ def test_bench_prints_one_contract_line(dtype):
     assert r["dtype"] == ("fp8-e4m3" if dtype == "fp8" else "bf16")
     assert r["e2e"]["h2d_bytes_per_step"] == 128 * 896 * (1 if dtype == "fp8" else 2)
     assert r["e2e"]["d2h_bytes_per_step"] == 128 * 4864 * 2
+    cs = r["context_sustained"]
+    assert cs["seconds"] >= 0.2 and cs["launches"] % 50 == 0 and cs["us_per_launch"] > 0
+    for key in ("sm_mhz", "samples", "reasons"):
+        assert key in cs["clocks"], key
+    if dtype == "fp8":
+        assert "sweep" not in r
+        return
+    import workloads
+    sw = r["sweep"]
+    assert [e["workload"] for e in sw] == [w.c for w in workloads.WORKLOADS]
+    for e, w in zip(sw, workloads.WORKLOADS):
+        assert (e["M"], e["K"], e["N"], e["variant"]) == (w.M, w.K, w.N, w.variant)
+        for key in ("us_per_launch", "tflops", "bound", "frac", "achieved_gbs", "clocks",
+                    "launches", "frac_of_roofline_time"):
+            assert key in e, (w.c, key)
+        assert e["us_per_launch"] > 0 and 0 < e["frac"] < 1.5, e
+        assert e["tflops"] == pytest.approx(w.flops / (e["us_per_launch"] * 1e-6) / 1e12)
+        assert e["bound"] == ("hbm" if w.M <= 128 else "tensor"), e

@@ -114,3 +114,25 @@ def test_fp8_rejects_bad_scales(sg):
     for bad in (0.0, -1.0, float("nan")):
         assert lib.swiglu_up_forward_fp8(fake, fake * 3, fake * 5, 16, 128, 128, bad, 1.0, 1.0,
                                          None, 0, None) == 1
+
+
+def test_fp8_binding_checks_shapes(sg):
+    """The binding rejects a Y of the wrong shape, an A that is not [M, K]
+    and packed weights that are too small, before anything is launched."""
+    M, N, K = 64, 136, 144
+    A8, W18, W28, sa, s1, s2 = workloads.random_case_fp8(M, N, K, seed=5)
+    Wp = sg.swiglu_pack_weights_fp8(_dev(W18), _dev(W28))
+    Ad = _dev(A8)
+    with pytest.raises(ValueError, match="Y must be"):
+        sg.swiglu_up_forward_fp8(Ad, Wp, N, sa, s1, s2,
+                                 Y=torch.empty((M, N + 8), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError, match="Y must be"):
+        sg.swiglu_up_forward_fp8(Ad, Wp, N, sa, s1, s2,
+                                 Y=torch.empty((M + 1, N), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError, match="A must be"):
+        sg.swiglu_up_forward_fp8(Ad.view(-1), Wp, N, sa, s1, s2)
+    with pytest.raises(ValueError, match="Wpacked"):
+        sg.swiglu_up_forward_fp8(Ad, Wp[:-16], N, sa, s1, s2)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    assert sg.swiglu_up_forward_fp8(Ad, Wp, N, sa, s1, s2, Y=Y) is Y
+    sg.swiglu_check_device_status()

@@ -226,3 +226,46 @@ def random_case(M: int, N: int, K: int, seed: int, a_scale: float = 1.0):
     w1 = rng.standard_normal(size=(K, N), dtype=np.float32) * s
     w2 = rng.standard_normal(size=(K, N), dtype=np.float32) * s
     return f32_to_bf16_bits(a), f32_to_bf16_bits(w1), f32_to_bf16_bits(w2)
+
+
+def make_inputs_device(w: Workload, device, fp8: bool = False):
+    """The workload's inputs drawn on the GPU with torch's seeded generator
+    (Philox), same distributions and seeds as the host recipe above but not
+    the same values: for timing many shapes without host-side generation.
+
+    Returns (A, W1, W2) as BF16 device tensors, or for fp8=True
+    (A8, W1_8, W2_8, s_a, s_w1, s_w2) with E4M3 bytes as uint8 tensors and
+    per-tensor scales s = amax / 448."""
+    import torch
+
+    c = w.seed_index
+
+    def normal(seed, shape, scale):
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        if scale != 1.0:
+            x *= scale
+        return x
+
+    a = normal(1000 + c, (w.M, w.K), 1.0)
+    if w.variant == "stress":
+        a *= 8.0
+    elif w.variant == "outlier":
+        g = torch.Generator(device=device)
+        g.manual_seed(4000 + c)
+        cols = torch.randperm(w.K, generator=g, device=device)[:int(round(0.01 * w.K))]
+        a[:, cols] *= 20.0
+    w1 = normal(2000 + c, (w.K, w.N), float(w.K) ** -0.5)
+    w2 = normal(3000 + c, (w.K, w.N), float(w.K) ** -0.5)
+    if not fp8:
+        return a.to(torch.bfloat16), w1.to(torch.bfloat16), w2.to(torch.bfloat16)
+
+    def quant(x):
+        amax = float(x.abs().max())
+        s = float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
+        q = (x / s).clamp_(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+        return q.view(torch.uint8), s
+
+    (a8, sa), (w18, s1), (w28, s2) = quant(a), quant(w1), quant(w2)
+    return a8, w18, w28, sa, s1, s2

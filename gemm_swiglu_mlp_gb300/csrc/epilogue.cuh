@@ -77,6 +77,7 @@ struct FusedArgs {
     WorkSched sched;
     float *partials;          // 2 * grid slots of kSlotCols * slot_rows floats (stream-K only)
     unsigned int *counters;   // one per stream-K tile, zero between launches
+    int ticket_index;         // counters[ticket_index]: start-order tickets of a K-split pair launch
 #ifdef SWIGLU_TEST_FAULT_INJECTION
     int skip_first_fill;      // test build only: never fill the first pipeline stage
 #endif

@@ -32,6 +32,16 @@
 // it, and they finish their parts of the tile first (their range starts in
 // it).
 //
+// Co-residency: an owner c_lo waits for pairs c_lo+1..c_hi, so those must be
+// running, or done, while it waits. A launch with a K split therefore numbers
+// its pairs by the order in which they start, not by cluster index: each
+// pair takes a ticket t from a counter in the workspace (atomicInc wrapping
+// at grid - 1, so the counter is back at its start after the launch) and
+// works as pair grid - 1 - t. The pairs an owner waits for took their tickets
+// before it did, so they are resident or finished, and they never wait for
+// anyone of a later ticket; the wait ends whatever else shares the GPU (other
+// streams, other processes) and however the clusters are dispatched.
+//
 // PLAIN = true: the same kernel computes a plain product out = A x W (no
 // activation), the down-projection out = Y x W3 that completes the gated
 // MLP. The packed weight tile then holds 256 output columns (one CTA loads
@@ -101,7 +111,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     const uint32_t half = rank & 1u;               // 0: leader (Gate rows), 1: Up rows
     constexpr uint32_t leader_rank = 0;
     const bool is_leader = half == 0;
-    const int pair = blockIdx.x / 2;               // schedule worker: one cluster
+    // schedule worker: one cluster; with a K split, by start order (below)
+    int pair = static_cast<int>(blockIdx.x / 2);
+    if (args.sched.sk_iters > 0) pair = args.sched.grid - 1 - pair;   // guess, for the prefetch
 
     auto full_bar = [&](int s) { return sbase + C::OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sbase + C::OFF_BAR + 8u * (STAGES + s); };
@@ -112,6 +124,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     volatile int *last_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);
+    volatile int *worker_slot = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 12);
     // the same flag in the other CTA of the pair
     auto set_abort_both = [&]() {
         *abort_flag = 1;
@@ -170,6 +183,19 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
         }
     }
     griddep_wait();
+    if (sched.sk_iters > 0) {
+        // worker number by start order (see the header comment); the peer
+        // CTA gets it through distributed shared memory
+        if (is_leader && warp == 0 && lane == 0) {
+            const unsigned int t =
+                atomicInc(args.counters + args.ticket_index, static_cast<unsigned int>(sched.grid - 1));
+            const int wid = sched.grid - 1 - static_cast<int>(t % static_cast<unsigned int>(sched.grid));
+            *worker_slot = wid;
+            st_cluster_u32(mapa_shared(sbase + C::OFF_MISC + 12, 1u), static_cast<uint32_t>(wid));
+        }
+        cluster_sync();
+        pair = *worker_slot;
+    }
 
     uint32_t issued_mask = 0, last_parity = 0;  // leader's drain bookkeeping
 

@@ -246,9 +246,11 @@ LaunchPlan choose_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_cluste
 // the device (so a counter never lands where another shape's call left
 // partial sums), then the partial slots. Every stream-K tile needs at most
 // one counter per CTA half, and there are fewer than 2 * grid stream-K
-// tiles, so 4 * sm_count counters always suffice.
+// tiles, so 4 * sm_count counters always suffice; one more, after them, is
+// the CTA-pair kernel's start-order ticket counter.
+int ticket_index(int sm_count) { return 4 * sm_count; }
 size_t counter_region_bytes(int sm_count) {
-    return (static_cast<size_t>(4) * sm_count * sizeof(unsigned int) + 255) / 256 * 256;
+    return (static_cast<size_t>(4 * sm_count + 1) * sizeof(unsigned int) + 255) / 256 * 256;
 }
 // Partial slots: 2 per worker (its first and last stream-K tile), and for
 // the 2-SM kernel one per CTA of the pair.
@@ -509,6 +511,7 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
     args.partials = ws_need ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                                         counter_region_bytes(st->sm_count))
                             : nullptr;
+    args.ticket_index = ticket_index(st->sm_count);
 
     // Both kernels are launched with programmatic stream serialization: a
     // launch may begin while the previous kernel in the stream finishes; the
@@ -706,6 +709,7 @@ int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M,
     args.partials = ws_need ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                                         counter_region_bytes(st->sm_count))
                             : nullptr;
+    args.ticket_index = ticket_index(st->sm_count);
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -908,3 +912,39 @@ extern "C" int swiglu_up_forward_noalloc(const void *A, const void *Wpacked, voi
     return swiglu_up_forward(A, Wpacked, Y, M, N, K, need ? na.scratch : nullptr,
                              need ? static_cast<size_t>(SWIGLU_NOALLOC_SCRATCH_BYTES) : 0, stream);
 }
+
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+namespace swiglu {
+namespace {
+// Test build only: other work that holds SMs for a fixed time. Each block
+// (one warp, with enough shared memory that no other large-footprint block
+// fits beside it on its SM) sleeps until `ns` nanoseconds of %globaltimer
+// have passed; the iteration count is capped as well, so it always returns.
+__global__ void test_busy_kernel(unsigned long long ns, unsigned long long max_iters) {
+    extern __shared__ uint8_t hold[];
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (unsigned long long i = 0; i < max_iters; ++i) {
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (t - t0 >= ns) break;
+        __nanosleep(1000);
+    }
+    if (ns == 0 && threadIdx.x == 0) hold[0] = 0;
+}
+constexpr int kBusySmemBytes = 200 * 1024;
+}  // namespace
+}  // namespace swiglu
+
+extern "C" int swiglu_test_busy_sms(int blocks, unsigned long long ns, void *stream) {
+    if (blocks < 1 || blocks > 4096 || ns > 10000000000ULL) return SWIGLU_ERR_INVALID_ARG;
+    if (cudaFuncSetAttribute(swiglu::test_busy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             swiglu::kBusySmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return SWIGLU_ERR_CUDA;
+    }
+    swiglu::test_busy_kernel<<<blocks, 32, swiglu::kBusySmemBytes,
+                               static_cast<cudaStream_t>(stream)>>>(ns, ns / 10 + 1000000ULL);
+    if (cudaGetLastError() != cudaSuccess) return SWIGLU_ERR_CUDA;
+    return SWIGLU_OK;
+}
+#endif

@@ -12,6 +12,7 @@ hangs a GPU: the only failure is a wait on a barrier that nothing completes.
 """
 import ctypes
 import os
+import time
 
 import numpy as np
 import pytest
@@ -139,4 +140,100 @@ def test_down_projection_wait_timeout(fi_lib, monkeypatch, mode, M, N, K):
     out, status, raw = run()
     assert status == 0 and raw == 0
     r = compare(from_device_bf16(out), oracle.matmul(Yb, W3)["C"])
+    assert r["mismatches"] == 0 and r["over_bound"] == 0, r
+
+
+def _busy_and_run(lib, op, n_busy=120, busy_ns=300_000_000):
+    """Other work holds `n_busy` SMs for `busy_ns` on another stream while
+    `op(stream)` runs on this one. Returns (op status word, raw word,
+    whether the busy kernel was still running when op's stream finished)."""
+    lib.swiglu_test_busy_sms.argtypes = [ctypes.c_int, ctypes.c_ulonglong, ctypes.c_void_p]
+    busy_stream = torch.cuda.Stream()
+    busy_done = torch.cuda.Event()
+    assert lib.swiglu_test_busy_sms(n_busy, busy_ns, busy_stream.cuda_stream) == 0
+    busy_done.record(busy_stream)
+    time.sleep(0.02)                                  # the busy blocks are resident by now
+    stream = torch.cuda.current_stream()
+    out = op(stream.cuda_stream)
+    stream.synchronize()
+    still_busy = not busy_done.query()
+    raw = ctypes.c_uint32(0)
+    status = lib.swiglu_check_device_status(stream.cuda_stream, ctypes.byref(raw))
+    busy_stream.synchronize()
+    return out, status, raw.value, still_busy
+
+
+@pytest.mark.parametrize("kind", ["down", "up"])
+def test_split_tiles_finish_while_other_work_holds_sms(fi_lib, monkeypatch, kind):
+    """A K-split launch of the CTA-pair kernel while a kernel on another
+    stream holds 120 of the SMs for 300 ms: only some of its pairs can run
+    at first. A split tile's owner waits only for pairs that started before
+    it (worker numbers follow the start order), so the call completes on the
+    free SMs, well within this build's ~10 ms wait limit, and is correct.
+    (Were owners to wait for pairs not yet started, they would hold their
+    SMs until the limit and report SWIGLU_ERR_DEVICE_TIMEOUT.)"""
+    import oracle
+    lib = fi_lib
+    vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    if kind == "down":
+        # 8 output tiles of 256 x 256, 64 k-blocks each: stream-K over 64 pairs
+        M, N, K = 512, 4096, 1024
+        lib.swiglu_pack_down_weights.argtypes = [vp, i64, i64, vp, vp]
+        lib.swiglu_down_packed_weight_bytes.argtypes = [i64, i64]
+        lib.swiglu_down_packed_weight_bytes.restype = sz
+        lib.swiglu_down_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.swiglu_down_workspace_bytes.restype = sz
+        lib.swiglu_down_forward.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+        rng = np.random.Generator(np.random.PCG64(79))
+        Yb = workloads.f32_to_bf16_bits(rng.standard_normal(size=(M, N), dtype=np.float32))
+        W3 = workloads.f32_to_bf16_bits(
+            rng.standard_normal(size=(N, K), dtype=np.float32) * np.float32(N ** -0.5))
+        Yd, W3d = to_device_bf16(Yb, "cuda"), to_device_bf16(W3, "cuda")
+        W3p = torch.empty(lib.swiglu_down_packed_weight_bytes(N, K), dtype=torch.uint8,
+                          device="cuda")
+        st0 = torch.cuda.current_stream().cuda_stream
+        assert lib.swiglu_pack_down_weights(W3d.data_ptr(), N, K, W3p.data_ptr(), st0) == 0
+        ws_bytes = lib.swiglu_down_workspace_bytes(M, N, K)
+        assert ws_bytes > 0                                  # the K split is planned
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+
+        def op(stream):
+            out = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+            assert lib.swiglu_down_forward(Yd.data_ptr(), W3p.data_ptr(), out.data_ptr(), M, N,
+                                           K, ws.data_ptr(), ws_bytes, stream) == 0
+            return out
+
+        out, status, raw, still_busy = _busy_and_run(lib, op)
+        assert status == 0 and raw == 0, raw
+        want = oracle.matmul(Yb, W3)["C"]
+    else:
+        # forced stream-K on the CTA-pair kernel: 16 tiles, 64 k-blocks each
+        monkeypatch.setenv("SWIGLU_FUSED_VARIANT", "2sm")
+        monkeypatch.setenv("SWIGLU_SCHEDULE", "sk")
+        M, N, K = 512, 1024, 4096
+        A, W1, W2 = workloads.random_case(M, N, K, seed=80)
+        Ad = to_device_bf16(A, "cuda")
+        W1d, W2d = to_device_bf16(W1, "cuda"), to_device_bf16(W2, "cuda")
+        Wp = torch.empty(lib.swiglu_packed_weight_bytes(N, K), dtype=torch.uint8, device="cuda")
+        st0 = torch.cuda.current_stream().cuda_stream
+        assert lib.swiglu_pack_weights(W1d.data_ptr(), W2d.data_ptr(), K, N, Wp.data_ptr(),
+                                       st0) == 0
+        ws_bytes = lib.swiglu_workspace_bytes(M, N, K)
+        assert ws_bytes > 0
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+
+        def op(stream):
+            Y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+            assert lib.swiglu_up_forward(Ad.data_ptr(), Wp.data_ptr(), Y.data_ptr(), M, N, K,
+                                         ws.data_ptr(), ws_bytes, stream) == 0
+            return Y
+
+        out, status, raw, still_busy = _busy_and_run(lib, op)
+        assert status == 0 and raw == 0, raw
+        want = oracle.swiglu_up(A, W1, W2)["Y"]
+    # the call ran beside the busy kernel, not after it
+    assert still_busy
+    r = compare(from_device_bf16(out), want)
     assert r["mismatches"] == 0 and r["over_bound"] == 0, r

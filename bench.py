@@ -500,6 +500,144 @@ def sweep(sg, peaks, dtype, dev, stream, sampler, window_s: float, labels):
     return out
 
 
+ABLATION_FORMS = (
+    # (packed layout, kernel variant, schedule form); "auto" = the library's choice
+    [(layout, "auto", mode) for layout in ("blocked", "interleaved")
+     for mode in ("auto", "dp", "split", "sk", "sk-tail")] +
+    [(layout, variant, "auto") for layout in ("blocked", "interleaved") for variant in ("1sm", "2sm")])
+
+
+def ablation(sg, peaks, dev, stream, sampler, window_s: float, labels, forms=ABLATION_FORMS):
+    """The schedule ablation (the pages' Kernel-1 / Kernel-2 trade on this
+    GPU): for every workload, each packed layout (blocked 128-row halves, or
+    the pages' column interleave) x kernel (1-SM, CTA pairs) x work split
+    (whole tiles, column sub-tiles for the last wave, stream-K), forced
+    through SWIGLU_FUSED_VARIANT / SWIGLU_SCHEDULE, timed like the sweep on
+    the same rotating inputs; plus the unfused cuBLAS path for the fusion
+    efficiency. BF16."""
+    import torch
+    import torch.nn.functional as F
+
+    import workloads
+    out = []
+    saved = {k: os.environ.get(k) for k in ("SWIGLU_FUSED_VARIANT", "SWIGLU_SCHEDULE")}
+    try:
+        for label in labels:
+            w = workloads.BY_LABEL[label]
+            A, W1, W2 = workloads.make_inputs_device(w, dev)
+            l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+            per_set = 2 * (w.M * w.K + 4 * w.K * w.N + w.M * w.N)
+            R = max(2, -(-2 * l2 // per_set))
+            As = [A] + [A.clone() for _ in range(R - 1)]
+            Ys = [torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+            packed = {"blocked": sg.swiglu_pack_weights(W1, W2),
+                      "interleaved": sg.swiglu_pack_weights_interleaved(W1, W2)}
+            Wps = {k: [v] + [v.clone() for _ in range(R - 1)] for k, v in packed.items()}
+            fwd = {"blocked": sg.swiglu_up_forward, "interleaved": sg.swiglu_up_forward_interleaved}
+            entry = {"workload": label, "name": w.name, "M": w.M, "K": w.K, "N": w.N, "forms": []}
+            for layout, variant, mode in forms:
+                for k, v in (("SWIGLU_FUSED_VARIANT", variant), ("SWIGLU_SCHEDULE", mode)):
+                    if v == "auto":
+                        os.environ.pop(k, None)
+                    else:
+                        os.environ[k] = v
+                ws = sg.swiglu_workspace_bytes(w.M, w.N, w.K)
+                Wss = [torch.zeros(ws, dtype=torch.uint8, device=dev) if ws else None
+                       for _ in range(R)]
+
+                def one(i, st, layout=layout, Wss=Wss):
+                    j = i % R
+                    fwd[layout](As[j], Wps[layout][j], w.N, Y=Ys[j], workspace=Wss[j], stream=st)
+
+                for i in range(3):
+                    one(i, stream)
+                torch.cuda.synchronize(dev)
+                sg.swiglu_check_device_status(stream)
+                n = graph_launches(R, roofline_us(w, peaks) * 1e-6)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    cs = torch.cuda.current_stream(dev)
+                    for i in range(n):
+                        one(i, cs)
+                el, rounds, t0, t1 = replay_window([g], stream, dev, window_s)
+                sg.swiglu_check_device_status(stream)
+                f = {"layout": layout, "variant": variant, "schedule": mode,
+                     "workspace_bytes": ws, "launches": n * rounds}
+                f.update(roofline_entry(w, peaks, "bf16", el / (n * rounds)))
+                f["sm_mhz"] = sampler.summary(t0, t1, min_samples=1).get("sm_mhz")
+                entry["forms"].append(f)
+                del g, Wss
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+            # the unfused path on the same rotating inputs
+            W1s = [W1] + [W1.clone() for _ in range(R - 1)]
+            W2s = [W2] + [W2.clone() for _ in range(R - 1)]
+
+            def unfused(i):
+                j = i % R
+                torch.mul(F.silu(torch.matmul(As[j], W1s[j])), torch.matmul(As[j], W2s[j]),
+                          out=Ys[j])
+
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    unfused(i)
+                torch.cuda.synchronize(dev)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                t_est = max(roofline_us(w, peaks) * 1e-6, 1e-6)
+                reps = max(R, int(window_s / (2 * t_est)))
+                for i in range(reps):
+                    unfused(i)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+            t_unf = e0.elapsed_time(e1) * 1e-3 / reps
+            entry["unfused_us"] = t_unf * 1e6
+            for f in entry["forms"]:
+                f["fusion_efficiency"] = fusion_efficiency(w, t_unf, f["us_per_launch"] * 1e-6,
+                                                           peaks["hbm_gbs"])
+                f["speedup_vs_unfused"] = t_unf / (f["us_per_launch"] * 1e-6)
+            out.append(entry)
+            del As, Ys, packed, Wps, W1s, W2s, A, W1, W2
+            torch.cuda.empty_cache()
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return out
+
+
+def run_ablation(args):
+    """`bench.py --ablation`: one JSON line with the ablation of every workload."""
+    import torch
+    world, rank, local = dist_env()
+    if world != 1:
+        raise SystemExit("--ablation runs on one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from gemm_swiglu_mlp_gb300 import build as lib_build
+    lib_build.build()
+    import gemm_swiglu_mlp_gb300 as sg
+
+    import workloads
+    peaks, peaks_src = load_peaks()
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    labels = args.ablation_workloads.split(",") if args.ablation_workloads else [
+        x.c for x in workloads.WORKLOADS]
+    res = ablation(sg, peaks, dev, torch.cuda.current_stream(dev), sampler, args.sweep_window_s,
+                   labels)
+    sampler.stop()
+    print(json.dumps({"ablation": res, "peaks": peaks, "peaks_source": peaks_src,
+                      "kernel_source_hash": kernel_source_hash(), "device": device_info(dev),
+                      "window_s": args.sweep_window_s}), flush=True)
+    return 0
+
+
 def time_unfused_context(w, W1, W2, As, Ys, R, dev, stream, steps, fused_value, hbm_gbs):
     """Context only (not this library): the unfused PyTorch path the pages
     compare against ("Tile-Level Activation Overlap for Efficient LLM
@@ -925,6 +1063,11 @@ def main(argv=None):
                    help="input type: bf16, or fp8 (E4M3 with per-tensor scales)")
     p.add_argument("--variant", choices=("auto", "1sm", "2sm"), default="auto",
                    help="fused kernel: auto (2-SM pairs for M >= 256), or force one (ablation)")
+    p.add_argument("--ablation", action="store_true",
+                   help="instead of the benchmark: time every workload under each packed layout, "
+                        "kernel variant and schedule form (one JSON line)")
+    p.add_argument("--ablation-workloads", default="",
+                   help="comma-separated workload labels for --ablation (default: all)")
     p.add_argument("--split", choices=("replicas", "columns"), default="replicas",
                    help="N > 1: every rank runs the whole workload (replicas), or its slice of "
                         "the output columns (column-parallel)")
@@ -944,6 +1087,8 @@ def main(argv=None):
         os.environ["SWIGLU_FUSED_VARIANT"] = args.variant
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.ablation:
+        return run_ablation(args)
     return run_gb300(args, w)
 
 

@@ -12,6 +12,8 @@ The names follow the C ABI:
     swiglu_pack_weights_nk(W1, W2, Wpacked=None) -> Wpacked  (nn.Linear [N, K] weights)
     swiglu_workspace_bytes(M, N, K) -> int
     swiglu_up_forward(A, Wpacked, N, Y=None, workspace=None) -> Y
+    swiglu_pack_weights_interleaved(W1, W2) / swiglu_up_forward_interleaved(A, Wp, N)
+        (the column-interleaved packing, for comparison with the default)
     swiglu_check_device_status() -> raw status word (raises on timeout)
     swiglu_status_string(status) -> str
 
@@ -36,7 +38,8 @@ __all__ = [
     "swiglu_packed_weight_bytes_fp8", "swiglu_pack_weights_fp8", "swiglu_workspace_bytes_fp8",
     "swiglu_up_forward_fp8", "swiglu_down_packed_weight_bytes", "swiglu_pack_down_weights",
     "swiglu_pack_down_weights_nk", "swiglu_down_workspace_bytes", "swiglu_down_forward",
-    "swiglu_mlp_workspace_bytes", "swiglu_mlp_forward", "EXPORTED_SYMBOLS",
+    "swiglu_mlp_workspace_bytes", "swiglu_mlp_forward", "swiglu_pack_weights_interleaved",
+    "swiglu_up_forward_interleaved", "EXPORTED_SYMBOLS",
 ]
 
 SWIGLU_OK = 0
@@ -52,7 +55,8 @@ EXPORTED_SYMBOLS = (
     "swiglu_packed_weight_bytes_fp8", "swiglu_pack_weights_fp8", "swiglu_workspace_bytes_fp8",
     "swiglu_up_forward_fp8", "swiglu_down_packed_weight_bytes", "swiglu_pack_down_weights",
     "swiglu_pack_down_weights_nk", "swiglu_down_workspace_bytes", "swiglu_down_forward",
-    "swiglu_mlp_workspace_bytes", "swiglu_mlp_forward",
+    "swiglu_mlp_workspace_bytes", "swiglu_mlp_forward", "swiglu_pack_weights_interleaved",
+    "swiglu_up_forward_interleaved",
 )
 
 _lock = threading.Lock()
@@ -118,6 +122,10 @@ def load_library(path: str = LIB_PATH):
         lib.swiglu_mlp_workspace_bytes.restype = sz
         lib.swiglu_mlp_forward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, sz, vp]
         lib.swiglu_mlp_forward.restype = ctypes.c_int
+        lib.swiglu_pack_weights_interleaved.argtypes = [vp, vp, i64, i64, vp, vp]
+        lib.swiglu_pack_weights_interleaved.restype = ctypes.c_int
+        lib.swiglu_up_forward_interleaved.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+        lib.swiglu_up_forward_interleaved.restype = ctypes.c_int
         lib.swiglu_check_device_status.argtypes = [vp, u32p]
         lib.swiglu_check_device_status.restype = ctypes.c_int
         _lib = lib
@@ -169,6 +177,17 @@ def swiglu_workspace_bytes(M: int, N: int, K: int) -> int:
 def swiglu_pack_weights(W1: torch.Tensor, W2: torch.Tensor, Wpacked: torch.Tensor = None,
                         stream=None) -> torch.Tensor:
     """Pack W1, W2 ([K, N] BF16 each) into the library's fused weight operand."""
+    return _pack_kn("swiglu_pack_weights", W1, W2, Wpacked, stream)
+
+
+def swiglu_pack_weights_interleaved(W1: torch.Tensor, W2: torch.Tensor,
+                                    Wpacked: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Pack W1, W2 ([K, N] BF16 each) column-interleaved (even packed rows
+    Gate, odd rows Up), for swiglu_up_forward_interleaved."""
+    return _pack_kn("swiglu_pack_weights_interleaved", W1, W2, Wpacked, stream)
+
+
+def _pack_kn(entry: str, W1, W2, Wpacked, stream) -> torch.Tensor:
     lib = load_library()
     _require_bf16_cuda(W1, "W1")
     _require_bf16_cuda(W2, "W2")
@@ -181,8 +200,8 @@ def swiglu_pack_weights(W1: torch.Tensor, W2: torch.Tensor, Wpacked: torch.Tenso
     elif Wpacked.numel() * Wpacked.element_size() < nbytes or not Wpacked.is_contiguous():
         raise ValueError("Wpacked must be contiguous with at least %d bytes" % nbytes)
     with torch.cuda.device(W1.device):
-        _check(lib.swiglu_pack_weights(W1.data_ptr(), W2.data_ptr(), K, N, Wpacked.data_ptr(),
-                                       _stream_handle(stream)), "swiglu_pack_weights")
+        _check(getattr(lib, entry)(W1.data_ptr(), W2.data_ptr(), K, N, Wpacked.data_ptr(),
+                                   _stream_handle(stream)), entry)
     return Wpacked
 
 
@@ -209,6 +228,17 @@ def swiglu_pack_weights_nk(W1: torch.Tensor, W2: torch.Tensor, Wpacked: torch.Te
 def swiglu_up_forward(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: torch.Tensor = None,
                       workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
     """Y[M, N] = SiLU(A x W1) (.) (A x W2) from A [M, K] BF16 and packed weights."""
+    return _forward("swiglu_up_forward", A, Wpacked, N, Y, workspace, stream)
+
+
+def swiglu_up_forward_interleaved(A: torch.Tensor, Wpacked: torch.Tensor, N: int,
+                                  Y: torch.Tensor = None, workspace: torch.Tensor = None,
+                                  stream=None) -> torch.Tensor:
+    """swiglu_up_forward on weights from swiglu_pack_weights_interleaved."""
+    return _forward("swiglu_up_forward_interleaved", A, Wpacked, N, Y, workspace, stream)
+
+
+def _forward(entry: str, A, Wpacked, N, Y, workspace, stream) -> torch.Tensor:
     lib = load_library()
     _require_bf16_cuda(A, "A")
     if A.dim() != 2:
@@ -240,9 +270,8 @@ def swiglu_up_forward(A: torch.Tensor, Wpacked: torch.Tensor, N: int, Y: torch.T
             if workspace is None:
                 workspace = _default_workspace(A.device, ws_need, stream)
             ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-        _check(lib.swiglu_up_forward(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(), M, N, K,
-                                     ws_ptr, ws_bytes, _stream_handle(stream)),
-               "swiglu_up_forward")
+        _check(getattr(lib, entry)(A.data_ptr(), Wpacked.data_ptr(), Y.data_ptr(), M, N, K,
+                                   ws_ptr, ws_bytes, _stream_handle(stream)), entry)
     finally:
         if switch:
             torch.cuda.set_device(prev)

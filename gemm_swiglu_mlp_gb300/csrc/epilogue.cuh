@@ -144,21 +144,60 @@ __device__ __forceinline__ void stage_y32(uint32_t ybuf, int lane, int c, const 
     }
 }
 
-// Gate columns [c, c+32) and the matching Up columns (up_off columns further
-// on: 128 for a whole tile, the sub-tile width for a column sub-tile).
+// Where a tile's Gate and Up accumulators sit in TMEM, by packed layout:
+//   * blocked (IL = false): the packed tile holds 128 Gate rows, then the
+//     128 matching Up rows, so Gate of output column c is accumulator column
+//     c and its Up is column up_off + c (128 for a whole tile, the sub-tile
+//     width for a column sub-tile);
+//   * interleaved (IL = true, the pages' Kernel-2 pairing: even packed rows
+//     Gate, odd rows Up): Gate of output column c is accumulator column 2c
+//     and its Up is 2c + 1, whatever the unit's width.
+// Output columns [c, c+32) take two 32-column TMEM loads either way:
+// columns c and up_off + c (blocked), or 2c and 2c + 32 (interleaved).
+template <bool IL>
+__device__ __forceinline__ void tmem_ld_pair_cols(uint32_t tbase, int c, int up_off,
+                                                  uint32_t (&ra)[32], uint32_t (&rb)[32]) {
+    if constexpr (IL) {
+        tmem_ld_32x32b_x32(tbase + 2 * c, ra);
+        tmem_ld_32x32b_x32(tbase + 2 * c + 32, rb);
+    } else {
+        tmem_ld_32x32b_x32(tbase + c, ra);
+        tmem_ld_32x32b_x32(tbase + up_off + c, rb);
+    }
+}
+
+// The 32 Gate and 32 Up values of the two loads above, in output-column
+// order.
+template <bool IL>
+__device__ __forceinline__ void split_gu(const uint32_t (&ra)[32], const uint32_t (&rb)[32],
+                                        float (&g)[32], float (&u)[32]) {
+    if constexpr (IL) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            g[i] = __uint_as_float(ra[2 * i]);
+            u[i] = __uint_as_float(ra[2 * i + 1]);
+            g[16 + i] = __uint_as_float(rb[2 * i]);
+            u[16 + i] = __uint_as_float(rb[2 * i + 1]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            g[i] = __uint_as_float(ra[i]);
+            u[i] = __uint_as_float(rb[i]);
+        }
+    }
+}
+
+// Gate and Up of output columns [c, c+32) of this thread's row.
+template <bool IL = false>
 __device__ __forceinline__ void tmem_ld_gu(uint32_t tbase, int c, float (&g)[32], float (&u)[32],
                                            int up_off = 128) {
     uint32_t gr[32], ur[32];
-    tmem_ld_32x32b_x32(tbase + c, gr);
-    tmem_ld_32x32b_x32(tbase + up_off + c, ur);
+    tmem_ld_pair_cols<IL>(tbase, c, up_off, gr, ur);
     tmem_ld_wait();
     reg_fence32(gr);
     reg_fence32(ur);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        g[i] = __uint_as_float(gr[i]);
-        u[i] = __uint_as_float(ur[i]);
-    }
+    split_gu<IL>(gr, ur, g, u);
 }
 
 // Whole-tile epilogue into the warp's staging buffer: the four 32-column
@@ -166,27 +205,20 @@ __device__ __forceinline__ void tmem_ld_gu(uint32_t tbase, int c, float (&g)[32]
 // each tcgen05.ld's latency hides behind the previous chunk's activation.
 // (tcgen05.wait::ld waits for all of the thread's loads, so the next chunk
 // is issued right after the wait that completes the current one.)
+template <bool IL = false>
 __device__ __forceinline__ void epilogue_stage_tile(uint32_t tbase, uint32_t ybuf, int lane,
                                                     float gs, float us) {
     uint32_t gr[2][32], ur[2][32];
-    tmem_ld_32x32b_x32(tbase, gr[0]);
-    tmem_ld_32x32b_x32(tbase + 128, ur[0]);
+    tmem_ld_pair_cols<IL>(tbase, 0, 128, gr[0], ur[0]);
     tmem_ld_wait();
     reg_fence32(gr[0]);
     reg_fence32(ur[0]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int cur = i & 1;
-        if (i + 1 < 4) {
-            tmem_ld_32x32b_x32(tbase + 32 * (i + 1), gr[cur ^ 1]);
-            tmem_ld_32x32b_x32(tbase + 128 + 32 * (i + 1), ur[cur ^ 1]);
-        }
+        if (i + 1 < 4) tmem_ld_pair_cols<IL>(tbase, 32 * (i + 1), 128, gr[cur ^ 1], ur[cur ^ 1]);
         float g[32], u[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            g[k] = __uint_as_float(gr[cur][k]);
-            u[k] = __uint_as_float(ur[cur][k]);
-        }
+        split_gu<IL>(gr[cur], ur[cur], g, u);
         stage_y32(ybuf, lane, 32 * i, g, u, gs, us);
         if (i + 1 < 4) {
             tmem_ld_wait();
@@ -280,13 +312,15 @@ __device__ __forceinline__ void store_staged_boxes(const CUtensorMap *tm, uint32
 }
 
 // Epilogue of a column sub-tile (width 64 or 32), or of a whole tile stored
-// without shared-memory staging (width 128): TMEM holds Gate in columns
-// [0, width) and Up in [width, 2*width). Each thread owns one output row.
+// without shared-memory staging (width 128): TMEM holds the unit's 2*width
+// Gate|Up columns (blocked: Gate in [0, width), Up in [width, 2*width);
+// interleaved: in pairs). Each thread owns one output row.
+template <bool IL = false>
 __device__ __forceinline__ void epilogue_subtile_store(uint32_t tbase, int width, int row,
                                                        int col0, const FusedArgs &args) {
     for (int c = 0; c < width; c += 32) {
         float g[32], v[32];
-        tmem_ld_gu(tbase, c, g, v, width);
+        tmem_ld_gu<IL>(tbase, c, g, v, width);
         store_y32_global(row, col0 + c, g, v, args);
     }
 }

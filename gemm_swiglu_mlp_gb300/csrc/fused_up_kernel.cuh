@@ -84,7 +84,11 @@ struct FusedCfg {
     static_assert(UMMA_N == kSlotCols, "workspace slot shape");
 };
 
-template <int STAGES, int BROWS, typename E>
+// IL: the packed weights are column-interleaved (even rows Gate, odd rows
+// Up, the pages' Kernel-2 pairing; pack_weights_il_kernel) instead of
+// 128-row blocked. Only the sub-tile weight boxes and the epilogue's TMEM
+// column addressing differ.
+template <int STAGES, int BROWS, typename E, bool IL = false>
 __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
     fused_up_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -158,7 +162,10 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
                     tma_prefetch_3d(&tmB, 0, 0, wtile);
                 } else {
                     const CUtensorMap *tmBn = (u.width == 64) ? &tmB64 : &tmB32;
-                    tma_prefetch_4d(tmBn, 0, u.sub * u.width, 0, wtile);
+                    if constexpr (IL)
+                        tma_prefetch_3d(tmBn, 0, 2 * u.width * u.sub, wtile);
+                    else
+                        tma_prefetch_4d(tmBn, 0, u.sub * u.width, 0, wtile);
                 }
             }
         }
@@ -209,13 +216,17 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
                         tma_load_3d(b_dst, &tmB, full_bar(stage), 0, 0, wtile);
                     } else {
                         // column sub-tile: its Gate rows, then the matching Up rows,
-                        // in one 4-D box (both halves of the packed tile)
+                        // in one 4-D box (both halves of the packed tile); with
+                        // interleaved weights its 2 * width rows are contiguous
                         const CUtensorMap *tmBn = (u.width == 64) ? &tmB64 : &tmB32;
                         mbar_arrive_expect_tx(full_bar(stage),
                                               args.a_tx_bytes + 2 * u.width * kRowBytes);
                         tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
                                     kb * E::kBK, mb * C::BM);
-                        tma_load_4d(b_dst, tmBn, full_bar(stage), 0, u.sub * u.width, 0, wtile);
+                        if constexpr (IL)
+                            tma_load_3d(b_dst, tmBn, full_bar(stage), 0, 2 * u.width * u.sub, wtile);
+                        else
+                            tma_load_4d(b_dst, tmBn, full_bar(stage), 0, u.sub * u.width, 0, wtile);
                     }
                     issued_mask |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -323,8 +334,8 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
             if (u.width != C::BN) {
                 // column sub-tile: straight from TMEM to global memory
                 if (rows_live)
-                    epilogue_subtile_store(tbase, u.width, row0 + lane, nb * C::BN + u.sub * u.width,
-                                           args);
+                    epilogue_subtile_store<IL>(tbase, u.width, row0 + lane,
+                                               nb * C::BN + u.sub * u.width, args);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -341,7 +352,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
                     if (lane == 0) bulk_wait_group_read0();  // last store has read ybuf
                     __syncwarp();
                     static_assert(C::BN == 128, "four 32-column chunks");
-                    epilogue_stage_tile(tbase, ybuf, lane, args.gate_scale, args.up_scale);
+                    epilogue_stage_tile<IL>(tbase, ybuf, lane, args.gate_scale, args.up_scale);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -355,7 +366,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
 #pragma unroll 1
                     for (int c = 0; c < C::BN; c += 32) {
                         float g[32], v[32];
-                        tmem_ld_gu(tbase, c, g, v);
+                        tmem_ld_gu<IL>(tbase, c, g, v);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             __stcg(slot + static_cast<size_t>(c + i) * args.slot_rows + row_in_tile,

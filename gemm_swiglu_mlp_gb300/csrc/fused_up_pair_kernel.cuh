@@ -91,7 +91,10 @@ struct PairCfg {
     static_assert(UMMA_N == kSlotCols, "workspace slot shape");
 };
 
-template <int STAGES, typename E, bool PLAIN = false>
+// IL: column-interleaved packed weights (see fused_up_kernel.cuh); a CTA's
+// half of a unit's weight rows is then the unit's first or second half of
+// its 2 * width packed rows.
+template <int STAGES, typename E, bool PLAIN = false, bool IL = false>
 __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     fused_up_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
@@ -99,7 +102,12 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                          const __grid_constant__ CUtensorMap tmB32,
                          const __grid_constant__ CUtensorMap tmY, const FusedArgs args) {
     using C = PairCfg<STAGES>;
-    static_assert(!PLAIN || !E::kFp8, "plain product: BF16 CTA pairs");
+    static_assert(!PLAIN || (!E::kFp8 && !IL), "plain product: BF16 CTA pairs, blocked weights");
+    // first packed row of this CTA's half of a unit's weight rows
+    auto brow0 = [](const Unit &u, uint32_t h) {
+        return IL ? 2 * u.width * u.sub + u.width * static_cast<int>(h)
+                  : C::BN * static_cast<int>(h) + u.sub * u.width;
+    };
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -177,8 +185,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
             const int kend = (u.kb1 - u.kb0 < kPrefetchStages) ? u.kb1 : u.kb0 + kPrefetchStages;
             for (int kb = u.kb0; kb < kend; ++kb) {
                 tma_prefetch_2d(&tmA, kb * E::kBK, tm * C::UMMA_M + C::BM * static_cast<int>(half));
-                tma_prefetch_3d(tmBu, 0, C::BN * static_cast<int>(half) + u.sub * u.width,
-                                nb * sched.k_blocks + kb);
+                tma_prefetch_3d(tmBu, 0, brow0(u, half), nb * sched.k_blocks + kb);
             }
         }
     }
@@ -238,8 +245,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                     const CUtensorMap *tmBu =
                         (brows == C::BN) ? &tmB : (brows == 64 ? &tmB64 : &tmB32);
                     tma_load_3d_pair(sbase + C::OFF_B + stage * C::B_BYTES, tmBu, bar, 0,
-                                     C::BN * static_cast<int>(half) + u.sub * brows,
-                                     nb * sched.k_blocks + kb);
+                                     brow0(u, half), nb * sched.k_blocks + kb);
                     issued_mask |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -356,11 +362,11 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
 #pragma unroll 1
                         for (int c = 0; c < 64; c += 32) {
                             float g[32], v[32];
-                            tmem_ld_gu(tbase, c, g, v, 64);
+                            tmem_ld_gu<IL>(tbase, c, g, v, 64);
                             stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
                         }
                     } else {
-                        epilogue_subtile_store(tbase, u.width, row0 + lane,
+                        epilogue_subtile_store<IL>(tbase, u.width, row0 + lane,
                                                nb * C::BN + u.sub * u.width, args);
                     }
                 }
@@ -388,7 +394,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                     } else {
                         if (lane == 0) bulk_wait_group_read0();
                         __syncwarp();
-                        epilogue_stage_tile(tbase, ybuf, lane, args.gate_scale, args.up_scale);
+                        epilogue_stage_tile<IL>(tbase, ybuf, lane, args.gate_scale, args.up_scale);
                     }
                 }
                 tc_fence_before();
@@ -422,7 +428,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
 #pragma unroll 1
                         for (int c = 0; c < C::BN; c += 32) {
                             float g[32], v[32];
-                            tmem_ld_gu(tbase, c, g, v);
+                            tmem_ld_gu<IL>(tbase, c, g, v);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
                                 __stcg(slot + static_cast<size_t>(c + i) * args.slot_rows +
@@ -528,7 +534,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
 #pragma unroll 1
                             for (int c = g0; c < g0 + G; c += 32) {
                                 float g[32], v[32];
-                                tmem_ld_gu(tbase, c, g, v);  // own part: first in k order
+                                tmem_ld_gu<IL>(tbase, c, g, v);  // own part: first in k order
                                 for (int q = 0; q < others; ++q) {
                                     const float *pg = ring + static_cast<size_t>(q) * 2u * G *
                                                                  args.slot_rows;

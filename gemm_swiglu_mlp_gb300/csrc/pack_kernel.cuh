@@ -52,6 +52,38 @@ __global__ void __launch_bounds__(256) pack_weights_kernel(const T *__restrict__
     }
 }
 
+// Column-interleaved packing, the pages' Kernel-2 pairing (technical
+// summary, "Kernel-2": the fused weight's even columns are Gate, odd columns
+// Up, so matching Gate and Up results sit side by side): the same
+// [NB][KB][256][64] tiles, with tile (j, b) row 2i = W1[64b..64b+63][128j + i]
+// and row 2i + 1 = W2[64b..64b+63][128j + i] (i < 128); zero outside N and
+// K. One 64-row chunk holds 32 output columns of both weights. A
+// permutation plus zero padding: bit-exact.
+__global__ void __launch_bounds__(256) pack_weights_il_kernel(const uint16_t *__restrict__ W1,
+                                                               const uint16_t *__restrict__ W2,
+                                                               uint16_t *__restrict__ Wp, int K,
+                                                               int N, int KB) {
+    __shared__ uint16_t tile[kPackTile][kPackTile + 2];
+    const int b = blockIdx.x;                // k-block
+    const int k0 = b * kPackTile;
+    const int p0 = blockIdx.y * kPackTile;   // first packed row (over all 2*Np rows)
+    const int j = p0 / 256;
+    const int r0 = p0 % 256;
+    const int n0 = 128 * j + r0 / 2;         // 32 output columns
+    for (int i = threadIdx.x; i < kPackTile * kPackTile; i += blockDim.x) {
+        const int kk = i / kPackTile, rr = i % kPackTile;
+        const int k = k0 + kk, n = n0 + rr / 2;
+        const uint16_t *__restrict__ W = (rr & 1) ? W2 : W1;
+        tile[kk][rr] = (k < K && n < N) ? W[static_cast<int64_t>(k) * N + n] : uint16_t(0);
+    }
+    __syncthreads();
+    uint16_t *__restrict__ out = Wp + ((static_cast<int64_t>(j) * KB + b) * 256 + r0) * kPackTile;
+    for (int i = threadIdx.x; i < kPackTile * kPackTile; i += blockDim.x) {
+        const int rr = i / kPackTile, kk = i % kPackTile;
+        out[rr * kPackTile + kk] = tile[kk][rr];
+    }
+}
+
 // Packing from nn.Linear-style weights: W1, W2 [N, K] row-major (each row is
 // one output column's K weights). The packed tile wants exactly such rows
 // (K-major), so this is a row gather: tile (j, b) row r < 128 is

@@ -126,6 +126,19 @@ int device_setup(int *dev_out, DeviceState **st_out) {
                                  FusedC::SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemE4M3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PairC::SMEM_BYTES) != cudaSuccess ||
+            // column-interleaved packed weights (BF16)
+            cudaFuncSetAttribute(fused_up_kernel<kFusedStages, 256, ElemBF16, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 FusedC::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_kernel<kNarrow64Stages, 128, ElemBF16, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Narrow64C::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_kernel<kNarrow32Stages, 64, ElemBF16, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Narrow32C::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairC::SMEM_BYTES) != cudaSuccess) {
             cudaGetLastError();
             st.status = SWIGLU_ERR_CUDA;
@@ -189,6 +202,16 @@ int schedule_mode() {
     return kSchedAuto;
 }
 
+// SWIGLU_GROUP_M=<rows> (ablation): token rows per group of the tile order
+// (a multiple of the kernel's tile height; default kGroupM * 128 = 2048);
+// read on every call. 0: the default.
+int group_rows_override() {
+    const char *v = std::getenv("SWIGLU_GROUP_M");
+    if (!v) return 0;
+    const long r = std::strtol(v, nullptr, 10);
+    return (r >= 128 && r <= (1L << 20)) ? static_cast<int>(r) : 0;
+}
+
 // Schedule for a kernel whose clusters hold `ctas` CTAs (1 or 2: tiles of
 // 128 or 256 rows), `workers` of them running at once.
 WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, int ctas, int kbk, int mode) {
@@ -198,7 +221,9 @@ WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, int ctas, int k
     const int k_blocks = static_cast<int>((K + kbk - 1) / kbk);
     // few token rows: the kernel streams weights (HBM-bound), see plan_schedule
     const bool weight_bound = M <= 128;
-    return plan_schedule(m_tiles, n_tiles, k_blocks, workers, kGroupM / ctas, kMinStreamKIters,
+    const int grows = group_rows_override();
+    const int group_m = grows ? std::max(1, grows / rows) : kGroupM / ctas;
+    return plan_schedule(m_tiles, n_tiles, k_blocks, workers, group_m, kMinStreamKIters,
                          weight_bound, mode);
 }
 
@@ -438,8 +463,8 @@ size_t workspace_bytes_impl(int64_t M, int64_t N, int64_t K) {
 
 // The fused forward for element type E (BF16, or FP8 E4M3 with per-tensor
 // scales folded into gate_scale / up_scale). A and Wpacked hold E elements;
-// Y is BF16.
-template <typename E>
+// Y is BF16. IL: Wpacked is column-interleaved (swiglu_pack_weights_interleaved).
+template <typename E, bool IL = false>
 int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t N, int64_t K,
                  float gate_scale, float up_scale, void *workspace, size_t workspace_bytes,
                  void *stream, size_t packed_bytes) {
@@ -485,11 +510,14 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
     if (!encode_2d(&tmA, A, K, M, E::kBK, a_rows, E::kFp8) ||
         !encode_packed_weights(&tmB, Wpacked, weight_tiles, pair ? 128u : 256u, E::kFp8) ||
         // sub-tile maps: the pair kernels load one half (Gate or Up) per CTA,
-        // the 1-SM kernel both halves in one 4-D box
+        // the 1-SM kernel both halves in one 4-D box (interleaved weights: the
+        // sub-tile's 2 * width contiguous rows in one 3-D box)
         !(pair ? encode_packed_weights(&tmB64, Wpacked, weight_tiles, 64u, E::kFp8)
-               : encode_packed_weight_halves(&tmB64, Wpacked, weight_tiles, 64u, E::kFp8)) ||
+               : IL ? encode_packed_weights(&tmB64, Wpacked, weight_tiles, 128u, E::kFp8)
+                    : encode_packed_weight_halves(&tmB64, Wpacked, weight_tiles, 64u, E::kFp8)) ||
         !(pair ? encode_packed_weights(&tmB32, Wpacked, weight_tiles, 32u, E::kFp8)
-               : encode_packed_weight_halves(&tmB32, Wpacked, weight_tiles, 32u, E::kFp8)) ||
+               : IL ? encode_packed_weights(&tmB32, Wpacked, weight_tiles, 64u, E::kFp8)
+                    : encode_packed_weight_halves(&tmB32, Wpacked, weight_tiles, 32u, E::kFp8)) ||
         !encode_2d(&tmY, Y, N, M, 64, 32))
         return SWIGLU_ERR_CUDA;
 
@@ -533,8 +561,8 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
         cfg.gridDim = dim3(static_cast<unsigned>(lp.ctas * sched.grid));
         cfg.blockDim = dim3(PairC::THREADS);
         cfg.dynamicSmemBytes = PairC::SMEM_BYTES;
-        err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages, E>, tmA, tmB, tmB64,
-                                 tmB32, tmY, args);
+        err = cudaLaunchKernelEx(&cfg, fused_up_pair_kernel<kPairStages, E, false, IL>, tmA, tmB,
+                                 tmB64, tmB32, tmY, args);
     } else {
         cfg.numAttrs = 1;
         cfg.gridDim = dim3(static_cast<unsigned>(sched.grid));
@@ -544,16 +572,16 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
         const bool all_sub = sched.n_split > 1 && sched.dp_tiles == 0 && sched.sk_iters == 0;
         if (all_sub && sched.n_split == 2) {
             cfg.dynamicSmemBytes = Narrow64C::SMEM_BYTES;
-            err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kNarrow64Stages, 128, E>, tmA, tmB,
+            err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kNarrow64Stages, 128, E, IL>, tmA, tmB,
                                      tmB64, tmB32, tmY, args);
         } else if (all_sub && sched.n_split == 4) {
             cfg.dynamicSmemBytes = Narrow32C::SMEM_BYTES;
-            err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kNarrow32Stages, 64, E>, tmA, tmB,
+            err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kNarrow32Stages, 64, E, IL>, tmA, tmB,
                                      tmB64, tmB32, tmY, args);
         } else {
             cfg.dynamicSmemBytes = FusedC::SMEM_BYTES;
-            err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kFusedStages, 256, E>, tmA, tmB, tmB64,
-                                     tmB32, tmY, args);
+            err = cudaLaunchKernelEx(&cfg, fused_up_kernel<kFusedStages, 256, E, IL>, tmA, tmB,
+                                     tmB64, tmB32, tmY, args);
         }
     }
     if (err != cudaSuccess) {
@@ -576,6 +604,30 @@ int swiglu_up_forward(const void *A, const void *Wpacked, void *Y, int64_t M, in
                       int64_t K, void *workspace, size_t workspace_bytes, void *stream) {
     return forward_impl<ElemBF16>(A, Wpacked, Y, M, N, K, 1.0f, 1.0f, workspace,
                                   workspace_bytes, stream, swiglu_packed_weight_bytes(N, K));
+}
+
+int swiglu_pack_weights_interleaved(const void *W1, const void *W2, int64_t K, int64_t N,
+                                    void *Wpacked, void *stream) {
+    dim3 grid;
+    int s = pack_checks(W1, W2, K, N, Wpacked, &grid);
+    if (s != SWIGLU_OK) return s;
+    int dev;
+    DeviceState *st;
+    s = device_setup(&dev, &st);
+    if (s != SWIGLU_OK) return s;
+    pack_weights_il_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(W1), static_cast<const uint16_t *>(W2),
+        static_cast<uint16_t *>(Wpacked), static_cast<int>(K), static_cast<int>(N),
+        static_cast<int>(grid.x));
+    if (cudaGetLastError() != cudaSuccess) return SWIGLU_ERR_CUDA;
+    return SWIGLU_OK;
+}
+
+int swiglu_up_forward_interleaved(const void *A, const void *Wpacked, void *Y, int64_t M,
+                                  int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+    return forward_impl<ElemBF16, true>(A, Wpacked, Y, M, N, K, 1.0f, 1.0f, workspace,
+                                        workspace_bytes, stream, swiglu_packed_weight_bytes(N, K));
 }
 
 size_t swiglu_packed_weight_bytes_fp8(int64_t N, int64_t K) {

@@ -134,7 +134,9 @@ size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * SWIGLU_SCHEDULE=dp|split|sk|sk-tail
  * (whole tiles, column sub-tiles in the last wave, split K over the last wave
  * and the remainder, or over the remainder only); swiglu_workspace_bytes
- * follows them too.
+ * follows them too. SWIGLU_GROUP_M=<rows> sets how many token rows the
+ * persistent tile order keeps together (default 2048) before it moves to
+ * the next output columns.
  * The first call on a device does one-time set-up (kernel attributes); after
  * it, calls may be captured into CUDA graphs and replayed.
  * Errors: SWIGLU_ERR_INVALID_ARG, SWIGLU_ERR_UNSUPPORTED (the current device
@@ -145,6 +147,37 @@ size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K);
 int swiglu_up_forward(const void *A, const void *Wpacked, void *Y,
                       int64_t M, int64_t N, int64_t K,
                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Column-interleaved packing: the pages' own Kernel-2 pairing (technical
+ * summary, "Kernel-2": the fused weight matrix takes Gate in its even and Up
+ * in its odd columns, so each Gate result sits next to its Up partner).
+ * Kept beside the default 128-row-blocked layout to measure the two against
+ * each other; the result is the same computation, bit for bit.
+ * ---------------------------------------------------------------------- */
+
+/*
+ * Packs W1 and W2 (device, BF16, [K, N] row-major each) into Wpacked
+ * (device, swiglu_packed_weight_bytes(N, K) bytes) column-interleaved:
+ * BF16 [NB][KB][256][64] as for swiglu_pack_weights, but tile (j, b) row 2i
+ * is W1[64b..64b+63, 128j+i] and row 2i+1 is W2[64b..64b+63, 128j+i]
+ * (i < 128); zero outside N and K. Valid only for
+ * swiglu_up_forward_interleaved. Requirements and errors as
+ * swiglu_pack_weights.
+ */
+int swiglu_pack_weights_interleaved(const void *W1, const void *W2, int64_t K, int64_t N,
+                                    void *Wpacked, void *stream);
+
+/*
+ * swiglu_up_forward on interleaved packed weights: the same kernels, tiles,
+ * schedule and workspace (sized by swiglu_workspace_bytes); the epilogue
+ * pairs accumulator columns 2i and 2i+1 instead of i and 128+i. Arguments,
+ * requirements and errors as swiglu_up_forward; Wpacked must come from
+ * swiglu_pack_weights_interleaved.
+ */
+int swiglu_up_forward_interleaved(const void *A, const void *Wpacked, void *Y,
+                                  int64_t M, int64_t N, int64_t K,
+                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Scratch size of swiglu_up_forward_noalloc, fixed at build time: 32 MiB.

@@ -149,6 +149,26 @@ def pack_reference(W1: np.ndarray, W2: np.ndarray) -> np.ndarray:
     return P.reshape(-1)
 
 
+def pack_reference_interleaved(W1: np.ndarray, W2: np.ndarray) -> np.ndarray:
+    """The column-interleaved packed layout (the pages' Kernel-2 pairing),
+    written out with numpy slicing: [NB][KB][256][64]; tile (j, b) row 2i =
+    W1[64b:64b+64, 128j+i], row 2i+1 = W2[64b:64b+64, 128j+i] (i < 128); zero
+    outside N and K. Flat uint16 array."""
+    K, N = W1.shape
+    NB, KB = -(-N // 128), -(-K // 64)
+    Np, Kp = NB * 128, KB * 64
+    w1 = np.zeros((Kp, Np), np.uint16)
+    w2 = np.zeros((Kp, Np), np.uint16)
+    w1[:K, :N] = W1
+    w2[:K, :N] = W2
+    P = np.zeros((NB, KB, 256, 64), np.uint16)
+    for j in range(NB):
+        for b in range(KB):
+            P[j, b, 0::2] = w1[64 * b:64 * b + 64, 128 * j:128 * j + 128].T
+            P[j, b, 1::2] = w2[64 * b:64 * b + 64, 128 * j:128 * j + 128].T
+    return P.reshape(-1)
+
+
 def unpack_reference(P: np.ndarray, K: int, N: int):
     """Inverse of pack_reference: (W1, W2) from the flat packed array."""
     NB, KB = -(-N // 128), -(-K // 64)

@@ -162,6 +162,28 @@ def test_pack_reference_layout_by_hand():
     assert np.array_equal(u1, A1) and np.array_equal(u2, A2)
 
 
+def test_interleaved_pack_reference_layout_by_hand():
+    # K=2, N=3: row 2i holds W1[:, i], row 2i+1 holds W2[:, i]
+    W1 = np.arange(6, dtype=np.uint16).reshape(2, 3)
+    W2 = (100 + np.arange(6, dtype=np.uint16)).reshape(2, 3)
+    P_ = parity.pack_reference_interleaved(W1, W2).reshape(256, 64)
+    assert P_[0, :2].tolist() == [0, 3] and P_[1, :2].tolist() == [100, 103]
+    assert P_[4, :2].tolist() == [2, 5] and P_[5, :2].tolist() == [102, 105]
+    assert not P_[:, 2:].any() and not P_[6:].any()
+    # W1[70, 130] sits in tile (j=1, b=1), row 2*2, column 6; W2's in row 5
+    K, N = 72, 136
+    A1 = np.arange(K * N, dtype=np.uint16).reshape(K, N)
+    A2 = A1 + np.uint16(1)
+    T = parity.pack_reference_interleaved(A1, A2).reshape(2, 2, 256, 64)
+    assert T[1, 1, 4, 6] == A1[70, 130] and T[1, 1, 5, 6] == A2[70, 130]
+    # the same values as the blocked layout, rows permuted within each tile
+    B = parity.pack_reference(A1, A2).reshape(2, 2, 256, 64)
+    perm = np.empty(256, np.int64)
+    perm[0::2] = np.arange(128)
+    perm[1::2] = 128 + np.arange(128)
+    assert np.array_equal(T, B[:, :, perm, :])
+
+
 def test_parity_criteria_by_hand():
     import workloads
     want = workloads.f32_to_bf16_bits(np.array([1.0, 0.0, 100.0, 1e-4], np.float32))

@@ -559,12 +559,20 @@ def ablation(sg, peaks, dev, stream, sampler, window_s: float, labels, forms=ABL
                     cs = torch.cuda.current_stream(dev)
                     for i in range(n):
                         one(i, cs)
+                # untimed half window first: the clock settles under this
+                # form's load before the timed window
+                replay_window([g], stream, dev, window_s / 2)
                 el, rounds, t0, t1 = replay_window([g], stream, dev, window_s)
                 sg.swiglu_check_device_status(stream)
                 f = {"layout": layout, "variant": variant, "schedule": mode,
                      "workspace_bytes": ws, "launches": n * rounds}
                 f.update(roofline_entry(w, peaks, "bf16", el / (n * rounds)))
-                f["sm_mhz"] = sampler.summary(t0, t1, min_samples=1).get("sm_mhz")
+                clk = sampler.summary(t0, t1, min_samples=1)
+                f["sm_mhz"] = clk.get("sm_mhz")
+                f["clock_samples"] = clk.get("samples")
+                if f["sm_mhz"]:
+                    # launch time x SM clock: comparable across power-capped clocks
+                    f["ms_x_ghz"] = f["us_per_launch"] * f["sm_mhz"] * 1e-6
                 entry["forms"].append(f)
                 del g, Wss
             for k, v in saved.items():

@@ -250,8 +250,10 @@ WorkSched plan_down(int64_t M, int64_t N, int64_t K, int workers) {
         const double eff = static_cast<double>(T) / (static_cast<double>(waves) * workers);
         mode = eff >= 0.9 ? kSchedDataParallel : (T >= workers ? kSchedStreamKTail : kSchedStreamK);
     }
-    return plan_schedule(m_tiles, n_tiles, k_blocks, workers, kGroupM / 2, kMinStreamKIters,
-                         false, mode);
+    const int grows = group_rows_override();
+    const int group_m = grows ? std::max(1, grows / rows) : kGroupM / 2;
+    return plan_schedule(m_tiles, n_tiles, k_blocks, workers, group_m, kMinStreamKIters, false,
+                         mode);
 }
 
 // Which kernel serves a call, and its schedule: the 1-SM kernel below 256

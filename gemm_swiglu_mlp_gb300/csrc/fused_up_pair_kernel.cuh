@@ -62,10 +62,7 @@
 
 namespace swiglu {
 
-// YSTAGE: the epilogue stages Y in shared memory and stores it with TMA
-// (a 32 KB buffer); without it, Y goes from registers straight to global
-// memory and the 32 KB go to one more pipeline stage instead.
-template <int STAGES, bool YSTAGE = true>
+template <int STAGES>
 struct PairCfg {
     static constexpr int BM = 128;                  // rows per CTA; the pair tile has 256
     static constexpr int BN = 128;                  // output columns per tile
@@ -78,7 +75,7 @@ struct PairCfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int EPI_WARPS = 4;
     static constexpr int Y_HALF_BYTES = 32 * 64 * 2;
-    static constexpr int Y_WARP_BYTES = YSTAGE ? 2 * Y_HALF_BYTES : 0;
+    static constexpr int Y_WARP_BYTES = 2 * Y_HALF_BYTES;
     static constexpr int TMEM_COLS = 2 * UMMA_N;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -97,16 +94,15 @@ struct PairCfg {
 // IL: column-interleaved packed weights (see fused_up_kernel.cuh); a CTA's
 // half of a unit's weight rows is then the unit's first or second half of
 // its 2 * width packed rows.
-template <int STAGES, typename E, bool PLAIN = false, bool IL = false, bool YSTAGE = true>
-__global__ void __launch_bounds__(PairCfg<STAGES, YSTAGE>::THREADS, 1)
+template <int STAGES, typename E, bool PLAIN = false, bool IL = false>
+__global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     fused_up_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmB64,
                          const __grid_constant__ CUtensorMap tmB32,
                          const __grid_constant__ CUtensorMap tmY, const FusedArgs args) {
-    using C = PairCfg<STAGES, YSTAGE>;
-    static_assert(!PLAIN || (!E::kFp8 && !IL && YSTAGE),
-                  "plain product: BF16 CTA pairs, blocked weights, staged output");
+    using C = PairCfg<STAGES>;
+    static_assert(!PLAIN || (!E::kFp8 && !IL), "plain product: BF16 CTA pairs, blocked weights");
     // first packed row of this CTA's half of a unit's weight rows
     auto brow0 = [](const Unit &u, uint32_t h) {
         return IL ? 2 * u.width * u.sub + u.width * static_cast<int>(h)
@@ -344,15 +340,13 @@ __global__ void __launch_bounds__(PairCfg<STAGES, YSTAGE>::THREADS, 1)
                 c_hi = sched.sk_owner(first + sched.k_blocks - 1);
             }
             const bool split = c_hi > c_lo;
-            bool store_y = !PLAIN && YSTAGE;   // a staged Y tile waits for its TMA store
+            bool store_y = !PLAIN;   // a staged Y tile waits for its TMA store
             // 32 summed columns of each accumulator half, at column c of the
-            // half (plain product, or no Y staging: straight to global memory)
+            // half (plain product: straight to global memory)
             auto emit32 = [&](int c, const float (&g)[32], const float (&v)[32]) {
                 if constexpr (PLAIN) {
                     store_plain32(row0 + lane, nb * C::UMMA_N + c, g, args);
                     store_plain32(row0 + lane, nb * C::UMMA_N + C::BN + c, v, args);
-                } else if constexpr (!YSTAGE) {
-                    store_y32_global(row0 + lane, nb * C::BN + c, g, v, args);
                 } else {
                     stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
                 }
@@ -362,7 +356,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, YSTAGE>::THREADS, 1)
                 // a 64-column sub-tile is one staged TMA box; a 32-column one
                 // (half a box) is stored from registers
                 if (rows_live) {
-                    if (u.width == 64 && YSTAGE) {
+                    if (u.width == 64) {
                         if (lane == 0) bulk_wait_group_read0();
                         __syncwarp();
 #pragma unroll 1
@@ -379,7 +373,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, YSTAGE>::THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(tempty_leader);
-                store_y = u.width == 64 && YSTAGE;
+                store_y = u.width == 64;
             } else if (!split) {
                 if (rows_live) {
                     static_assert(C::BN == 128, "four 32-column chunks");
@@ -397,12 +391,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES, YSTAGE>::THREADS, 1)
                                 bulk_commit_group();
                             }
                         }
-                    } else if constexpr (YSTAGE) {
+                    } else {
                         if (lane == 0) bulk_wait_group_read0();
                         __syncwarp();
                         epilogue_stage_tile<IL>(tbase, ybuf, lane, args.gate_scale, args.up_scale);
-                    } else {
-                        epilogue_subtile_store<IL>(tbase, C::BN, row0 + lane, nb * C::BN, args);
                     }
                 }
                 tc_fence_before();

@@ -100,26 +100,23 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     return mbar_wait(bar, parity, &never);
 }
 
-// Named barrier 1 over the NT threads of the epilogue warps only (the 1-SM
-// kernel has four epilogue warps, the CTA-pair kernel eight).
-template <int NT = 128>
+// Named barrier over the four epilogue warps only.
 __device__ __forceinline__ void epilogue_bar() {
-    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+    asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
-// Named barrier over the epilogue warps that also ANDs a predicate over
-// them: every epilogue thread gets the same answer, so all of the warps take
+// Named barrier over the four epilogue warps that also ANDs a predicate over
+// them: every epilogue thread gets the same answer, so all four warps take
 // the same branch afterwards (no warp can be left alone at a later barrier).
-template <int NT = 128>
 __device__ __forceinline__ bool epilogue_all(bool v) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "n"(NT)
+        : "r"(static_cast<uint32_t>(v))
         : "memory");
     return r != 0;
 }
@@ -231,33 +228,6 @@ __device__ __forceinline__ void epilogue_stage_tile(uint32_t tbase, uint32_t ybu
     }
 }
 
-// The same for NCHUNK 32-column chunks of output columns starting at tile
-// column c0, staged at columns 0, 32, ... of the warp's buffer (the CTA-pair
-// kernel's epilogue warps each own 64 of a tile's 128 columns).
-template <bool IL, int NCHUNK>
-__device__ __forceinline__ void epilogue_stage_cols(uint32_t tbase, int c0, uint32_t ybuf, int lane,
-                                                    float gs, float us) {
-    uint32_t gr[2][32], ur[2][32];
-    tmem_ld_pair_cols<IL>(tbase, c0, 128, gr[0], ur[0]);
-    tmem_ld_wait();
-    reg_fence32(gr[0]);
-    reg_fence32(ur[0]);
-#pragma unroll
-    for (int i = 0; i < NCHUNK; ++i) {
-        const int cur = i & 1;
-        if (i + 1 < NCHUNK)
-            tmem_ld_pair_cols<IL>(tbase, c0 + 32 * (i + 1), 128, gr[cur ^ 1], ur[cur ^ 1]);
-        float g[32], u[32];
-        split_gu<IL>(gr[cur], ur[cur], g, u);
-        stage_y32(ybuf, lane, 32 * i, g, u, gs, us);
-        if (i + 1 < NCHUNK) {
-            tmem_ld_wait();
-            reg_fence32(gr[cur ^ 1]);
-            reg_fence32(ur[cur ^ 1]);
-        }
-    }
-}
-
 // y for 32 consecutive columns [col, col+32) of one output row, from FP32
 // Gate and Up (times their scales), stored straight to global memory in
 // 16-byte pieces. Rows >= M and columns >= N are skipped; N is a multiple of
@@ -321,22 +291,6 @@ __device__ __forceinline__ void stage_bf16x32(uint32_t stg, int lane, int col,
 __device__ __forceinline__ void stage_plain_128(uint32_t tbase, uint32_t stg, int lane) {
 #pragma unroll 1
     for (int c = 0; c < 128; c += 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tbase + c, r);
-        tmem_ld_wait();
-        reg_fence32(r);
-        float x[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
-        stage_bf16x32(stg, lane, c, x);
-    }
-}
-
-// 64 accumulator columns [tcol, tcol+64) of this thread's row, rounded to
-// BF16 into one 64 x 32 box of the warp's staging buffer.
-__device__ __forceinline__ void stage_plain_64(uint32_t tbase, uint32_t stg, int lane) {
-#pragma unroll 1
-    for (int c = 0; c < 64; c += 32) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tbase + c, r);
         tmem_ld_wait();

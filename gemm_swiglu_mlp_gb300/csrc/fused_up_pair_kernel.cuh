@@ -73,13 +73,9 @@ struct PairCfg {
     static constexpr int A_BYTES = BM * BK * 2;     // 16 KB: this CTA's A rows
     static constexpr int B_BYTES = BN * BK * 2;     // 16 KB: this CTA's half of Gate|Up
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    // Epilogue: eight warps, two per TMEM lane quarter (a warp may read only
-    // the 32 TMEM lanes of its warp index mod 4), each owning 32 rows and one
-    // 64-column half of the tile's 128 output columns.
-    static constexpr int EPI_WARPS = 8;
-    static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-    static constexpr int EPI_COLS = BN / 2;                 // output columns per epilogue warp
-    static constexpr int Y_WARP_BYTES = 32 * 64 * 2;        // one 64-column x 32-row TMA box
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int Y_HALF_BYTES = 32 * 64 * 2;
+    static constexpr int Y_WARP_BYTES = 2 * Y_HALF_BYTES;
     static constexpr int TMEM_COLS = 2 * UMMA_N;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -315,13 +311,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
             }
         }
     } else {
-        const int quad = warp & 3;                 // TMEM lane quarter: rows 32 * quad ..
-        const int colh = (warp - 2) >> 2;          // which 64-column half of the tile
-        const int cw0 = C::EPI_COLS * colh;        // first tile column of this warp
+        const int quad = warp & 3;
         const int row_in_tile = 32 * quad + lane;  // row within this CTA's 128 rows
         const uint32_t ybuf = sbase + C::OFF_Y + (warp - 2) * C::Y_WARP_BYTES;
         const bool lead_thread = (warp == 2 && lane == 0);
-        constexpr int NT = C::EPI_THREADS;
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
@@ -331,7 +324,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
         while (it.next(u)) {
             int tm, nb;
             sched.order.coords(u.tile, tm, nb);
-            ok = epilogue_all<NT>(mbar_wait(tfull_bar(acc), acc_phase, abort_flag));
+            ok = epilogue_all(mbar_wait(tfull_bar(acc), acc_phase, abort_flag));
             if (!ok) break;
             tc_fence_after();
             const int row0 = tm * C::UMMA_M + C::BM * static_cast<int>(half) + 32 * quad;
@@ -347,23 +340,22 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                 c_hi = sched.sk_owner(first + sched.k_blocks - 1);
             }
             const bool split = c_hi > c_lo;
-            bool store_y = !PLAIN;   // a staged Y box waits for its TMA store
-            // 32 summed columns [c, c+32) of each accumulator half, c in this
-            // warp's columns (plain product: straight to global memory)
+            bool store_y = !PLAIN;   // a staged Y tile waits for its TMA store
+            // 32 summed columns of each accumulator half, at column c of the
+            // half (plain product: straight to global memory)
             auto emit32 = [&](int c, const float (&g)[32], const float (&v)[32]) {
                 if constexpr (PLAIN) {
                     store_plain32(row0 + lane, nb * C::UMMA_N + c, g, args);
                     store_plain32(row0 + lane, nb * C::UMMA_N + C::BN + c, v, args);
                 } else {
-                    stage_y32(ybuf, lane, c - cw0, g, v, args.gate_scale, args.up_scale);
+                    stage_y32(ybuf, lane, c, g, v, args.gate_scale, args.up_scale);
                 }
             };
 
             if (!PLAIN && u.width != C::BN) {
-                // column sub-tiles are done by the first column half's warps: a
-                // 64-column one as one staged TMA box, a 32-column one (half a
-                // box) from registers
-                if (rows_live && colh == 0) {
+                // a 64-column sub-tile is one staged TMA box; a 32-column one
+                // (half a box) is stored from registers
+                if (rows_live) {
                     if (u.width == 64) {
                         if (lane == 0) bulk_wait_group_read0();
                         __syncwarp();
@@ -375,36 +367,34 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                         }
                     } else {
                         epilogue_subtile_store<IL>(tbase, u.width, row0 + lane,
-                                                   nb * C::BN + u.sub * u.width, args);
+                                               nb * C::BN + u.sub * u.width, args);
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(tempty_leader);
-                store_y = u.width == 64 && colh == 0;
+                store_y = u.width == 64;
             } else if (!split) {
                 if (rows_live) {
-                    static_assert(C::BN == 128 && C::EPI_COLS == 64, "two 32-column chunks per warp");
+                    static_assert(C::BN == 128, "four 32-column chunks");
                     if constexpr (PLAIN) {
-                        // this warp's 128 of the 256 output columns, in two
-                        // passes of 64 through its staging box
+                        // two passes of 128 output columns through the staging buffer
                         for (int p = 0; p < 2; ++p) {
                             if (lane == 0) bulk_wait_group_read0();
                             __syncwarp();
-                            const int oc = 2 * C::EPI_COLS * colh + C::EPI_COLS * p;
-                            stage_plain_64(tbase + oc, ybuf, lane);
+                            stage_plain_128(tbase + 128 * p, ybuf, lane);
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                store_staged_boxes(&tmY, ybuf, nb * C::UMMA_N + oc, row0, 1, args.N);
+                                store_staged_boxes(&tmY, ybuf, nb * C::UMMA_N + 128 * p, row0, 2,
+                                                   args.N);
                                 bulk_commit_group();
                             }
                         }
                     } else {
                         if (lane == 0) bulk_wait_group_read0();
                         __syncwarp();
-                        epilogue_stage_cols<IL, 2>(tbase, cw0, ybuf, lane, args.gate_scale,
-                                                   args.up_scale);
+                        epilogue_stage_tile<IL>(tbase, ybuf, lane, args.gate_scale, args.up_scale);
                     }
                 }
                 tc_fence_before();
@@ -422,23 +412,21 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                 // column group width G (Gate and Up columns) whose partials of
                 // every other contributor fit in the operand ring at once
                 const uint32_t col_bytes = static_cast<uint32_t>(args.slot_rows) * 4u;
-                // (plain product: the ring's last 64 KB stage the owner's
-                // output, 8 KB per warp: its Gate-side and Up-side boxes)
-                constexpr uint32_t kPlainWarpStage = 2u * 32u * 64u * 2u;
-                constexpr uint32_t kPlainStage = PLAIN ? C::EPI_WARPS * kPlainWarpStage : 0u;
+                // (plain product: the ring's last 64 KB stage the owner's output)
+                constexpr uint32_t kPlainStage = PLAIN ? C::EPI_WARPS * 4u * 32u * 64u * 2u : 0u;
                 const uint32_t ring_bytes = STAGES * (C::A_BYTES + C::B_BYTES) - kPlainStage;
                 int G = 128;
                 while (G > 32 && static_cast<uint32_t>(others) * 2u * G * col_bytes > ring_bytes)
                     G >>= 1;
                 const bool staged = static_cast<uint32_t>(others) * 2u * G * col_bytes <= ring_bytes;
-                const uint32_t pstg = sbase + ring_bytes + (warp - 2) * kPlainWarpStage;
+                const uint32_t pstg = sbase + ring_bytes + (warp - 2) * (4u * 32u * 64u * 2u);
                 if (pair != c_lo || !staged) {
                     // a contributor (or an owner with too many partners to
                     // stage): this CTA's FP32 partial -> its workspace slot
                     float *slot = slot_of(pair);
                     if (rows_live) {
 #pragma unroll 1
-                        for (int c = cw0; c < cw0 + C::EPI_COLS; c += 32) {
+                        for (int c = 0; c < C::BN; c += 32) {
                             float g[32], v[32];
                             tmem_ld_gu<IL>(tbase, c, g, v);
 #pragma unroll
@@ -456,12 +444,12 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(tempty_leader);
                     __threadfence();
-                    epilogue_bar<NT>();
+                    epilogue_bar();
                     if (lead_thread) {
                         const unsigned int prev = atomicAdd(counter, 1u);
                         *last_flag = (prev == static_cast<unsigned int>(others)) ? 1 : 0;
                     }
-                    epilogue_bar<NT>();
+                    epilogue_bar();
                     const bool last = *last_flag != 0;
                     store_y = store_y && last;
                     if (last) {
@@ -472,7 +460,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                             if (lane == 0) bulk_wait_group_read0();
                             __syncwarp();
 #pragma unroll 1
-                            for (int c = cw0; c < cw0 + C::EPI_COLS; c += 32) {
+                            for (int c = 0; c < C::BN; c += 32) {
                                 float g[32], v[32];
 #pragma unroll
                                 for (int i = 0; i < 32; ++i) {
@@ -508,7 +496,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                         got = wait_counter_geq(counter, static_cast<unsigned int>(others));
                         fence_proxy_async_global();
                     }
-                    ok = epilogue_all<NT>(got);
+                    ok = epilogue_all(got);
                     if (!ok) {
                         if (lead_thread && !*abort_flag) {
                             atomicOr(&g_status_word, kStatusEpilogueTimeout);
@@ -524,7 +512,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                     uint32_t fix_phase = 0;
 #pragma unroll 1
                     for (int g0 = 0; g0 < C::BN; g0 += G) {
-                        epilogue_bar<NT>();  // everyone is done reading the ring
+                        epilogue_bar();  // everyone is done reading the ring
                         if (lead_thread) {
                             mbar_arrive_expect_tx(fix_bar, static_cast<uint32_t>(others) * 2u *
                                                                part_bytes);
@@ -538,16 +526,13 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                                               part_bytes, fix_bar);
                             }
                         }
-                        ok = epilogue_all<NT>(mbar_wait(fix_bar, fix_phase, abort_flag));
+                        ok = epilogue_all(mbar_wait(fix_bar, fix_phase, abort_flag));
                         fix_phase ^= 1u;
                         if (!ok) break;
-                        // this warp's columns within the group
-                        const int ca = g0 > cw0 ? g0 : cw0;
-                        const int cb = (g0 + G < cw0 + C::EPI_COLS) ? g0 + G : cw0 + C::EPI_COLS;
                         if (rows_live) {
                             const float *ring = reinterpret_cast<const float *>(smem);
 #pragma unroll 1
-                            for (int c = ca; c < cb; c += 32) {
+                            for (int c = g0; c < g0 + G; c += 32) {
                                 float g[32], v[32];
                                 tmem_ld_gu<IL>(tbase, c, g, v);  // own part: first in k order
                                 for (int q = 0; q < others; ++q) {
@@ -563,8 +548,8 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                                     }
                                 }
                                 if constexpr (PLAIN) {
-                                    stage_bf16x32(pstg, lane, c - cw0, g);
-                                    stage_bf16x32(pstg, lane, C::EPI_COLS + c - cw0, v);
+                                    stage_bf16x32(pstg, lane, c, g);
+                                    stage_bf16x32(pstg, lane, C::BN + c, v);
                                 } else {
                                     emit32(c, g, v);
                                 }
@@ -583,10 +568,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                // Gate-side box: output columns cw0 ..; Up-side: BN + cw0 ..
-                                store_staged_boxes(&tmY, pstg, nb * C::UMMA_N + cw0, row0, 1, args.N);
-                                store_staged_boxes(&tmY, pstg + 32u * 64u * 2u,
-                                                   nb * C::UMMA_N + C::BN + cw0, row0, 1, args.N);
+                                store_staged_boxes(&tmY, pstg, nb * C::UMMA_N, row0, 4, args.N);
                                 bulk_commit_group();
                             }
                         }
@@ -601,10 +583,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    // whole tile: this warp's 64-column half; 64-column sub-tile:
-                    // the whole sub-tile (first column half's warps only)
-                    const int x0 = nb * C::BN + (u.width == C::BN ? cw0 : u.sub * u.width);
+                    const int x0 = nb * C::BN + u.sub * u.width;   // whole tiles: sub = 0
                     if (x0 < args.N) tma_store_2d(&tmY, ybuf, x0, row0);
+                    if (u.width == C::BN && x0 + 64 < args.N)
+                        tma_store_2d(&tmY, ybuf + C::Y_HALF_BYTES, x0 + 64, row0);
                     bulk_commit_group();
                 }
             }

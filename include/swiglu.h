@@ -124,6 +124,13 @@ size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *            8.2 us), so the interface keeps a caller-owned workspace, and
  *            swiglu_up_forward_noalloc below serves callers that cannot
  *            provide one.
+ *            A split tile on CTA pairs is finished by one pair, which waits
+ *            (bounded) for the others' partial sums. The pairs of such a
+ *            launch are numbered by the order in which they start (a
+ *            ticket counter in the workspace, back at its starting value
+ *            after every launch), so a pair only ever waits for pairs that
+ *            are already running: the call completes even while other
+ *            kernels occupy part of the GPU.
  * Requirements: M >= 1, N >= 8, K >= 8, N % 8 == 0, K % 8 == 0 (16-byte row
  * strides), M, N, K < 2^31; A, Wpacked, Y 16-byte aligned; Y must not overlap
  * A, Wpacked or the workspace. M, N and K need not be multiples of any tile

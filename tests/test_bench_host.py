@@ -54,3 +54,38 @@ def test_reference_arm_prints_one_contract_line(monkeypatch, capsys):
     assert r["value"] > 0 and r["cpu_baseline"]["kind"] == "oracle"
     assert r["e2e"]["h2d_bytes_per_step"] == 0 and r["gpu_launches"] == 0
     assert r["config"]["M"] == 128 and r["config"]["N"] == 4864 and r["config"]["K"] == 896
+
+
+def test_roofline_entry_by_hand():
+    peaks = {"hbm_gbs": 5000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0}
+    big = workloads.BY_LABEL["11"]                  # tensor-bound
+    t = big.flops / 1000e12                         # a launch at 1000 TFLOP/s
+    e = bench.roofline_entry(big, peaks, "bf16", t)
+    assert e["bound"] == "tensor"
+    assert abs(e["tflops"] - 1000.0) < 1e-6 and abs(e["frac"] - 0.5) < 1e-9
+    assert abs(e["frac_of_sustained"] - 1000.0 / 1600.0) < 1e-9
+    assert abs(e["frac_of_roofline_time"] - (big.flops / 2000e12) / t) < 1e-9
+    small = workloads.BY_LABEL["2"]                 # M=1: weight streaming
+    t = small.roofline_bytes / 2500e9               # 2500 GB/s
+    e = bench.roofline_entry(small, peaks, "bf16", t)
+    assert e["bound"] == "hbm" and abs(e["achieved_gbs"] - 2500.0) < 1e-6
+    assert abs(e["frac"] - 0.5) < 1e-9 and "frac_of_sustained" not in e
+
+
+def test_graph_launches_rounds_to_the_rotation():
+    # about 2 ms of launches per graph, a multiple of R, capped at 256
+    assert bench.graph_launches(3, 1e-3) == 3            # 2 launches -> one rotation
+    assert bench.graph_launches(2, 8e-6) == 250          # 250 = 2 ms / 8 us
+    assert bench.graph_launches(3, 8e-6) == 252          # rounded up to a multiple of 3
+    assert bench.graph_launches(2, 1e-6) == 256          # capped
+    assert bench.graph_launches(3, 1e-6) == 255
+    assert bench.graph_launches(2, 5e-3) == 2
+
+
+def test_every_workload_is_in_the_sweep_labels():
+    labels = [w.c for w in workloads.WORKLOADS]
+    assert len(labels) == 13 and len(set(labels)) == 13
+    assert bench.DEFAULT_WORKLOAD == "11"
+    w = workloads.BY_LABEL[bench.DEFAULT_WORKLOAD]
+    assert (w.M, w.K, w.N) == (8192, 8192, 29568)      # the largest single-GPU config
+    assert max(workloads.WORKLOADS, key=lambda x: x.flops) is w

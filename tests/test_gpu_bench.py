@@ -61,3 +61,42 @@ def test_bench_prints_one_contract_line(dtype):
         assert e["us_per_launch"] > 0 and 0 < e["frac"] < 1.5, e
         assert e["tflops"] == pytest.approx(w.flops / (e["us_per_launch"] * 1e-6) / 1e12)
         assert e["bound"] == ("hbm" if w.M <= 128 else "tensor"), e
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_column_split_ranks_reassemble_the_whole_forward(world, monkeypatch):
+    """What each rank of `bench.py --split columns` runs, done here for every
+    rank in turn on one GPU: its slice of W1/W2's columns packed and run
+    through the public forward. Side by side, the slices are exactly the
+    whole forward's Y (columns of Y are independent; whole tiles are forced
+    so that every element is summed over k in the same order)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    monkeypatch.setenv("SWIGLU_SCHEDULE", "dp")
+    import numpy as np
+
+    import bench
+    import workloads
+    from gemm_swiglu_mlp_gb300 import build
+    build.build()
+    import gemm_swiglu_mlp_gb300 as sg
+    from tests.parity import from_device_bf16, to_device_bf16
+    M, K, N = 520, 512, 1000
+    w = workloads.Workload("t", "column-split-test", M, K, N)
+    inputs = workloads.random_case(M, N, K, seed=55)
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.current_stream(dev)
+    A, W1, W2 = inputs
+    whole = from_device_bf16(sg.swiglu_up_forward(
+        to_device_bf16(A, dev),
+        sg.swiglu_pack_weights(to_device_bf16(W1, dev), to_device_bf16(W2, dev)), N))
+    parts = []
+    for rank in range(world):
+        c0, c1 = bench.column_slice(N, world, rank)
+        p = bench.pack_problem(sg, w, "bf16", dev, inputs, split=(c0, c1))
+        assert p.N == c1 - c0
+        p.forward(0, st)
+        torch.cuda.synchronize()
+        parts.append(from_device_bf16(p.Ys[0]))
+    sg.swiglu_check_device_status()
+    assert np.array_equal(np.concatenate(parts, axis=1), whole)

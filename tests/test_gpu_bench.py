@@ -100,3 +100,26 @@ def test_column_split_ranks_reassemble_the_whole_forward(world, monkeypatch):
         parts.append(from_device_bf16(p.Ys[0]))
     sg.swiglu_check_device_status()
     assert np.array_equal(np.concatenate(parts, axis=1), whole)
+
+
+def test_ablation_mode_prints_every_form():
+    """`bench.py --ablation` on one workload: one JSON line with every packed
+    layout x kernel x schedule form, each with its time, roofline fraction
+    and fusion efficiency against the unfused cuBLAS path."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bench
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--ablation", "--ablation-workloads",
+           "0", "--sweep-window-s", "0.02"]
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    r = json.loads(lines[0])
+    (e,) = r["ablation"]
+    assert (e["M"], e["K"], e["N"]) == (128, 896, 4864) and e["unfused_us"] > 0
+    forms = {(f["layout"], f["variant"], f["schedule"]) for f in e["forms"]}
+    assert forms == set(bench.ABLATION_FORMS)
+    for f in e["forms"]:
+        assert f["us_per_launch"] > 0 and f["bound"] == "hbm" and "fusion_efficiency" in f
+        assert (f["workspace_bytes"] > 0) == (f["schedule"] in ("sk", "sk-tail")), f

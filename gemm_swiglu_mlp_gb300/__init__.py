@@ -260,8 +260,7 @@ def _forward(entry: str, A, Wpacked, N, Y, workspace, stream) -> torch.Tensor:
         prev = torch.cuda.current_device()
         torch.cuda.set_device(dev)
     try:
-        key = (dev, M, N, K, os.environ.get("SWIGLU_FUSED_VARIANT"),
-               os.environ.get("SWIGLU_SCHEDULE"))
+        key = _plan_key(entry, dev, M, N, K)
         ws_need = _ws_bytes.get(key)
         if ws_need is None:
             ws_need = _ws_bytes[key] = swiglu_workspace_bytes(M, N, K)
@@ -317,11 +316,20 @@ def swiglu_up_forward_noalloc(A: torch.Tensor, Wpacked: torch.Tensor, N: int,
     return Y
 
 
+_PLAN_SWITCHES = ("SWIGLU_FUSED_VARIANT", "SWIGLU_SCHEDULE", "SWIGLU_DYNAMIC_TILES",
+                  "SWIGLU_GROUP_M")
+
+
+def _plan_key(*head):
+    """Cache key of a workspace size: the problem and every environment
+    switch that can change the library's plan for it."""
+    return tuple(head) + tuple(os.environ.get(k) for k in _PLAN_SWITCHES)
+
+
 def _workspace_args(kind: str, fn, dev: int, M: int, N: int, K: int, device, workspace, stream):
     """(pointer, bytes) of the workspace for one call: the caller's, or this
     module's per-(device, stream) default, sized by the library's own query."""
-    key = (kind, dev, M, N, K, os.environ.get("SWIGLU_FUSED_VARIANT"),
-           os.environ.get("SWIGLU_SCHEDULE"))
+    key = _plan_key(kind, dev, M, N, K)
     need = _ws_bytes.get(key)
     if need is None:
         need = _ws_bytes[key] = int(fn(M, N, K))

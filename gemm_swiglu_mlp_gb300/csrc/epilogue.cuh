@@ -78,6 +78,8 @@ struct FusedArgs {
     float *partials;          // 2 * grid slots of kSlotCols * slot_rows floats (stream-K only)
     unsigned int *counters;   // one per stream-K tile, zero between launches
     int ticket_index;         // counters[ticket_index]: start-order tickets of a K-split pair launch
+    int dyn_tiles;            // 1: tiles past the first wave are handed out at run time (pair kernel)
+    int tile_counter_index;   // counters[i]: next dynamic tile; counters[i + 1]: pairs finished
 #ifdef SWIGLU_TEST_FAULT_INJECTION
     int skip_first_fill;      // test build only: never fill the first pipeline stage
 #endif

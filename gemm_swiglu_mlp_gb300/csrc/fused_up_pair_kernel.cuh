@@ -32,6 +32,23 @@
 // it, and they finish their parts of the tile first (their range starts in
 // it).
 //
+// Dynamic tiles: in a launch of whole tiles only and at least two waves,
+// the pairs drift apart in time (some SMs are a few percent slower than
+// others, so over ~100 tiles the spread grows past three tile durations):
+// pairs that should share a weight tile in L2 then fetch it from DRAM at
+// different times, and the fast pairs idle at the end. Such a launch hands
+// out the tiles past the first wave at run time: the leader CTA's producer of
+// each pair takes the next tile index from a counter in the workspace
+// (atomicAdd) when it starts loading its previous tile, and publishes it in
+// a small ring of tile indices in both CTAs' shared memory, which the MMA
+// issuer, both CTAs' epilogue warps and the peer's producer read (tile-full
+// and tile-empty mbarriers per ring slot; the index -1 ends the sequence).
+// The tiles in flight are then always the lowest-numbered ones left, a
+// compact window of the tile order, and every pair works until the tiles
+// run out. Each tile is still computed whole by one pair in k order, so the
+// result is bit-identical to the static order. The last pair to finish
+// resets the counter for the next launch.
+//
 // Co-residency: an owner c_lo waits for pairs c_lo+1..c_hi, so those must be
 // running, or done, while it waits. A launch with a K split therefore numbers
 // its pairs by the order in which they start, not by cluster index: each
@@ -62,6 +79,8 @@
 
 namespace swiglu {
 
+constexpr int kTileRing = 8;   // slots of the dynamic tile ring
+
 template <int STAGES>
 struct PairCfg {
     static constexpr int BM = 128;                  // rows per CTA; the pair tile has 256
@@ -81,10 +100,15 @@ struct PairCfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_Y = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_BAR = OFF_Y + EPI_WARPS * Y_WARP_BYTES;
-    // full, empty, tfull x2, tempty x2, drain, fixup (split-tile partials)
-    static constexpr int NUM_BARS = 2 * STAGES + 6;
+    // full, empty, tfull x2, tempty x2, drain, fixup (split-tile partials),
+    // tile-ring full, tile-ring empty
+    static constexpr int NUM_BARS = 2 * STAGES + 6 + 2 * kTileRing;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int OFF_RING = OFF_MISC + 16;           // kTileRing tile indices
+    static constexpr int SMEM_BYTES = OFF_RING + 4 * kTileRing + 1024;
+    // readers of a ring slot: the MMA issuer, the peer's producer and both
+    // CTAs' epilogue warps, all arriving on the leader's tile-empty barrier
+    static constexpr int RING_READERS = 2 + 2 * EPI_WARPS;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static_assert(TMEM_COLS == 512, "two 256-column accumulator stages fill TMEM");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -129,6 +153,23 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     auto tempty_bar = [&](int a) { return sbase + C::OFF_BAR + 8u * (2 * STAGES + 2 + a); };
     const uint32_t drain_bar = sbase + C::OFF_BAR + 8u * (2 * STAGES + 4);
     const uint32_t fix_bar = sbase + C::OFF_BAR + 8u * (2 * STAGES + 5);
+    auto rfull_bar = [&](int i) { return sbase + C::OFF_BAR + 8u * (2 * STAGES + 6 + i); };
+    auto rempty_bar = [&](int i) {
+        return sbase + C::OFF_BAR + 8u * (2 * STAGES + 6 + kTileRing + i);
+    };
+    volatile int *ring = reinterpret_cast<volatile int *>(smem + C::OFF_RING);
+    const bool dyn = args.dyn_tiles != 0;   // the same in every CTA
+    // a whole tile of the data-parallel schedule
+    auto dp_unit = [&](int t) {
+        Unit u;
+        u.tile = t;
+        u.kb0 = 0;
+        u.kb1 = args.sched.k_blocks;
+        u.sk = -1;
+        u.width = C::BN;
+        u.sub = 0;
+        return u;
+    };
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     volatile int *last_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);
@@ -150,6 +191,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
         }
         mbar_init(drain_bar, 1);
         mbar_init(fix_bar, 1);
+        for (int i = 0; i < kTileRing; ++i) {
+            mbar_init(rfull_bar(i), 1);
+            mbar_init(rempty_bar(i), C::RING_READERS);
+        }
         *abort_flag = 0;
         *last_flag = 0;
         fence_barrier_init();
@@ -211,17 +256,13 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            UnitIter it;
-            it.init(sched, pair);
-            Unit u;
-            while (ok && it.next(u)) {
+            // issue the loads of every k-block of one unit; false if a wait
+            // for a free stage ran out or the launch is aborting
+            auto load_unit = [&](const Unit &u) -> bool {
                 int tm, nb;
                 sched.order.coords(u.tile, tm, nb);
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) return false;
 #ifdef SWIGLU_TEST_FAULT_INJECTION
                     // test build: the leader never arms or fills the first
                     // stage, so the MMA wait for it runs out
@@ -253,10 +294,74 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
                         phase ^= 1u;
                     }
                 }
+                return true;
+            };
+            if (!dyn) {
+                UnitIter it;
+                it.init(sched, pair);
+                Unit u;
+                while (ok && it.next(u)) ok = load_unit(u);
+            } else if (is_leader) {
+                // the pair's tile sequence: its first-wave tile, then whatever
+                // the counter hands out, published in the ring (-1 ends it)
+                unsigned int *next_tile = args.counters + args.tile_counter_index;
+                int t = pair, slot = 0;
+                uint32_t rph = 0;
+                while (ok) {
+                    const int pub = t < sched.num_tiles ? t : -1;
+                    if (!mbar_wait_cluster(rempty_bar(slot), rph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ring[slot] = pub;
+                    st_cluster_u32(mapa_shared(sbase + C::OFF_RING + 4u * slot, 1u),
+                                   static_cast<uint32_t>(pub));
+                    mbar_arrive(rfull_bar(slot));
+                    mbar_arrive_cluster(mapa_shared(rfull_bar(slot), 1u));
+                    if (++slot == kTileRing) {
+                        slot = 0;
+                        rph ^= 1u;
+                    }
+                    if (pub < 0) break;
+                    // the next tile's ticket is in flight while this tile's
+                    // loads go out
+                    const unsigned int ticket = atomicAdd(next_tile, 1u);
+                    ok = load_unit(dp_unit(t));
+                    t = sched.grid + static_cast<int>(ticket);
+                }
+            } else {
+                // the peer loads its half of the tiles its leader publishes
+                int slot = 0;
+                uint32_t rph = 0;
+                while (ok) {
+                    if (!mbar_wait_cluster(rfull_bar(slot), rph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int t = ring[slot];
+                    mbar_arrive_cluster(mapa_shared(rempty_bar(slot), leader_rank));
+                    if (++slot == kTileRing) {
+                        slot = 0;
+                        rph ^= 1u;
+                    }
+                    if (t < 0) break;
+                    ok = load_unit(dp_unit(t));
+                }
             }
             if (!ok && !*abort_flag) {
                 atomicOr(&g_status_word, kStatusProducerTimeout);
                 set_abort_both();
+            }
+            if (dyn && is_leader) {
+                // this pair takes no more tiles; the last pair to get here
+                // resets the counter pair for the next launch
+                __threadfence();
+                unsigned int *ctr = args.counters + args.tile_counter_index;
+                if (atomicAdd(ctr + 1, 1u) == static_cast<unsigned int>(sched.grid - 1)) {
+                    __threadfence();
+                    ctr[0] = 0u;
+                    ctr[1] = 0u;
+                }
             }
         }
     } else if (warp == 1) {
@@ -270,7 +375,28 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
             UnitIter it;
             it.init(sched, pair);
             Unit u;
-            while (ok && it.next(u)) {
+            int rslot = 0;
+            uint32_t rph = 0;
+            // the next unit: static schedule, or the leader's tile ring
+            auto next_unit = [&](Unit &nu) -> int {
+                if (!dyn) return it.next(nu) ? 1 : 0;
+                if (!mbar_wait(rfull_bar(rslot), rph, abort_flag)) return -1;
+                const int t = ring[rslot];
+                mbar_arrive(rempty_bar(rslot));
+                if (++rslot == kTileRing) {
+                    rslot = 0;
+                    rph ^= 1u;
+                }
+                if (t < 0) return 0;
+                nu = dp_unit(t);
+                return 1;
+            };
+            while (ok) {
+                const int got = next_unit(u);
+                if (got <= 0) {
+                    ok = got == 0;
+                    break;
+                }
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
                     ok = false;
                     break;
@@ -321,7 +447,30 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
         UnitIter it;
         it.init(sched, pair);
         Unit u;
-        while (it.next(u)) {
+        int rslot = 0;
+        uint32_t rph = 0;
+        // the next unit: static schedule, or the leader's tile ring (every
+        // epilogue warp reads the slot; each warp counts once as a reader)
+        auto next_unit = [&](Unit &nu) -> int {
+            if (!dyn) return it.next(nu) ? 1 : 0;
+            if (!epilogue_all(mbar_wait_cluster(rfull_bar(rslot), rph, abort_flag))) return -1;
+            const int t = ring[rslot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(rempty_bar(rslot), leader_rank));
+            if (++rslot == kTileRing) {
+                rslot = 0;
+                rph ^= 1u;
+            }
+            if (t < 0) return 0;
+            nu = dp_unit(t);
+            return 1;
+        };
+        while (true) {
+            const int got = next_unit(u);
+            if (got <= 0) {
+                ok = got == 0;
+                break;
+            }
             int tm, nb;
             sched.order.coords(u.tile, tm, nb);
             ok = epilogue_all(mbar_wait(tfull_bar(acc), acc_phase, abort_flag));

@@ -51,6 +51,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with acquire semantics at cluster scope: for a barrier whose
+// completing arrive came from another CTA of the cluster with release.cluster
+// semantics (data that CTA wrote before arriving is then visible here).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits until the phase with the given parity has completed. Returns false if
 // `abort_flag` (shared memory, set by another role that gave up) becomes
 // non-zero or the wait exceeds kWaitLimitCycles.
@@ -60,6 +75,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitLimitCycles) return false;
+    }
+}
+
+// The same, acquiring at cluster scope (see mbar_try_wait_cluster).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  const volatile int *abort_flag) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitLimitCycles) return false;
     }

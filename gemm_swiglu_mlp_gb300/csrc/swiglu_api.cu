@@ -273,11 +273,26 @@ LaunchPlan choose_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_cluste
 // the device (so a counter never lands where another shape's call left
 // partial sums), then the partial slots. Every stream-K tile needs at most
 // one counter per CTA half, and there are fewer than 2 * grid stream-K
-// tiles, so 4 * sm_count counters always suffice; one more, after them, is
-// the CTA-pair kernel's start-order ticket counter.
+// tiles, so 4 * sm_count counters always suffice; after them come the
+// CTA-pair kernel's start-order ticket counter and its dynamic-tile counter
+// pair (next tile, pairs finished).
 int ticket_index(int sm_count) { return 4 * sm_count; }
+int tile_counter_index(int sm_count) { return 4 * sm_count + 1; }
 size_t counter_region_bytes(int sm_count) {
-    return (static_cast<size_t>(4 * sm_count + 1) * sizeof(unsigned int) + 255) / 256 * 256;
+    return (static_cast<size_t>(4 * sm_count + 3) * sizeof(unsigned int) + 255) / 256 * 256;
+}
+
+// SWIGLU_DYNAMIC_TILES=0 keeps the static tile order everywhere (ablation);
+// read on every call.
+bool dynamic_tiles_allowed() {
+    const char *v = std::getenv("SWIGLU_DYNAMIC_TILES");
+    return !(v && std::strcmp(v, "0") == 0);
+}
+// Whether a CTA-pair launch hands out its tiles at run time: whole tiles
+// only, at least two waves of them.
+bool dynamic_tiles(const WorkSched &s, bool pair) {
+    return pair && s.sk_iters == 0 && s.n_split == 1 && s.num_tiles >= 2 * s.grid &&
+           dynamic_tiles_allowed();
 }
 // Partial slots: 2 per worker (its first and last stream-K tile), and for
 // the 2-SM kernel one per CTA of the pair.
@@ -287,7 +302,7 @@ size_t workspace_partials_bytes(const WorkSched &s, int64_t M, bool pair) {
                           : 0;
 }
 size_t workspace_bytes_for(const WorkSched &s, int64_t M, bool pair, int sm_count) {
-    if (s.sk_iters == 0) return 0;
+    if (s.sk_iters == 0) return dynamic_tiles(s, pair) ? counter_region_bytes(sm_count) : 0;
     return counter_region_bytes(sm_count) + workspace_partials_bytes(s, M, pair);
 }
 
@@ -523,7 +538,7 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
         !encode_2d(&tmY, Y, N, M, 64, 32))
         return SWIGLU_ERR_CUDA;
 
-    FusedArgs args;
+    FusedArgs args{};
     args.M = static_cast<int>(M);
     args.N = static_cast<int>(N);
     args.K = static_cast<int>(K);
@@ -542,6 +557,8 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
                                                         counter_region_bytes(st->sm_count))
                             : nullptr;
     args.ticket_index = ticket_index(st->sm_count);
+    args.tile_counter_index = tile_counter_index(st->sm_count);
+    args.dyn_tiles = dynamic_tiles(sched, pair) ? 1 : 0;
 
     // Both kernels are launched with programmatic stream serialization: a
     // launch may begin while the previous kernel in the stream finishes; the
@@ -745,7 +762,7 @@ int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M,
         !encode_2d(&tmOut, out, K, M, 64, 32))
         return SWIGLU_ERR_CUDA;
 
-    FusedArgs args;
+    FusedArgs args{};
     args.M = static_cast<int>(M);
     args.N = static_cast<int>(K);   // output columns
     args.K = static_cast<int>(N);   // reduction
@@ -764,6 +781,8 @@ int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M,
                                                         counter_region_bytes(st->sm_count))
                             : nullptr;
     args.ticket_index = ticket_index(st->sm_count);
+    args.tile_counter_index = tile_counter_index(st->sm_count);
+    args.dyn_tiles = dynamic_tiles(sched, true) ? 1 : 0;
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];

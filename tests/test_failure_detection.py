@@ -237,3 +237,45 @@ def test_split_tiles_finish_while_other_work_holds_sms(fi_lib, monkeypatch, kind
     assert still_busy
     r = compare(from_device_bf16(out), want)
     assert r["mismatches"] == 0 and r["over_bound"] == 0, r
+
+
+def test_dynamic_tile_counter_survives_a_timeout(fi_lib, monkeypatch):
+    """A whole-tile launch of several waves on CTA pairs hands out tiles from
+    a counter in the workspace. After a launch that times out, the same
+    workspace (not zeroed again) must serve the next launch correctly: every
+    pair counts itself out on its way through teardown, and the last one
+    resets the counter."""
+    monkeypatch.setenv("SWIGLU_FUSED_VARIANT", "2sm")
+    import oracle
+    M, N, K = 2048, 2432, 128
+    A, W1, W2 = workloads.random_case(M, N, K, seed=83)
+    Ad = to_device_bf16(A, "cuda")
+    W1d, W2d = to_device_bf16(W1, "cuda"), to_device_bf16(W2, "cuda")
+    Wp = torch.empty(fi_lib.swiglu_packed_weight_bytes(N, K), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert fi_lib.swiglu_pack_weights(W1d.data_ptr(), W2d.data_ptr(), K, N, Wp.data_ptr(),
+                                      stream) == 0
+    ws_bytes = fi_lib.swiglu_workspace_bytes(M, N, K)
+    assert ws_bytes > 0                                       # the tile counters
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+
+    def run():
+        Y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+        assert fi_lib.swiglu_up_forward(Ad.data_ptr(), Wp.data_ptr(), Y.data_ptr(), M, N, K,
+                                        ws.data_ptr(), ws_bytes, stream) == 0
+        raw = ctypes.c_uint32(0)
+        return Y, fi_lib.swiglu_check_device_status(stream, ctypes.byref(raw)), raw.value
+
+    fi_lib.swiglu_test_set_fault_injection(1)
+    try:
+        _, status, raw = run()
+    finally:
+        fi_lib.swiglu_test_set_fault_injection(0)
+    assert status == TIMEOUT_STATUS and raw & (MMA_TIMEOUT_BIT | PRODUCER_TIMEOUT_BIT), raw
+    assert not ws.any()                                       # counters back at zero
+    want = oracle.swiglu_up(A, W1, W2)["Y"]
+    for _ in range(2):
+        Y, status, raw = run()
+        assert status == 0 and raw == 0
+        r = compare(from_device_bf16(Y), want)
+        assert r["mismatches"] == 0 and r["over_bound"] == 0, r

@@ -282,17 +282,20 @@ size_t counter_region_bytes(int sm_count) {
     return (static_cast<size_t>(4 * sm_count + 3) * sizeof(unsigned int) + 255) / 256 * 256;
 }
 
-// SWIGLU_DYNAMIC_TILES=0 keeps the static tile order everywhere (ablation);
-// read on every call.
-bool dynamic_tiles_allowed() {
-    const char *v = std::getenv("SWIGLU_DYNAMIC_TILES");
-    return !(v && std::strcmp(v, "0") == 0);
-}
-// Whether a CTA-pair launch hands out its tiles at run time: whole tiles
-// only, at least two waves of them.
+// Whether a CTA-pair launch hands out its tiles at run time (whole tiles
+// only): automatically from kDynamicMinWaves waves of tiles on, where the
+// pairs' drift costs DRAM re-reads (72B, M=8192, 97 waves: 15.2 -> 4.7 GB
+// read per launch, 2% faster at the power cap) and the ring's hand-offs
+// cost nothing (7B M=512, 3.9 waves: 1% slower dynamic, so static there).
+// SWIGLU_DYNAMIC_TILES=0 keeps the static order everywhere, =1 takes the
+// dynamic one from two waves on (ablations and tests); read on every call.
+constexpr int kDynamicMinWaves = 8;
 bool dynamic_tiles(const WorkSched &s, bool pair) {
-    return pair && s.sk_iters == 0 && s.n_split == 1 && s.num_tiles >= 2 * s.grid &&
-           dynamic_tiles_allowed();
+    if (!pair || s.sk_iters != 0 || s.n_split != 1) return false;
+    const char *v = std::getenv("SWIGLU_DYNAMIC_TILES");
+    if (v && std::strcmp(v, "0") == 0) return false;
+    const int min_waves = (v && std::strcmp(v, "1") == 0) ? 2 : kDynamicMinWaves;
+    return s.num_tiles >= static_cast<long long>(min_waves) * s.grid;
 }
 // Partial slots: 2 per worker (its first and last stream-K tile), and for
 // the 2-SM kernel one per CTA of the pair.

@@ -97,6 +97,12 @@ int swiglu_pack_weights_nk(const void *W1, const void *W2, int64_t N, int64_t K,
  * CTAs, plus one counter per such tile. K is split only for problems of a
  * handful of output tiles (whole tiles or column sub-tiles would leave most
  * SMs idle), or when SWIGLU_SCHEDULE forces it (see swiglu_up_forward).
+ * Launches of whole tiles on CTA pairs with eight or more waves of tiles
+ * need only the counter region (a few KB): their tiles past the first wave
+ * are handed out at run time from a counter there, so that the pairs, which
+ * drift apart over many tiles, keep working on neighbouring tiles and share
+ * them in L2 (SWIGLU_DYNAMIC_TILES=0 turns this off, =1 uses it from two
+ * waves on; the result is the same either way).
  */
 size_t swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K);
 

@@ -246,6 +246,7 @@ def test_dynamic_tile_counter_survives_a_timeout(fi_lib, monkeypatch):
     pair counts itself out on its way through teardown, and the last one
     resets the counter."""
     monkeypatch.setenv("SWIGLU_FUSED_VARIANT", "2sm")
+    monkeypatch.setenv("SWIGLU_DYNAMIC_TILES", "1")      # two waves: dynamic when asked
     import oracle
     M, N, K = 2048, 2432, 128
     A, W1, W2 = workloads.random_case(M, N, K, seed=83)

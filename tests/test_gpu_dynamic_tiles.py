@@ -1,8 +1,9 @@
 """GPU parity of the CTA-pair kernel's dynamic tile order.
 
-A launch of whole tiles and at least two waves hands out the tiles past the
-first wave at run time (a counter in the workspace, a ring of tile indices
-shared by the pair's roles). Every tile is still computed whole by one pair,
+A launch of whole tiles and at least eight waves hands out the tiles past
+the first wave at run time (a counter in the workspace, a ring of tile
+indices shared by the pair's roles); SWIGLU_DYNAMIC_TILES=1 takes the
+dynamic order from two waves on, which the small cases here use. Every tile is still computed whole by one pair,
 summing k in order, so the result must be bit-identical to the static order
 (SWIGLU_DYNAMIC_TILES=0) and meet the oracle criteria; the counter must be
 back at zero after every launch, so back-to-back launches and a launch after
@@ -63,6 +64,8 @@ def _forward(sg, layout, A, W1, W2):
 def test_dynamic_tiles_match_static_order_and_oracle(sg, orc, monkeypatch, layout, M, N, K):
     A, W1, W2 = workloads.random_case(M, N, K, seed=M + N + K)
     monkeypatch.delenv("SWIGLU_DYNAMIC_TILES", raising=False)
+    assert sg.swiglu_workspace_bytes(M, N, K) == 0          # 2-3 waves: static by default
+    monkeypatch.setenv("SWIGLU_DYNAMIC_TILES", "1")
     assert sg.swiglu_workspace_bytes(M, N, K) > 0          # the tile counters
     dyn = _forward(sg, layout, A, W1, W2)
     monkeypatch.setenv("SWIGLU_DYNAMIC_TILES", "0")
@@ -82,7 +85,7 @@ def test_dynamic_tiles_fp8(sg, orc, monkeypatch):
     def run():
         return from_device_bf16(sg.swiglu_up_forward_fp8(dev(A8), Wp, N, sa, s1, s2))
 
-    monkeypatch.delenv("SWIGLU_DYNAMIC_TILES", raising=False)
+    monkeypatch.setenv("SWIGLU_DYNAMIC_TILES", "1")
     assert sg.swiglu_workspace_bytes_fp8(M, N, K) > 0
     y_dyn = run()
     monkeypatch.setenv("SWIGLU_DYNAMIC_TILES", "0")
@@ -95,7 +98,7 @@ def test_dynamic_tiles_fp8(sg, orc, monkeypatch):
 
 def test_dynamic_tiles_down_projection(sg, orc, monkeypatch):
     """The plain (down-projection) mode: 152 output tiles of 256 x 256 on 76
-    pairs, whole tiles, so dynamic."""
+    pairs, whole tiles (two waves, dynamic when asked for)."""
     M, N, K = 2048, 512, 4864
     rng = np.random.Generator(np.random.PCG64(42))
     Yb = workloads.f32_to_bf16_bits(rng.standard_normal(size=(M, N), dtype=np.float32))
@@ -103,7 +106,7 @@ def test_dynamic_tiles_down_projection(sg, orc, monkeypatch):
         rng.standard_normal(size=(N, K), dtype=np.float32) * np.float32(N ** -0.5))
     W3p = sg.swiglu_pack_down_weights(to_device_bf16(W3, "cuda"))
     Yd = to_device_bf16(Yb, "cuda")
-    monkeypatch.delenv("SWIGLU_DYNAMIC_TILES", raising=False)
+    monkeypatch.setenv("SWIGLU_DYNAMIC_TILES", "1")
     assert sg.swiglu_down_workspace_bytes(M, N, K) > 0
     outs = [from_device_bf16(sg.swiglu_down_forward(Yd, W3p, K)) for _ in range(2)]
     monkeypatch.setenv("SWIGLU_DYNAMIC_TILES", "0")
@@ -115,9 +118,11 @@ def test_dynamic_tiles_down_projection(sg, orc, monkeypatch):
     assert r["mismatches"] == 0 and r["over_bound"] == 0, r
 
 
-def test_dynamic_tiles_whole_workload(sg, orc):
-    """The 7B M=2048 prefill shape (1184 pair tiles, 15.6 waves) as the bench
-    runs it, checked on one row of every 256-row pair tile."""
+def test_dynamic_tiles_whole_workload(sg, orc, monkeypatch):
+    """The 7B M=2048 prefill shape (1184 pair tiles, 15.6 waves: dynamic by
+    default) as the bench runs it, checked on one row of every 256-row pair
+    tile."""
+    monkeypatch.delenv("SWIGLU_DYNAMIC_TILES", raising=False)
     w = workloads.BY_LABEL["6"]
     A, W1, W2 = workloads.make_inputs(w)
     assert sg.swiglu_workspace_bytes(w.M, w.N, w.K) > 0

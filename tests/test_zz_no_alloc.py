@@ -36,11 +36,11 @@ def sg():
 # shared scratch array: three shapes split K across CTAs (stream-K) by the
 # library's own choice on a 152-SM part, two are forced to stream-K (one per
 # kernel) so that the scratch path is run whatever the automatic choice
-# becomes, and one runs two waves of whole tiles on CTA pairs, handed out at
-# run time from a tile counter in the scratch. The last group runs one wave
+# becomes, and one runs eight waves of whole tiles on CTA pairs, handed out
+# at run time from a tile counter in the scratch. The last group runs one wave
 # of whole tiles or column sub-tiles and needs no scratch.
 SCRATCH_CASES = [(33, 264, 2000, None), (70, 520, 1000, None), (2048, 392, 520, None),
-                 (300, 392, 1000, "sk"), (128, 4864, 896, "sk"), (2048, 2432, 200, None)]
+                 (300, 392, 1000, "sk"), (128, 4864, 896, "sk"), (2048, 9728, 136, None)]
 PLAIN_CASES = [(128, 4864, 896, None), (512, 4864, 256, None), (1300, 2000, 256, None),
                (200, 9728, 256, None)]
 

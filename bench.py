@@ -946,6 +946,7 @@ def run_gb300(args, w):
     barrier(world, dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    ew0 = time.time()
     e0.record(stream)
     s_in.wait_event(e0)
     s_out.wait_event(e0)
@@ -957,6 +958,8 @@ def run_gb300(args, w):
         stream.wait_event(done)
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    ew1 = time.time()
+    e2e_clocks = sampler.summary(ew0, ew1)
     barrier(world, dev)
     e_el = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world, dev)
     e2e_value = job_flops_per_step * Ke / e_el / 1e12
@@ -1027,7 +1030,8 @@ def run_gb300(args, w):
                 "d2h_bytes_per_step": w.M * w_rank.N * 2, "steps": Ke,
                 "ms_per_step": e_el / Ke * 1e3,
                 "how": "pinned host A -> device, forward, device Y -> pinned host, every step; "
-                       "copy-in, compute and copy-out of consecutive steps overlap on 3 streams"},
+                       "copy-in, compute and copy-out of consecutive steps overlap on 3 streams",
+                "clocks": e2e_clocks},
         "gpu_launches": K, "clocks": clocks_timed, "context_l2_warm": l2_warm,
         "device": device_info(dev),
     }

@@ -239,4 +239,34 @@ inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_co
     return s;
 }
 
+// Schedule of the wide plain-product kernel (down_wide_kernel.cuh): T =
+// m_tiles * n_tiles tiles of 256 rows x 512 output columns, k_blocks each, on
+// `workers` CTA pairs. `mode`: kSchedDataParallel (whole tiles), kSchedStreamK
+// (stream-K over all tiles on all pairs), kSchedStreamKTail (stream-K over
+// the tiles past the last full wave, or over all of them when that remainder
+// is too small to share); kSchedAligned: every tile cut into j = floor(W/T)
+// equal K ranges, one per pair (j*T pairs, each one unit; falls back to
+// stream-K over all tiles when T >= W or the ranges would be too short).
+// Anything else: whole tiles.
+constexpr int kSchedAligned = 5;
+
+inline WorkSched plan_down_wide(int m_tiles, int n_tiles, int k_blocks, int workers, int group_m,
+                                int min_sk_iters, int mode) {
+    const int T = m_tiles * n_tiles;
+    if (mode == kSchedAligned) {
+        const int j = T < workers ? workers / T : 1;
+        if (j >= 2 && k_blocks / j >= (min_sk_iters > 0 ? min_sk_iters : 1)) {
+            const WorkSched s = plan_schedule(m_tiles, n_tiles, k_blocks, j * T, group_m,
+                                              min_sk_iters, false, kSchedStreamK);
+            if (s.grid == j * T && s.dp_tiles == 0) return s;
+        }
+        mode = kSchedStreamK;
+    }
+    if (mode == kSchedStreamK || mode == kSchedStreamKTail)
+        return plan_schedule(m_tiles, n_tiles, k_blocks, workers, group_m, min_sk_iters, false,
+                             mode);
+    return plan_schedule(m_tiles, n_tiles, k_blocks, workers, group_m, min_sk_iters, false,
+                         kSchedDataParallel);
+}
+
 }  // namespace swiglu

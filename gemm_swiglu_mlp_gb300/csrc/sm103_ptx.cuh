@@ -68,15 +68,18 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 
 // Waits until the phase with the given parity has completed. Returns false if
 // `abort_flag` (shared memory, set by another role that gave up) becomes
-// non-zero or the wait exceeds kWaitLimitCycles.
+// non-zero or the wait exceeds `limit` cycles (kWaitLimitCycles by default;
+// a role downstream of another passes a longer one, so that when both would
+// run out the upstream wait, the cause, is the one reported).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          const volatile int *abort_flag) {
+                                          const volatile int *abort_flag,
+                                          long long limit = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimitCycles) return false;
+        if (clock64() - t0 > limit) return false;
     }
 }
 

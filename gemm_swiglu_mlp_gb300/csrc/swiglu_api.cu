@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "down_wide_kernel.cuh"
 #include "fused_up_kernel.cuh"
 #include "fused_up_pair_kernel.cuh"
 #include "pack_kernel.cuh"
@@ -28,6 +29,7 @@ constexpr int kMinStreamKIters = 8;  // k-blocks per CTA share, at least
 constexpr int kAssumedMaxSms = 256;  // workspace sizing when no device answers
 constexpr int kPairStages = 6;
 constexpr int kDownTileCols = 256;   // output columns of a plain-product (down) tile
+constexpr int64_t kWideMinM = 256;   // from this many rows on, the wide down-projection kernel
 constexpr int64_t kPairMinM = 256;   // from this many tokens on, the 2-SM kernel
 using FusedC = FusedCfg<kFusedStages>;
 using Narrow64C = FusedCfg<kNarrow64Stages, 128>;
@@ -139,7 +141,9 @@ int device_setup(int *dev_out, DeviceState **st_out) {
                                  Narrow32C::SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(fused_up_pair_kernel<kPairStages, ElemBF16, false, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 PairC::SMEM_BYTES) != cudaSuccess) {
+                                 PairC::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(down_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 WideCfg::SMEM_BYTES) != cudaSuccess) {
             cudaGetLastError();
             st.status = SWIGLU_ERR_CUDA;
             return;
@@ -190,7 +194,8 @@ int current_sm_count() {
 
 // Schedule of one call. `workers` = CTAs (1-SM kernel) or CTA pairs (2-SM
 // kernel) that run at once; a 2-SM tile has 256 rows.
-// SWIGLU_SCHEDULE=dp|split|sk|sk-tail forces one schedule form (ablations);
+// SWIGLU_SCHEDULE=dp|split|sk|sk-tail|sk-aligned forces one schedule form
+// (ablations; sk-aligned applies to the wide down-projection kernel only);
 // unset or anything else: the automatic choice.
 int schedule_mode() {
     const char *v = std::getenv("SWIGLU_SCHEDULE");
@@ -199,7 +204,14 @@ int schedule_mode() {
     if (std::strcmp(v, "split") == 0) return kSchedColumnSplit;
     if (std::strcmp(v, "sk") == 0) return kSchedStreamK;
     if (std::strcmp(v, "sk-tail") == 0) return kSchedStreamKTail;
+    if (std::strcmp(v, "sk-aligned") == 0) return kSchedAligned;
     return kSchedAuto;
+}
+// The same for the fused kernels and the CTA-pair plain mode, which have no
+// aligned form.
+int schedule_mode_fused() {
+    const int m = schedule_mode();
+    return m == kSchedAligned ? kSchedAuto : m;
 }
 
 // SWIGLU_GROUP_M=<rows> (ablation): token rows per group of the tile order
@@ -227,22 +239,22 @@ WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, int ctas, int k
                          weight_bound, mode);
 }
 
-// Schedule of the plain product out = Y x W3 (Y [M, N], W3 [N, K]): CTA
-// pairs on tiles of 256 rows x 256 output columns, k-blocks over N. Its
-// output has few tiles against a long reduction (the hidden size is a few
-// times smaller than the intermediate size), so whole tiles are kept only
-// when they fill at least 90% of the last wave and stream-K splits the
-// k-blocks otherwise (a split tile's partial sums cost a few k-blocks of
-// time against tiles of a hundred): over all tiles when there are fewer
-// tiles than pairs, else over the tiles past the last full wave (7B, M=2048:
-// 177 us against 201 us for all tiles and 185 us for whole tiles). Column
-// sub-tiles do not apply.
+// Schedule of the plain product out = Y x W3 (Y [M, N], W3 [N, K]) on the
+// CTA-pair kernel's plain mode: tiles of 256 rows x 256 output columns,
+// k-blocks over N. Its output has few tiles against a long reduction (the
+// hidden size is a few times smaller than the intermediate size), so whole
+// tiles are kept only when they fill at least 90% of the last wave and
+// stream-K splits the k-blocks otherwise (a split tile's partial sums cost a
+// few k-blocks of time against tiles of a hundred): over all tiles when there
+// are fewer tiles than pairs, else over the tiles past the last full wave
+// (7B, M=2048: 177 us against 201 us for all tiles and 185 us for whole
+// tiles). Column sub-tiles do not apply.
 WorkSched plan_down(int64_t M, int64_t N, int64_t K, int workers) {
     const int rows = FusedC::BM * 2;
     const int m_tiles = static_cast<int>((M + rows - 1) / rows);
     const int n_tiles = static_cast<int>((K + kDownTileCols - 1) / kDownTileCols);
     const int k_blocks = static_cast<int>((N + ElemBF16::kBK - 1) / ElemBF16::kBK);
-    int mode = schedule_mode();
+    int mode = schedule_mode_fused();
     if (mode == kSchedColumnSplit) mode = kSchedAuto;
     if (mode == kSchedAuto) {
         const long long T = static_cast<long long>(m_tiles) * n_tiles;
@@ -256,6 +268,41 @@ WorkSched plan_down(int64_t M, int64_t N, int64_t K, int workers) {
                          mode);
 }
 
+// The down-projection's kernel and schedule. The wide kernel
+// (down_wide_kernel.cuh, tiles of 256 x 512) feeds the tensor cores with a
+// third fewer operand bytes per flop, which shows at the power cap as a
+// higher SM clock (7B, M=8192: 621 against 663 us, 1545 against 1432 MHz),
+// but it has one accumulator stage and its split tiles move whole 512-column
+// FP32 partials through L2; so it takes a call when whole wide tiles fill at
+// least 90% of their last wave (from kWideMinM rows on), as whole tiles. The
+// CTA-pair kernel's plain mode (256 x 256, plan_down) takes the rest: few
+// output tiles, where a K split is needed, and decode-sized products.
+// SWIGLU_DOWN_TILE=256|512, read on every call, forces one of them
+// (ablations and tests); with the wide kernel forced, SWIGLU_SCHEDULE picks
+// its form (dp, sk, sk-tail, sk-aligned; whole tiles otherwise).
+struct DownPlan {
+    bool wide;
+    WorkSched sched;
+};
+DownPlan plan_down_any(int64_t M, int64_t N, int64_t K, int workers) {
+    const int rows = WideCfg::UMMA_M;
+    const int m_tiles = static_cast<int>((M + rows - 1) / rows);
+    const int n_tiles = static_cast<int>((K + WideCfg::TILE_N - 1) / WideCfg::TILE_N);
+    const int k_blocks = static_cast<int>((N + ElemBF16::kBK - 1) / ElemBF16::kBK);
+    const long long T = static_cast<long long>(m_tiles) * n_tiles;
+    const long long waves = (T + workers - 1) / workers;
+    const double eff = static_cast<double>(T) / (static_cast<double>(waves) * workers);
+    bool wide = M >= kWideMinM && eff >= 0.9;
+    const char *v = std::getenv("SWIGLU_DOWN_TILE");
+    if (v && std::strcmp(v, "256") == 0) wide = false;
+    if (v && std::strcmp(v, "512") == 0) wide = true;
+    if (!wide) return {false, plan_down(M, N, K, workers)};
+    const int grows = group_rows_override();
+    const int group_m = grows ? std::max(1, grows / rows) : kGroupM / 2;
+    return {true, plan_down_wide(m_tiles, n_tiles, k_blocks, workers, group_m, kMinStreamKIters,
+                                 schedule_mode())};
+}
+
 // Which kernel serves a call, and its schedule: the 1-SM kernel below 256
 // rows, the CTA-pair kernel from there on.
 struct LaunchPlan {
@@ -264,22 +311,23 @@ struct LaunchPlan {
 };
 LaunchPlan choose_plan(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters, int kbk) {
     const int v = variant_override();
-    const int mode = schedule_mode();
+    const int mode = schedule_mode_fused();
     if (v == 1 || (v == 0 && M < kPairMinM)) return {1, plan_for(M, N, K, sms, 1, kbk, mode)};
     return {2, plan_for(M, N, K, pair_clusters, 2, kbk, mode)};
 }
 
 // Workspace layout: a counter region at offset 0 whose size depends only on
 // the device (so a counter never lands where another shape's call left
-// partial sums), then the partial slots. Every stream-K tile needs at most
-// one counter per CTA half, and there are fewer than 2 * grid stream-K
-// tiles, so 4 * sm_count counters always suffice; after them come the
+// partial sums), then the partial slots. There are fewer than 2 * grid
+// stream-K tiles; a tile needs at most one counter per CTA half in the fused
+// kernels and one per CTA half and part (4) in the wide down-projection
+// kernel, so 16 * sm_count counters always suffice; after them come the
 // CTA-pair kernel's start-order ticket counter and its dynamic-tile counter
 // pair (next tile, pairs finished).
-int ticket_index(int sm_count) { return 4 * sm_count; }
-int tile_counter_index(int sm_count) { return 4 * sm_count + 1; }
+int ticket_index(int sm_count) { return 16 * sm_count; }
+int tile_counter_index(int sm_count) { return 16 * sm_count + 1; }
 size_t counter_region_bytes(int sm_count) {
-    return (static_cast<size_t>(4 * sm_count + 3) * sizeof(unsigned int) + 255) / 256 * 256;
+    return (static_cast<size_t>(16 * sm_count + 3) * sizeof(unsigned int) + 255) / 256 * 256;
 }
 
 // Whether a CTA-pair launch hands out its tiles at run time (whole tiles
@@ -307,6 +355,14 @@ size_t workspace_partials_bytes(const WorkSched &s, int64_t M, bool pair) {
 size_t workspace_bytes_for(const WorkSched &s, int64_t M, bool pair, int sm_count) {
     if (s.sk_iters == 0) return dynamic_tiles(s, pair) ? counter_region_bytes(sm_count) : 0;
     return counter_region_bytes(sm_count) + workspace_partials_bytes(s, M, pair);
+}
+// The down-projection's: the wide kernel keeps 2 slots per worker and CTA
+// half of a whole FP32 partial tile half (128 rows x 512 columns).
+size_t down_workspace_bytes_for(const DownPlan &p, int64_t M, int sm_count) {
+    if (!p.wide) return workspace_bytes_for(p.sched, M, true, sm_count);
+    if (p.sched.sk_iters == 0) return 0;
+    return counter_region_bytes(sm_count) + static_cast<size_t>(2) * p.sched.grid * 2 *
+                                                WideCfg::SLOT_FLOATS * sizeof(float);
 }
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
@@ -711,9 +767,10 @@ size_t down_workspace_bytes_impl(int64_t M, int64_t N, int64_t K) {
     int dev;
     DeviceState *st;
     if (device_setup(&dev, &st) == SWIGLU_OK)
-        return workspace_bytes_for(plan_down(M, N, K, st->pair_clusters), M, true, st->sm_count);
+        return down_workspace_bytes_for(plan_down_any(M, N, K, st->pair_clusters), M,
+                                        st->sm_count);
     const int sms = current_sm_count();
-    return workspace_bytes_for(plan_down(M, N, K, sms / 2), M, true, sms);
+    return down_workspace_bytes_for(plan_down_any(M, N, K, sms / 2), M, sms);
 }
 
 // Argument checks of the plain product out [M, K] = Y [M, N] x W3 [N, K].
@@ -731,8 +788,55 @@ int down_checks(const void *Y, const void *W3packed, const void *out, int64_t M,
     return SWIGLU_OK;
 }
 
+// The wide kernel's launch (plan from plan_down_any, checks done).
+int down_wide_launch(const WorkSched &sched, const void *Y, const void *W3packed, void *out,
+                     int64_t M, int64_t N, int64_t K, void *workspace, bool ws, int sm_count,
+                     void *stream) {
+    const int kt = static_cast<int>((K + kDownTileCols - 1) / kDownTileCols);
+    const uint64_t weight_tiles = static_cast<uint64_t>(kt) * static_cast<uint64_t>(sched.k_blocks);
+    CUtensorMap tmA, tmB, tmOut;
+    if (!encode_2d(&tmA, Y, N, M, ElemBF16::kBK, WideCfg::BM) ||
+        !encode_packed_weights(&tmB, W3packed, weight_tiles, 128u, false) ||
+        !encode_2d(&tmOut, out, K, M, 64, 32))
+        return SWIGLU_ERR_CUDA;
+    WideArgs args{};
+    args.M = static_cast<int>(M);
+    args.N = static_cast<int>(K);   // output columns
+    args.K = static_cast<int>(N);   // reduction
+    args.kt_tiles = kt;
+    args.sched = sched;
+    args.counters = ws ? static_cast<unsigned int *>(workspace) : nullptr;
+    args.partials = ws ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                   counter_region_bytes(sm_count))
+                       : nullptr;
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+    args.skip_first_fill = g_test_skip_first_fill;
+#endif
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * sched.grid));
+    cfg.blockDim = dim3(WideCfg::THREADS);
+    cfg.dynamicSmemBytes = WideCfg::SMEM_BYTES;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, down_wide_kernel, tmA, tmB, tmOut, args);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SWIGLU_ERR_CUDA;
+    }
+    return SWIGLU_OK;
+}
+
 // out [M, K] = Y [M, N] x W3 [N, K] (W3 packed by swiglu_pack_down_weights),
-// BF16 in and out, FP32 accumulation: the CTA-pair kernel in its plain mode.
+// BF16 in and out, FP32 accumulation: the wide kernel, or the CTA-pair
+// kernel in its plain mode (plan_down_any).
 int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M, int64_t N,
                       int64_t K, void *workspace, size_t workspace_bytes, void *stream) {
     const int c = down_checks(Y, W3packed, out, M, N, K);
@@ -745,8 +849,9 @@ int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M,
     DeviceState *st;
     const int s = device_setup(&dev, &st);
     if (s != SWIGLU_OK) return s;
-    const WorkSched sched = plan_down(M, N, K, st->pair_clusters);
-    const size_t ws_need = workspace_bytes_for(sched, M, true, st->sm_count);
+    const DownPlan plan = plan_down_any(M, N, K, st->pair_clusters);
+    const WorkSched &sched = plan.sched;
+    const size_t ws_need = down_workspace_bytes_for(plan, M, st->sm_count);
     if (ws_need > 0) {
         if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
             workspace_bytes < ws_need)
@@ -755,6 +860,9 @@ int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M,
             overlaps(workspace, ws_need, W3packed, pbytes))
             return SWIGLU_ERR_INVALID_ARG;
     }
+    if (plan.wide)
+        return down_wide_launch(sched, Y, W3packed, out, M, N, K, workspace, ws_need > 0,
+                                st->sm_count, stream);
     const uint64_t weight_tiles =
         static_cast<uint64_t>(sched.order.n_tiles) * static_cast<uint64_t>(sched.k_blocks);
     // the sub-tile maps are never used in the plain mode: the whole-tile map

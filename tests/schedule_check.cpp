@@ -33,7 +33,12 @@ int main() {
     int bad = 0;
     while (std::scanf("%d %d %d %d %d %d %d", &mt, &nt, &kb, &sms, &min_iters, &wbound, &mode) ==
            7) {
-        const WorkSched s = plan_schedule(mt, nt, kb, sms, 16, min_iters, wbound != 0, mode);
+        // modes 10..14: the wide down-projection kernel's planner (plan_down_wide)
+        // with mode - 10, `sms` CTA pairs
+        const bool wide = mode >= 10;
+        if (wide) mode -= 10;
+        const WorkSched s = wide ? plan_down_wide(mt, nt, kb, sms, 8, min_iters, mode)
+                                 : plan_schedule(mt, nt, kb, sms, 16, min_iters, wbound != 0, mode);
         const int T = mt * nt;
         if (s.grid < 1 || s.grid > sms) { bad |= fail("grid", s.grid, sms); continue; }
         if (s.sk_iters > 0 && s.dp_tiles % s.grid != 0) { bad |= fail("dp multiple", s.dp_tiles, s.grid); continue; }
@@ -48,12 +53,17 @@ int main() {
         std::map<int, std::vector<std::pair<int, int>>> contrib;  // sk tile -> (cta, kb0)
         std::vector<long long> work(s.grid, 0);
         std::set<long long> coords_seen;
+        // the wide planner's aligned form (every tile cut into grid / T equal
+        // K ranges): exactly one unit per pair, never two tiles
+        const bool aligned = wide && s.dp_tiles == 0 && s.sk_iters > 0 && s.grid % T == 0 &&
+                             s.grid > T && kb % (s.grid / T) == 0;
         for (int c = 0; c < s.grid; ++c) {
             UnitIter it;
             it.init(s, c);
             Unit u;
-            int n_dp = 0;
+            int n_dp = 0, n_units = 0;
             while (it.next(u)) {
+                ++n_units;
                 if (u.tile < 0 || u.tile >= T || u.kb0 < 0 || u.kb1 > kb || u.kb0 >= u.kb1 ||
                     (u.width != 128 && u.width != 64 && u.width != 32) || u.sub < 0 ||
                     (u.sub + 1) * u.width > 128) {
@@ -79,6 +89,7 @@ int main() {
                 if (mb < 0 || mb >= mt || nb < 0 || nb >= nt) bad |= fail("coords", mb, nb);
                 coords_seen.insert((long long)mb * nt + nb);
             }
+            if (aligned && n_units != 1) bad |= fail("aligned split: units per pair", n_units, c);
             const int want_dp = s.dp_tiles / s.grid + (c < s.dp_tiles % s.grid ? 1 : 0);
             if (s.n_split == 1 && n_dp != want_dp) bad |= fail("dp per cta", n_dp, c);
         }
@@ -115,7 +126,7 @@ int main() {
         if (s.sk_iters == 0 && s.n_split == 1) {
             if (wmax - wmin > 4 * kb) bad |= fail("dp imbalance", (int)wmin, (int)wmax);
             const int waves = (T + sms - 1) / sms;
-            if (mode == kSchedAuto && T < 0.85 * waves * sms && 2 * T < sms)
+            if (!wide && mode == kSchedAuto && T < 0.85 * waves * sms && 2 * T < sms)
                 bad |= fail("dp chosen below threshold", T, waves * sms);
         }
         if (s.n_split > 1 && wmax - wmin > 4 * kb / s.n_split) bad |= fail("split imbalance", (int)wmin, (int)wmax);

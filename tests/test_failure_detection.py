@@ -94,13 +94,18 @@ def test_wait_timeout_is_reported_and_context_survives(fi_lib, monkeypatch, vari
     assert r["mismatches"] == 0 and r["over_bound"] == 0, r
 
 
+@pytest.mark.parametrize("tile", ["256", "512"])
 @pytest.mark.parametrize("mode,M,N,K", [("auto", 512, 2048, 512), ("dp", 512, 512, 512)])
-def test_down_projection_wait_timeout(fi_lib, monkeypatch, mode, M, N, K):
-    """The same for the down-projection (the CTA-pair kernel's plain mode),
-    with stream-K split tiles (auto: 4 output tiles on all pairs) and with
-    whole tiles: the timeout is reported and the next call is correct."""
+def test_down_projection_wait_timeout(fi_lib, monkeypatch, tile, mode, M, N, K):
+    """The same for the down-projection, on both of its kernels (the
+    CTA-pair kernel's plain mode, tile 256, and the wide kernel, tile 512),
+    with stream-K split tiles (auto: 4 or 2 output tiles on many pairs) and
+    with whole tiles: the timeout is reported and the next call is correct."""
+    monkeypatch.setenv("SWIGLU_DOWN_TILE", tile)
     if mode != "auto":
         monkeypatch.setenv("SWIGLU_SCHEDULE", mode)
+    elif tile == "512":
+        monkeypatch.setenv("SWIGLU_SCHEDULE", "sk")   # the wide kernel's split tiles
     import oracle
     lib = fi_lib
     vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
@@ -163,20 +168,27 @@ def _busy_and_run(lib, op, n_busy=120, busy_ns=300_000_000):
     return out, status, raw.value, still_busy
 
 
-@pytest.mark.parametrize("kind", ["down", "up"])
+@pytest.mark.parametrize("kind", ["down", "down-wide", "up"])
 def test_split_tiles_finish_while_other_work_holds_sms(fi_lib, monkeypatch, kind):
-    """A K-split launch of the CTA-pair kernel while a kernel on another
-    stream holds 120 of the SMs for 300 ms: only some of its pairs can run
-    at first. A split tile's owner waits only for pairs that started before
-    it (worker numbers follow the start order), so the call completes on the
-    free SMs, well within this build's ~10 ms wait limit, and is correct.
-    (Were owners to wait for pairs not yet started, they would hold their
-    SMs until the limit and report SWIGLU_ERR_DEVICE_TIMEOUT.)"""
+    """A K-split launch while a kernel on another stream holds 120 of the
+    SMs for 300 ms: only some of its pairs can run at first. In the CTA-pair
+    kernel a split tile's owner waits only for pairs that started before it
+    (worker numbers follow the start order); in the wide down-projection
+    kernel nobody waits (the last to count in on a part finishes it). Either
+    way the call completes on the free SMs, well within this build's ~10 ms
+    wait limit, and is correct. (Were owners to wait for pairs not yet
+    started, they would hold their SMs until the limit and report
+    SWIGLU_ERR_DEVICE_TIMEOUT.)"""
     import oracle
     lib = fi_lib
     vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
-    if kind == "down":
-        # 8 output tiles of 256 x 256, 64 k-blocks each: stream-K over 64 pairs
+    if kind.startswith("down"):
+        # CTA-pair kernel: 8 output tiles of 256 x 256, 64 k-blocks each,
+        # stream-K over 64 pairs; wide kernel: 4 tiles of 256 x 512,
+        # stream-K forced, on 32 pairs
+        monkeypatch.setenv("SWIGLU_DOWN_TILE", "512" if kind == "down-wide" else "256")
+        if kind == "down-wide":
+            monkeypatch.setenv("SWIGLU_SCHEDULE", "sk")
         M, N, K = 512, 4096, 1024
         lib.swiglu_pack_down_weights.argtypes = [vp, i64, i64, vp, vp]
         lib.swiglu_down_packed_weight_bytes.argtypes = [i64, i64]

@@ -97,8 +97,11 @@ def test_dynamic_tiles_fp8(sg, orc, monkeypatch):
 
 
 def test_dynamic_tiles_down_projection(sg, orc, monkeypatch):
-    """The plain (down-projection) mode: 152 output tiles of 256 x 256 on 76
-    pairs, whole tiles (two waves, dynamic when asked for)."""
+    """The CTA-pair kernel's plain (down-projection) mode: 152 output tiles
+    of 256 x 256 on 76 pairs, whole tiles (two waves, dynamic when asked
+    for). The wide down-projection kernel, which would take this shape, has
+    no dynamic order, so the CTA-pair kernel is forced."""
+    monkeypatch.setenv("SWIGLU_DOWN_TILE", "256")
     M, N, K = 2048, 512, 4864
     rng = np.random.Generator(np.random.PCG64(42))
     Yb = workloads.f32_to_bf16_bits(rng.standard_normal(size=(M, N), dtype=np.float32))

@@ -11,9 +11,9 @@ import numpy as np
 import pytest
 
 import workloads
-from tests.parity import (bits_to_f64, compare, fp32_accumulation_bound, from_device_bf16,
-                          pack_down_reference, plain_accumulation_bound, to_device_bf16,
-                          ulp_bf16)
+from tests.parity import (beyond_scale_allowance, bits_to_f64, compare, fp32_accumulation_bound,
+                          from_device_bf16, pack_down_reference, plain_accumulation_bound,
+                          plain_certified_bound, to_device_bf16, ulp_bf16)
 
 torch = pytest.importorskip("torch")
 
@@ -50,9 +50,10 @@ def _down_case(M, N, K, seed):
 
 
 def _check_plain(got, want, Yb, W3b, label):
-    r = compare(got, want, plain_accumulation_bound(Yb, W3b))
+    r = compare(got, want, plain_accumulation_bound(Yb, W3b), plain_certified_bound(Yb, W3b))
     assert r["nonfinite"] == 0, (label, r)
     assert r["mismatches"] == 0 and r["over_bound"] == 0, (label, r)
+    assert r["beyond_accum_scale"] <= beyond_scale_allowance(r["elements"]), (label, r)
     return r
 
 

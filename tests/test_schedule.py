@@ -40,6 +40,7 @@ def _cases():
 
 
 MODES = {"auto": 0, "dp": 1, "split": 2, "sk": 3, "sk-tail": 4}
+WIDE_MODES = {"auto": 10, "dp": 11, "sk": 13, "sk-tail": 14, "sk-aligned": 15}
 
 
 @pytest.mark.parametrize("mode", sorted(MODES))
@@ -49,3 +50,48 @@ def test_schedule_covers_every_iteration_once_and_balances(checker, mode):
     r = subprocess.run([checker], input=inp, capture_output=True, text=True)
     assert r.returncode == 0, r.stdout[-3000:]
     assert r.stdout.count("\n") == len(cases)
+
+
+def _wide_cases():
+    """The wide down-projection planner: tiles of 256 rows x 512 output
+    columns of every workload's down-projection (out [M, K] = Y [M, N] x
+    W3 [N, K]: k-blocks over N), on 76, 74 and 66 pairs, and random shapes."""
+    cases = []
+    for w in workloads.WORKLOADS:
+        mt, nt, kb = -(-w.M // 256), -(-w.K // 512), -(-w.N // 64)
+        for pairs in (76, 74, 66):
+            cases.append((mt, nt, kb, pairs, 8, 0))
+    rng = np.random.Generator(np.random.PCG64(4))
+    for _ in range(400):
+        cases.append((int(rng.integers(1, 40)), int(rng.integers(1, 20)), int(rng.integers(1, 500)),
+                      int(rng.integers(1, 100)), 8, 0))
+    cases += [(8, 3, 140, 76, 8, 0), (6, 4, 33, 76, 8, 0), (12, 7, 76, 76, 8, 0),
+              (12, 7, 32, 76, 8, 0), (2, 7, 296, 76, 8, 0), (1, 1, 1, 76, 8, 0)]
+    return cases
+
+
+@pytest.mark.parametrize("mode", sorted(WIDE_MODES))
+def test_wide_down_schedule_covers_every_iteration_once(checker, mode):
+    """Coverage, k order and slot checks of plan_down_wide's plans; its
+    aligned form (each tile cut into equal K ranges) gives every pair one
+    unit."""
+    cases = [c + (WIDE_MODES[mode],) for c in _wide_cases()]
+    inp = "\n".join(" ".join(map(str, c)) for c in cases) + "\n"
+    r = subprocess.run([checker], input=inp, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout[-3000:]
+    assert r.stdout.count("\n") == len(cases)
+
+
+def test_wide_down_plans_of_the_workload_shapes(checker):
+    """The forms of the wide planner at the down-projection shapes on 76
+    pairs: the aligned split cuts the 1.5B shape's 24 tiles in three K
+    ranges on 72 pairs and the 7B M=512 shape's 14 tiles in five on 70;
+    whole tiles (the automatic form) keep one pair per tile."""
+    want = [("1", 15, 72, 0), ("5", 15, 70, 0), ("7", 10, 76, 224), ("11", 10, 76, 512)]
+    for label, mode, grid, dp in want:
+        w = workloads.BY_LABEL[label]
+        case = (-(-w.M // 256), -(-w.K // 512), -(-w.N // 64), 76, 8, 0, mode)
+        r = subprocess.run([checker], input=" ".join(map(str, case)) + "\n", capture_output=True,
+                           text=True)
+        assert r.returncode == 0, r.stdout
+        assert "grid=%d dp=%d " % (grid, dp) in r.stdout, (label, r.stdout)

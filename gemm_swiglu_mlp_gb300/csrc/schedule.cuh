@@ -239,6 +239,47 @@ inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_co
     return s;
 }
 
+// Stream-K over all T tiles (fewer than `workers`) with the grid chosen for
+// its finishing cost: on g CTAs each takes about T*k/g k-blocks, and a tile
+// whose k-blocks span n CTAs' ranges is summed through the workspace, which
+// costs its finisher about kSplitFixKb per partial to read (and an owner
+// waits for partials written at the same time). Among g in [ceil(W/2), W],
+// the grid minimising ceil(T*k/g) + kSplitFixKb * (n_max(g) - 1) wins; e.g.
+// 48 tiles of 140 k-blocks on 76 pairs: g = 76 gives 88.4 k-blocks each but
+// tiles among three pairs, g = 72 gives 93.3 each and every tile between
+// exactly two (two tiles per three pairs).
+constexpr int kSplitFixKb = 14;
+
+inline WorkSched plan_stream_k_grid(int m_tiles, int n_tiles, int k_blocks, int workers,
+                                    int group_m, int min_sk_iters) {
+    const int T = m_tiles * n_tiles;
+    WorkSched best = plan_schedule(m_tiles, n_tiles, k_blocks, workers, group_m, min_sk_iters,
+                                   false, kSchedStreamK);
+    if (best.sk_iters == 0 || best.dp_tiles != 0) return best;
+    auto cost = [&](const WorkSched &s) {
+        int n_max = 1;
+        for (int t = 0; t < T; ++t) {
+            const long long first = static_cast<long long>(t) * k_blocks;
+            const int n = s.sk_owner(first + k_blocks - 1) - s.sk_owner(first) + 1;
+            n_max = n > n_max ? n : n_max;
+        }
+        const long long per = (s.sk_iters + s.grid - 1) / s.grid;
+        return static_cast<double>(per) + kSplitFixKb * (n_max - 1);
+    };
+    double best_c = cost(best);
+    for (int g = workers - 1; g > T && 2 * g >= workers; --g) {
+        const WorkSched s = plan_schedule(m_tiles, n_tiles, k_blocks, g, group_m, min_sk_iters,
+                                          false, kSchedStreamK);
+        if (s.grid != g || s.dp_tiles != 0 || s.sk_iters == 0) continue;
+        const double c = cost(s);
+        if (c < best_c - 1e-9) {
+            best = s;
+            best_c = c;
+        }
+    }
+    return best;
+}
+
 // Schedule of the wide plain-product kernel (down_wide_kernel.cuh): T =
 // m_tiles * n_tiles tiles of 256 rows x 512 output columns, k_blocks each, on
 // `workers` CTA pairs. `mode`: kSchedDataParallel (whole tiles), kSchedStreamK

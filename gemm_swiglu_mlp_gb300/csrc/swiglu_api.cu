@@ -248,7 +248,9 @@ WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, int ctas, int k
 // few k-blocks of time against tiles of a hundred): over all tiles when there
 // are fewer tiles than pairs, else over the tiles past the last full wave
 // (7B, M=2048: 177 us against 201 us for all tiles and 185 us for whole
-// tiles). Column sub-tiles do not apply.
+// tiles). With fewer tiles than pairs the grid is picked for the split's
+// finishing cost (schedule.cuh, plan_stream_k_grid: 1.5B, 48 tiles, on 72 of
+// the 76 pairs, two per tile). Column sub-tiles do not apply.
 WorkSched plan_down(int64_t M, int64_t N, int64_t K, int workers) {
     const int rows = FusedC::BM * 2;
     const int m_tiles = static_cast<int>((M + rows - 1) / rows);
@@ -264,6 +266,8 @@ WorkSched plan_down(int64_t M, int64_t N, int64_t K, int workers) {
     }
     const int grows = group_rows_override();
     const int group_m = grows ? std::max(1, grows / rows) : kGroupM / 2;
+    if (mode == kSchedStreamK && schedule_mode_fused() == kSchedAuto)
+        return plan_stream_k_grid(m_tiles, n_tiles, k_blocks, workers, group_m, kMinStreamKIters);
     return plan_schedule(m_tiles, n_tiles, k_blocks, workers, group_m, kMinStreamKIters, false,
                          mode);
 }

@@ -35,10 +35,15 @@ int main() {
            7) {
         // modes 10..14: the wide down-projection kernel's planner (plan_down_wide)
         // with mode - 10, `sms` CTA pairs
-        const bool wide = mode >= 10;
+        // mode 20: stream-K over all tiles with the grid searched for the
+        // finishing cost (plan_stream_k_grid)
+        const bool grid_search = mode == 20;
+        const bool wide = mode >= 10 && !grid_search;
         if (wide) mode -= 10;
-        const WorkSched s = wide ? plan_down_wide(mt, nt, kb, sms, 8, min_iters, mode)
-                                 : plan_schedule(mt, nt, kb, sms, 16, min_iters, wbound != 0, mode);
+        if (grid_search) mode = kSchedStreamK;
+        const WorkSched s = grid_search ? plan_stream_k_grid(mt, nt, kb, sms, 8, min_iters)
+                            : wide      ? plan_down_wide(mt, nt, kb, sms, 8, min_iters, mode)
+                                        : plan_schedule(mt, nt, kb, sms, 16, min_iters, wbound != 0, mode);
         const int T = mt * nt;
         if (s.grid < 1 || s.grid > sms) { bad |= fail("grid", s.grid, sms); continue; }
         if (s.sk_iters > 0 && s.dp_tiles % s.grid != 0) { bad |= fail("dp multiple", s.dp_tiles, s.grid); continue; }

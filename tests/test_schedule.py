@@ -95,3 +95,18 @@ def test_wide_down_plans_of_the_workload_shapes(checker):
                            text=True)
         assert r.returncode == 0, r.stdout
         assert "grid=%d dp=%d " % (grid, dp) in r.stdout, (label, r.stdout)
+
+
+def test_stream_k_grid_search(checker):
+    """plan_stream_k_grid: coverage and k order on random few-tile shapes,
+    and the 1.5B down-projection shape (48 tiles of 256 x 256, 140 k-blocks,
+    76 pairs) lands on 72 pairs (two per tile)."""
+    rng = np.random.Generator(np.random.PCG64(5))
+    cases = [(int(rng.integers(1, 10)), int(rng.integers(1, 10)), int(rng.integers(1, 400)),
+              int(rng.integers(2, 100)), 8, 0, 20) for _ in range(300)]
+    cases.append((8, 6, 140, 76, 8, 0, 20))
+    inp = "\n".join(" ".join(map(str, c)) for c in cases) + "\n"
+    r = subprocess.run([checker], input=inp, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout[-3000:]
+    last = r.stdout.strip().splitlines()[-1]
+    assert "grid=72 " in last and "max_contrib=2" in last, last

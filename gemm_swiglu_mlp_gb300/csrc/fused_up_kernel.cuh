@@ -88,7 +88,17 @@ struct FusedCfg {
 // Up, the pages' Kernel-2 pairing; pack_weights_il_kernel) instead of
 // 128-row blocked. Only the sub-tile weight boxes and the epilogue's TMEM
 // column addressing differ.
-template <int STAGES, int BROWS, typename E, bool IL = false>
+//
+// PLAIN = true: a plain product out = A x W (no activation), the
+// down-projection out = Y x W3 of a decode-sized MLP (M <= 128). W is the
+// down-projection's packed layout ([KT][KB][256][64]); a tile is 128 rows x
+// 64 output columns, the 64 rows 64*(t%4).. of packed tile t/4 (one UMMA
+// N=64 per K step), in the narrow 64-row configuration. With so few rows the
+// product streams W3 from HBM, and its few output columns leave most SMs idle
+// unless K is split: the stream-K partial of a tile is only 64 columns wide,
+// so the last contributor's sum reads a few KB per partner. The epilogue
+// rounds to BF16 and stores from registers; whole tiles and stream-K only.
+template <int STAGES, int BROWS, typename E, bool IL = false, bool PLAIN = false>
 __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
     fused_up_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -96,6 +106,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
                     const __grid_constant__ CUtensorMap tmB32,
                     const __grid_constant__ CUtensorMap tmY, const FusedArgs args) {
     using C = FusedCfg<STAGES, BROWS>;
+    static_assert(!PLAIN || (!IL && !E::kFp8 && BROWS == 64), "plain product: BF16, 64-row stages");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -158,7 +169,9 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
             for (int kb = u.kb0; kb < kend; ++kb) {
                 const int wtile = nb * sched.k_blocks + kb;
                 tma_prefetch_2d(&tmA, kb * E::kBK, mb * C::BM);
-                if (u.width == C::BN) {
+                if constexpr (PLAIN) {
+                    tma_prefetch_3d(&tmB, 0, 64 * (nb & 3), (nb >> 2) * sched.k_blocks + kb);
+                } else if (u.width == C::BN) {
                     tma_prefetch_3d(&tmB, 0, 0, wtile);
                 } else {
                     const CUtensorMap *tmBn = (u.width == 64) ? &tmB64 : &tmB32;
@@ -203,13 +216,20 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
                         continue;
                     }
 #endif
-                    if (2 * u.width > BROWS) {  // never planned: a unit wider than a stage
+                    if (!PLAIN && 2 * u.width > BROWS) {  // never planned: a unit wider than a stage
                         ok = false;
                         break;
                     }
                     const uint32_t b_dst = sbase + C::OFF_B + stage * C::B_BYTES;
                     const int wtile = nb * sched.k_blocks + kb;
-                    if (u.width == C::BN) {
+                    if constexpr (PLAIN) {
+                        // 64 output columns: rows 64*(nb%4) of packed tile nb/4
+                        mbar_arrive_expect_tx(full_bar(stage), args.a_tx_bytes + 64 * kRowBytes);
+                        tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
+                                    kb * E::kBK, mb * C::BM);
+                        tma_load_3d(b_dst, &tmB, full_bar(stage), 0, 64 * (nb & 3),
+                                    (nb >> 2) * sched.k_blocks + kb);
+                    } else if (u.width == C::BN) {
                         mbar_arrive_expect_tx(full_bar(stage), args.stage_tx_bytes);
                         tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
                                     kb * E::kBK, mb * C::BM);
@@ -260,8 +280,9 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::UMMA_N);
                 // Gate|Up columns of this unit: 256, or 2 x the sub-tile width
-                const uint32_t idesc_u =
-                    (u.width == C::BN) ? idesc : E::idesc(C::BM, 2 * u.width);
+                // (plain product: the tile's 64 output columns)
+                const uint32_t idesc_u = PLAIN ? E::idesc(C::BM, 64)
+                                         : (u.width == C::BN) ? idesc : E::idesc(C::BM, 2 * u.width);
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
                         ok = false;
@@ -331,7 +352,95 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
             const bool split = c_hi > c_lo;
             bool store_y = true;
 
-            if (u.width != C::BN) {
+            if constexpr (PLAIN) {
+                // 64 output columns from registers; a split tile goes through
+                // the workspace (its first 64 slot columns), and the last
+                // contributor to count in sums every partial in k order
+                store_y = false;
+                const int col0 = nb * 64;
+                if (!split) {
+                    if (rows_live) {
+#pragma unroll 1
+                        for (int c = 0; c < 64; c += 32) {
+                            uint32_t r[32];
+                            tmem_ld_32x32b_x32(tbase + c, r);
+                            tmem_ld_wait();
+                            reg_fence32(r);
+                            float x[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+                            store_plain32(row0 + lane, col0 + c, x, args);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(acc));
+                } else {
+                    const size_t slot_floats = static_cast<size_t>(kSlotCols) * args.slot_rows;
+                    float *slot = args.partials +
+                                  static_cast<size_t>(2 * cta + sched.sk_slot(cta, u.sk)) * slot_floats;
+                    if (rows_live) {
+#pragma unroll 1
+                        for (int c = 0; c < 64; c += 32) {
+                            uint32_t r[32];
+                            tmem_ld_32x32b_x32(tbase + c, r);
+                            tmem_ld_wait();
+                            reg_fence32(r);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                __stcg(slot + static_cast<size_t>(c + i) * args.slot_rows + row_in_tile,
+                                       __uint_as_float(r[i]));
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(acc));
+                    __threadfence();
+                    epilogue_bar();
+                    if (leader) {
+                        const unsigned int prev = atomicAdd(args.counters + u.sk, 1u);
+                        *last_flag = (prev == static_cast<unsigned int>(c_hi - c_lo)) ? 1 : 0;
+                    }
+                    epilogue_bar();
+                    if (*last_flag != 0) {
+                        __threadfence();
+                        if (rows_live) {
+                            // the partials of four contributors are loaded
+                            // before any is added, so a tile split many ways
+                            // waits for a quarter as many load round trips
+#pragma unroll 1
+                            for (int c = 0; c < 64; c += 32) {
+                                float x[32];
+#pragma unroll 1
+                                for (int k0 = c_lo; k0 <= c_hi; k0 += 4) {
+                                    float v[4][32];
+#pragma unroll
+                                    for (int q = 0; q < 4; ++q) {
+                                        if (k0 + q > c_hi) break;
+                                        const int k = k0 + q;
+                                        const float *src = args.partials +
+                                            static_cast<size_t>(2 * k + sched.sk_slot(k, u.sk)) *
+                                                slot_floats;
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i)
+                                            v[q][i] = __ldcg(src + static_cast<size_t>(c + i) *
+                                                                       args.slot_rows + row_in_tile);
+                                    }
+#pragma unroll
+                                    for (int q = 0; q < 4; ++q) {
+                                        if (k0 + q > c_hi) break;
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i)
+                                            x[i] = (k0 + q == c_lo) ? v[q][i] : x[i] + v[q][i];
+                                    }
+                                }
+                                store_plain32(row0 + lane, col0 + c, x, args);
+                            }
+                        }
+                        if (leader) args.counters[u.sk] = 0u;  // ready for the next launch
+                    }
+                }
+            } else if (u.width != C::BN) {
                 // column sub-tile: straight from TMEM to global memory
                 if (rows_live)
                     epilogue_subtile_store<IL>(tbase, u.width, row0 + lane,

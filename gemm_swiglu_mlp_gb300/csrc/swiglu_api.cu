@@ -30,6 +30,8 @@ constexpr int kAssumedMaxSms = 256;  // workspace sizing when no device answers
 constexpr int kPairStages = 6;
 constexpr int kDownTileCols = 256;   // output columns of a plain-product (down) tile
 constexpr int64_t kWideMinM = 256;   // from this many rows on, the wide down-projection kernel
+constexpr int64_t kSlimMaxM = 128;   // up to this many rows, and
+constexpr int kSlimMaxPairTiles = 8; // fewer 256-column tiles: the 1-SM plain kernel (64 columns)
 constexpr int64_t kPairMinM = 256;   // from this many tokens on, the 2-SM kernel
 using FusedC = FusedCfg<kFusedStages>;
 using Narrow64C = FusedCfg<kNarrow64Stages, 128>;
@@ -143,7 +145,11 @@ int device_setup(int *dev_out, DeviceState **st_out) {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairC::SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(down_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 WideCfg::SMEM_BYTES) != cudaSuccess) {
+                                 WideCfg::SMEM_BYTES) != cudaSuccess ||
+            // plain product on the 1-SM kernel (decode-sized down-projection)
+            cudaFuncSetAttribute(fused_up_kernel<kNarrow32Stages, 64, ElemBF16, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Narrow32C::SMEM_BYTES) != cudaSuccess) {
             cudaGetLastError();
             st.status = SWIGLU_ERR_CUDA;
             return;
@@ -272,23 +278,57 @@ WorkSched plan_down(int64_t M, int64_t N, int64_t K, int workers) {
                          mode);
 }
 
-// The down-projection's kernel and schedule. The wide kernel
-// (down_wide_kernel.cuh, tiles of 256 x 512) feeds the tensor cores with a
-// third fewer operand bytes per flop, which shows at the power cap as a
-// higher SM clock (7B, M=8192: 621 against 663 us, 1545 against 1432 MHz),
-// but it has one accumulator stage and its split tiles move whole 512-column
-// FP32 partials through L2; so it takes a call when whole wide tiles fill at
-// least 90% of their last wave (from kWideMinM rows on), as whole tiles. The
-// CTA-pair kernel's plain mode (256 x 256, plan_down) takes the rest: few
-// output tiles, where a K split is needed, and decode-sized products.
-// SWIGLU_DOWN_TILE=256|512, read on every call, forces one of them
+// Schedule of the plain product on the 1-SM kernel (tiles of 128 rows x 64
+// output columns, k-blocks over N): whole tiles when they fill at least 90%
+// of their last wave, else stream-K over the tiles past the last full wave,
+// or over all tiles when there are fewer tiles than SMs (the usual case: a
+// decode-sized down-projection has K/64 tiles, e.g. 56 for 7B). A split
+// tile's partials are 64 columns wide, summed by the last contributor.
+WorkSched plan_down_slim(int64_t M, int64_t N, int64_t K, int sms) {
+    const int m_tiles = static_cast<int>((M + FusedC::BM - 1) / FusedC::BM);
+    const int n_tiles = static_cast<int>((K + 63) / 64);
+    const int k_blocks = static_cast<int>((N + ElemBF16::kBK - 1) / ElemBF16::kBK);
+    int mode = schedule_mode_fused();
+    if (mode == kSchedColumnSplit) mode = kSchedAuto;
+    if (mode == kSchedAuto) {
+        const long long T = static_cast<long long>(m_tiles) * n_tiles;
+        const long long waves = (T + sms - 1) / sms;
+        const double eff = static_cast<double>(T) / (static_cast<double>(waves) * sms);
+        mode = eff >= 0.9 ? kSchedDataParallel : (T >= sms ? kSchedStreamKTail : kSchedStreamK);
+    }
+    const int grows = group_rows_override();
+    const int group_m = grows ? std::max(1, grows / FusedC::BM) : kGroupM;
+    return plan_schedule(m_tiles, n_tiles, k_blocks, sms, group_m, kMinStreamKIters, false, mode);
+}
+
+// The down-projection's kernel and schedule. Three kernels serve it, on the
+// same packed W3:
+//   * kDownWide (down_wide_kernel.cuh, CTA pairs, tiles of 256 x 512): a
+//     third fewer operand bytes per flop than 256-column tiles, which shows
+//     at the power cap as a higher SM clock (7B, M=8192: 631 against 666 us;
+//     72B, M=8192: 2261 against 2361 us), but one accumulator stage and
+//     512-column FP32 partials for split tiles; it takes a call when whole
+//     wide tiles fill at least 90% of their last wave (from kWideMinM rows
+//     on), as whole tiles;
+//   * kDownSlim (the 1-SM kernel's plain mode, tiles of 128 x 64): decode-
+//     sized products (up to kSlimMaxM rows) with a handful of 256-column
+//     tiles, where the CTA-pair kernel's K split would put ten or more pairs
+//     on each tile (0.5B, M=128: 21.8 against 41.1 us); with more output
+//     columns its 64-column tiles re-read A once per tile, which costs more
+//     than the pairs' larger partials (72B, M=32: 110 against 82 us), so the
+//     pairs keep those;
+//   * kDownPair (the CTA-pair kernel's plain mode, 256 x 256, plan_down):
+//     the rest (few output tiles for the pairs, e.g. the 1.5B and 7B M=2048
+//     shapes).
+// SWIGLU_DOWN_TILE=64|256|512, read on every call, forces one of them
 // (ablations and tests); with the wide kernel forced, SWIGLU_SCHEDULE picks
 // its form (dp, sk, sk-tail, sk-aligned; whole tiles otherwise).
+enum DownKind { kDownPair = 0, kDownWide = 1, kDownSlim = 2 };
 struct DownPlan {
-    bool wide;
+    int kind;
     WorkSched sched;
 };
-DownPlan plan_down_any(int64_t M, int64_t N, int64_t K, int workers) {
+DownPlan plan_down_any(int64_t M, int64_t N, int64_t K, int workers, int sms) {
     const int rows = WideCfg::UMMA_M;
     const int m_tiles = static_cast<int>((M + rows - 1) / rows);
     const int n_tiles = static_cast<int>((K + WideCfg::TILE_N - 1) / WideCfg::TILE_N);
@@ -296,15 +336,21 @@ DownPlan plan_down_any(int64_t M, int64_t N, int64_t K, int workers) {
     const long long T = static_cast<long long>(m_tiles) * n_tiles;
     const long long waves = (T + workers - 1) / workers;
     const double eff = static_cast<double>(T) / (static_cast<double>(waves) * workers);
-    bool wide = M >= kWideMinM && eff >= 0.9;
+    // the CTA-pair kernel's tiles for this product (256 x 256)
+    const long long pair_tiles = ((M + 255) / 256) * ((K + kDownTileCols - 1) / kDownTileCols);
+    int kind = (M <= kSlimMaxM && pair_tiles < kSlimMaxPairTiles)
+                   ? kDownSlim
+                   : (M >= kWideMinM && eff >= 0.9 ? kDownWide : kDownPair);
     const char *v = std::getenv("SWIGLU_DOWN_TILE");
-    if (v && std::strcmp(v, "256") == 0) wide = false;
-    if (v && std::strcmp(v, "512") == 0) wide = true;
-    if (!wide) return {false, plan_down(M, N, K, workers)};
+    if (v && std::strcmp(v, "64") == 0) kind = kDownSlim;
+    if (v && std::strcmp(v, "256") == 0) kind = kDownPair;
+    if (v && std::strcmp(v, "512") == 0) kind = kDownWide;
+    if (kind == kDownPair) return {kDownPair, plan_down(M, N, K, workers)};
+    if (kind == kDownSlim) return {kDownSlim, plan_down_slim(M, N, K, sms)};
     const int grows = group_rows_override();
     const int group_m = grows ? std::max(1, grows / rows) : kGroupM / 2;
-    return {true, plan_down_wide(m_tiles, n_tiles, k_blocks, workers, group_m, kMinStreamKIters,
-                                 schedule_mode())};
+    return {kDownWide, plan_down_wide(m_tiles, n_tiles, k_blocks, workers, group_m,
+                                      kMinStreamKIters, schedule_mode())};
 }
 
 // Which kernel serves a call, and its schedule: the 1-SM kernel below 256
@@ -363,7 +409,7 @@ size_t workspace_bytes_for(const WorkSched &s, int64_t M, bool pair, int sm_coun
 // The down-projection's: the wide kernel keeps 2 slots per worker and CTA
 // half of a whole FP32 partial tile half (128 rows x 512 columns).
 size_t down_workspace_bytes_for(const DownPlan &p, int64_t M, int sm_count) {
-    if (!p.wide) return workspace_bytes_for(p.sched, M, true, sm_count);
+    if (p.kind != kDownWide) return workspace_bytes_for(p.sched, M, p.kind == kDownPair, sm_count);
     if (p.sched.sk_iters == 0) return 0;
     return counter_region_bytes(sm_count) + static_cast<size_t>(2) * p.sched.grid * 2 *
                                                 WideCfg::SLOT_FLOATS * sizeof(float);
@@ -771,10 +817,10 @@ size_t down_workspace_bytes_impl(int64_t M, int64_t N, int64_t K) {
     int dev;
     DeviceState *st;
     if (device_setup(&dev, &st) == SWIGLU_OK)
-        return down_workspace_bytes_for(plan_down_any(M, N, K, st->pair_clusters), M,
-                                        st->sm_count);
+        return down_workspace_bytes_for(plan_down_any(M, N, K, st->pair_clusters, st->sm_count),
+                                        M, st->sm_count);
     const int sms = current_sm_count();
-    return down_workspace_bytes_for(plan_down_any(M, N, K, sms / 2), M, sms);
+    return down_workspace_bytes_for(plan_down_any(M, N, K, sms / 2, sms), M, sms);
 }
 
 // Argument checks of the plain product out [M, K] = Y [M, N] x W3 [N, K].
@@ -838,9 +884,60 @@ int down_wide_launch(const WorkSched &sched, const void *Y, const void *W3packed
     return SWIGLU_OK;
 }
 
+// The 1-SM kernel's plain-mode launch (plan from plan_down_any, checks done).
+int down_slim_launch(const WorkSched &sched, const void *Y, const void *W3packed, void *out,
+                     int64_t M, int64_t N, int64_t K, void *workspace, bool ws, int sm_count,
+                     void *stream) {
+    const int kt = static_cast<int>((K + kDownTileCols - 1) / kDownTileCols);
+    const uint64_t weight_tiles = static_cast<uint64_t>(kt) * static_cast<uint64_t>(sched.k_blocks);
+    const int a_rows = M >= FusedC::BM ? FusedC::BM : static_cast<int>(round_up(M, 8));
+    CUtensorMap tmA, tmB, tmOut;
+    if (!encode_2d(&tmA, Y, N, M, ElemBF16::kBK, a_rows) ||
+        !encode_packed_weights(&tmB, W3packed, weight_tiles, 64u, false) ||
+        !encode_2d(&tmOut, out, K, M, 64, 32))
+        return SWIGLU_ERR_CUDA;
+    FusedArgs args{};
+    args.M = static_cast<int>(M);
+    args.N = static_cast<int>(K);   // output columns
+    args.K = static_cast<int>(N);   // reduction
+    args.stage_tx_bytes = a_rows * kRowBytes + 64 * kRowBytes;
+    args.a_tx_bytes = a_rows * kRowBytes;
+    args.Y = static_cast<uint16_t *>(out);
+    args.gate_scale = 1.0f;
+    args.up_scale = 1.0f;
+    args.slot_rows = slot_rows_for(M);
+    args.sched = sched;
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+    args.skip_first_fill = g_test_skip_first_fill;
+#endif
+    args.counters = ws ? static_cast<unsigned int *>(workspace) : nullptr;
+    args.partials = ws ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                   counter_region_bytes(sm_count))
+                       : nullptr;
+    args.ticket_index = ticket_index(sm_count);
+    args.tile_counter_index = tile_counter_index(sm_count);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(sched.grid));
+    cfg.blockDim = dim3(Narrow32C::THREADS);
+    cfg.dynamicSmemBytes = Narrow32C::SMEM_BYTES;
+    const cudaError_t err =
+        cudaLaunchKernelEx(&cfg, fused_up_kernel<kNarrow32Stages, 64, ElemBF16, false, true>, tmA,
+                           tmB, tmB, tmB, tmOut, args);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SWIGLU_ERR_CUDA;
+    }
+    return SWIGLU_OK;
+}
+
 // out [M, K] = Y [M, N] x W3 [N, K] (W3 packed by swiglu_pack_down_weights),
-// BF16 in and out, FP32 accumulation: the wide kernel, or the CTA-pair
-// kernel in its plain mode (plan_down_any).
+// BF16 in and out, FP32 accumulation, on the kernel plan_down_any picks.
 int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M, int64_t N,
                       int64_t K, void *workspace, size_t workspace_bytes, void *stream) {
     const int c = down_checks(Y, W3packed, out, M, N, K);
@@ -853,7 +950,7 @@ int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M,
     DeviceState *st;
     const int s = device_setup(&dev, &st);
     if (s != SWIGLU_OK) return s;
-    const DownPlan plan = plan_down_any(M, N, K, st->pair_clusters);
+    const DownPlan plan = plan_down_any(M, N, K, st->pair_clusters, st->sm_count);
     const WorkSched &sched = plan.sched;
     const size_t ws_need = down_workspace_bytes_for(plan, M, st->sm_count);
     if (ws_need > 0) {
@@ -864,8 +961,11 @@ int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M,
             overlaps(workspace, ws_need, W3packed, pbytes))
             return SWIGLU_ERR_INVALID_ARG;
     }
-    if (plan.wide)
+    if (plan.kind == kDownWide)
         return down_wide_launch(sched, Y, W3packed, out, M, N, K, workspace, ws_need > 0,
+                                st->sm_count, stream);
+    if (plan.kind == kDownSlim)
+        return down_slim_launch(sched, Y, W3packed, out, M, N, K, workspace, ws_need > 0,
                                 st->sm_count, stream);
     const uint64_t weight_tiles =
         static_cast<uint64_t>(sched.order.n_tiles) * static_cast<uint64_t>(sched.k_blocks);

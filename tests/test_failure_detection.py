@@ -94,11 +94,12 @@ def test_wait_timeout_is_reported_and_context_survives(fi_lib, monkeypatch, vari
     assert r["mismatches"] == 0 and r["over_bound"] == 0, r
 
 
-@pytest.mark.parametrize("tile", ["256", "512"])
+@pytest.mark.parametrize("tile", ["64", "256", "512"])
 @pytest.mark.parametrize("mode,M,N,K", [("auto", 512, 2048, 512), ("dp", 512, 512, 512)])
 def test_down_projection_wait_timeout(fi_lib, monkeypatch, tile, mode, M, N, K):
-    """The same for the down-projection, on both of its kernels (the
-    CTA-pair kernel's plain mode, tile 256, and the wide kernel, tile 512),
+    """The same for the down-projection, on each of its kernels (the 1-SM
+    kernel's plain mode, tile 64, the CTA-pair kernel's plain mode, tile 256,
+    and the wide kernel, tile 512),
     with stream-K split tiles (auto: 4 or 2 output tiles on many pairs) and
     with whole tiles: the timeout is reported and the next call is correct."""
     monkeypatch.setenv("SWIGLU_DOWN_TILE", tile)

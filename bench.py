@@ -500,6 +500,80 @@ def sweep(sg, peaks, dtype, dev, stream, sampler, window_s: float, labels):
     return out
 
 
+DOWN_SWEEP_LABELS = ("0", "1", "3", "5", "6", "7", "9", "10", "11")
+
+
+def down_sweep(sg, dev, stream, sampler, window_s: float, labels=DOWN_SWEEP_LABELS):
+    """The down-projection out = Y W3 (Y [M, N], W3 [N, K]) of the gated MLP
+    at the workloads' shapes, this library's kernel (whichever it picks)
+    against cuBLAS (torch.matmul) on the same rotating inputs (Y ~ N(0, 1),
+    W3 ~ N(0, 1/N), drawn on the GPU, seeded): CUDA graphs replayed for
+    `window_s` seconds each, in the order ours, cuBLAS, ours, cuBLAS, so that
+    neither side gets the cooler GPU; each side's number is its faster
+    window, with the SM clock of that window. BF16."""
+    import torch
+
+    import workloads
+    out = []
+    for label in labels:
+        w = workloads.BY_LABEL[label]
+        M, N, K = w.M, w.N, w.K
+        per = 2 * (M * N + N * K + M * K)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        R = max(2, min(8, int(2.5 * l2 // per) + 1))   # the sets exceed twice the L2
+        g = torch.Generator(device=dev)
+        g.manual_seed(7000 + w.seed_index)
+        Ys = [torch.randn(M, N, generator=g, device=dev).to(torch.bfloat16) for _ in range(R)]
+        W3s = [(torch.randn(N, K, generator=g, device=dev) * N ** -0.5).to(torch.bfloat16)
+               for _ in range(R)]
+        W3ps = [sg.swiglu_pack_down_weights(x) for x in W3s]
+        Os = [torch.empty(M, K, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        ws = sg.swiglu_down_workspace_bytes(M, N, K)
+        Wss = [torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev) for _ in range(R)]
+
+        def ours(i, st):
+            j = i % R
+            sg.swiglu_down_forward(Ys[j], W3ps[j], K, out=Os[j],
+                                   workspace=Wss[j] if ws else None, stream=st)
+
+        def cublas(i, st):
+            j = i % R
+            torch.matmul(Ys[j], W3s[j], out=Os[j])
+
+        flops = 2.0 * M * N * K
+        graphs = {}
+        for name, fn in (("ours", ours), ("cublas", cublas)):
+            with torch.cuda.stream(stream):
+                for i in range(R):
+                    fn(i, stream)
+            torch.cuda.synchronize(dev)
+            est = max(flops / 1.5e15, per / R / 6e12)
+            n = graph_launches(R, est)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                cs = torch.cuda.current_stream(dev)
+                for i in range(n):
+                    fn(i, cs)
+            graphs[name] = (gr, n)
+        best = {}
+        for name in ("ours", "cublas", "ours", "cublas"):
+            gr, n = graphs[name]
+            el, rounds, t0, t1 = replay_window([gr], stream, dev, window_s)
+            us = el / (n * rounds) * 1e6
+            if name not in best or us < best[name][0]:
+                best[name] = (us, sampler.summary(t0, t1, min_samples=2))
+        sg.swiglu_check_device_status(stream)
+        e = {"workload": label, "name": w.name, "M": M, "N": N, "K": K}
+        for name in ("ours", "cublas"):
+            us, clk = best[name]
+            e[name] = {"us": us, "tflops": flops / (us * 1e-6) / 1e12, "clocks": clk}
+        e["ours_over_cublas_time"] = best["ours"][0] / best["cublas"][0]
+        out.append(e)
+        del graphs, Ys, W3s, W3ps, Os, Wss
+        torch.cuda.empty_cache()
+    return out
+
+
 ABLATION_FORMS = (
     # (packed layout, kernel variant, schedule form); "auto" = the library's choice
     [(layout, "auto", mode) for layout in ("blocked", "interleaved")
@@ -986,6 +1060,9 @@ def run_gb300(args, w):
         import workloads
         labels = [x.c for x in workloads.WORKLOADS]
         sweep_out = sweep(sg, peaks, args.dtype, dev, stream, sampler, args.sweep_window_s, labels)
+    down_out = None
+    if world == 1 and not args.no_context and not args.no_sweep and not fp8:
+        down_out = down_sweep(sg, dev, stream, sampler, min(args.sweep_window_s, 0.15))
     sampler.stop()
 
     if rank != 0:
@@ -1043,6 +1120,8 @@ def run_gb300(args, w):
         line["context_unfused_torch"] = unfused
     if mlp is not None:
         line["context_mlp"] = mlp
+    if down_out is not None:
+        line["context_down"] = down_out
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inputs)
     print(json.dumps(line), flush=True)

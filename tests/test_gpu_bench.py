@@ -63,6 +63,33 @@ def test_bench_prints_one_contract_line(dtype):
         assert e["bound"] == ("hbm" if w.M <= 128 else "tensor"), e
 
 
+def test_bench_context_down_projection():
+    """With the context on: the whole MLP at the bench workload and the
+    down-projection sweep (this library against cuBLAS at the workloads'
+    down-projection shapes, alternating windows, clocks per window)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "0", "--steps", "20",
+           "--warmup", "3", "--no-cpu-baseline", "--sustained-s", "0", "--sweep-window-s", "0.03"]
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    r = json.loads(lines[0])
+    import bench
+    import workloads
+    assert "context_mlp" in r and r["context_mlp"]["fused_mlp_ms"] > 0
+    cd = r["context_down"]
+    assert [e["workload"] for e in cd] == list(bench.DOWN_SWEEP_LABELS)
+    for e in cd:
+        w = workloads.BY_LABEL[e["workload"]]
+        assert (e["M"], e["N"], e["K"]) == (w.M, w.N, w.K)
+        for side in ("ours", "cublas"):
+            assert e[side]["us"] > 0 and e[side]["tflops"] > 0, e
+            assert "sm_mhz" in e[side]["clocks"], e
+        assert e["ours_over_cublas_time"] == pytest.approx(e["ours"]["us"] / e["cublas"]["us"])
+
+
 @pytest.mark.parametrize("world", [2, 3])
 def test_column_split_ranks_reassemble_the_whole_forward(world, monkeypatch):
     """What each rank of `bench.py --split columns` runs, done here for every

@@ -21,9 +21,12 @@
 // first stages. With a long reduction (the MLP's intermediate size) a tile
 // lasts hundreds of k-blocks and the exposed TMEM read is a small fraction.
 //
-// Work split (schedule.cuh, plan_down_wide): whole tiles, stream-K over the
-// tiles past the last full wave, or stream-K over all tiles (few output
-// tiles). A tile split between the K ranges of pairs c_lo..c_hi is finished
+// Work split (schedule.cuh, plan_down_wide): whole tiles, which the library
+// picks when they fill their last wave to 90% (the extra operand bytes saved
+// per flop leave more of the power cap to the SMs: a higher clock at the same
+// work per cycle); or, forced for ablations, stream-K over the tiles past the
+// last full wave, stream-K over all tiles, or every tile cut into equal K
+// ranges. A tile split between the K ranges of pairs c_lo..c_hi is finished
 // without any CTA waiting for another: its 512 accumulator columns form four
 // parts of 128. Each participant CTA writes each part of its FP32 partial to
 // its workspace slot and counts itself in on that part's counter; whoever
@@ -36,7 +39,11 @@
 // signaler also brings the other partials of its parts into the then idle
 // operand ring with bulk copies. No wait depends on another cluster, so the
 // call completes whatever else occupies the GPU, and the sums do not depend
-// on who finishes.
+// on who finishes. (Measured: the split forms move whole 512-column FP32
+// partials through L2 -- 256 KB per CTA -- and, with many tiles in flight at
+// different K offsets, lose the L2 sharing of whole tiles; neither is cheaper
+// than the CTA-pair kernel's 256-column split tiles on the shapes that need a
+// split, so the library does not pick them.)
 //
 // Every wait is bounded (sm103_ptx.cuh); an abort sets both CTAs' abort
 // flags, and the teardown drains loads and MMAs in flight before TMEM is

@@ -830,10 +830,21 @@ def time_mlp_context(w, W1, W2, sg, p, dev, stream, steps):
         j = i % R
         sg.swiglu_down_forward(Ys[j], W3ps[j], w.K, out=O[j], workspace=MWs[j], stream=stream)
 
-    eager_ms = timed(eager)
-    fused_ms = timed(fused)
-    fused_cublas_ms = timed(fused_cublas_down)
-    down_ms = timed(down)
+    # The whole-MLP variants and the two down-projections in alternating
+    # rounds, the faster of two rounds each: timed one after the other, the
+    # later ones ran on a warmer GPU at a lower clock under the power cap.
+    def down_cublas(i):
+        ops["down_gemm"](i)
+
+    variants = (("eager", eager), ("fused", fused), ("fused_cublas", fused_cublas_down),
+                ("down", down), ("down_cublas", down_cublas))
+    best = {}
+    for _ in range(2):
+        for name, fn in variants:
+            t = timed(fn)
+            best[name] = min(t, best.get(name, t))
+    eager_ms, fused_ms, fused_cublas_ms = best["eager"], best["fused"], best["fused_cublas"]
+    down_ms = best["down"]
     mlp_flops = w.flops + 2 * w.M * w.N * w.K
     down_flops = 2 * w.M * w.N * w.K
     del W1s, W2s, W3s, W3ps, MWs, G, U, O
@@ -842,14 +853,15 @@ def time_mlp_context(w, W1, W2, sg, p, dev, stream, steps):
             "fused_mlp_tflops": mlp_flops / (fused_ms * 1e-3) / 1e12,
             "fused_up_cublas_down_mlp_ms": fused_cublas_ms,
             "down_ms": down_ms, "down_tflops": down_flops / (down_ms * 1e-3) / 1e12,
-            "down_cublas_ms": op_ms["down_gemm"],
+            "down_cublas_ms": best["down_cublas"],
             "eager_op_ms": op_ms,
             "activation_share_of_eager_mlp": op_ms["silu_mul"] / sum(op_ms.values()),
             "what": "out = (SiLU(A W1) * (A W2)) W3, W3 [N, K] ~ N(0, 1/N) synthetic; fused = this "
                     "library's swiglu_mlp_forward (fused up-projection + its down-projection "
                     "kernel); eager = 3 cuBLAS GEMMs + silu*mul (Figure 1 of the pages measures "
-                    "this share on H100); down_* = the down-projection alone, this library's "
-                    "kernel and cuBLAS"}
+                    "this share on H100; eager_op_ms times each op alone, one after the other); "
+                    "down_* = the down-projection alone, this library's kernel and cuBLAS; the "
+                    "MLP variants and down_* in two alternating rounds, the faster of each"}
 
 
 def config_of(w, l2_note, dtype: str = "bf16", split: str = "replicas", world: int = 1):

@@ -75,7 +75,8 @@ struct FusedCfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_Y = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_BAR = OFF_Y + EPI_WARPS * Y_WARP_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull x2, tempty x2, drain
+    // full, empty, tfull x2, tempty x2, drain, fix (bulk copies of split partials)
+    static constexpr int NUM_BARS = 2 * STAGES + 6;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag, last flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + 1 KB alignment slack
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
     auto tfull_bar = [&](int a) { return sbase + C::OFF_BAR + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return sbase + C::OFF_BAR + 8u * (2 * STAGES + 2 + a); };
     const uint32_t drain_bar = sbase + C::OFF_BAR + 8u * (2 * STAGES + 4);
+    const uint32_t fix_bar = sbase + C::OFF_BAR + 8u * (2 * STAGES + 5);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     volatile int *last_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);
@@ -135,6 +137,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
             mbar_init(tempty_bar(a), C::EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(fix_bar, 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_barrier_init();
@@ -322,6 +325,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
         const int row_in_tile = 32 * quad + lane;
         const uint32_t ybuf = sbase + C::OFF_Y + (warp - 2) * C::Y_WARP_BYTES;
         const bool leader = (warp == 2 && lane == 0);
+        uint32_t fix_phase = 0;   // bulk copies of split partials (plain product)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
@@ -404,18 +408,92 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
                     epilogue_bar();
                     if (*last_flag != 0) {
                         __threadfence();
-                        if (rows_live) {
-                            // the partials of four contributors are loaded
-                            // before any is added, so a tile split many ways
-                            // waits for a quarter as many load round trips
+                        // The sum of every contributor's partial, in k order.
+                        // When this is the CTA's last unit its operand ring
+                        // is idle (all its MMAs are complete): the partials'
+                        // 64 columns (contiguous at the start of each slot)
+                        // come in by bulk copies, as many per round as the
+                        // ring holds; otherwise by loads, four contributors'
+                        // at a time.
+                        UnitIter peek = it;
+                        Unit after;
+                        const bool last_unit = !peek.next(after);
+                        const uint32_t part_bytes = 64u * static_cast<uint32_t>(args.slot_rows) * 4u;
+                        constexpr uint32_t kRingBytes = STAGES * (C::A_BYTES + C::B_BYTES);
+                        const int per_round = static_cast<int>(kRingBytes / part_bytes);
+                        if (last_unit && per_round >= 2) {
+                            // round 1 brings the first per_round partials to
+                            // slots 0..; later rounds bring the next ones to
+                            // slots 1.. and add to the running sum in slot 0
+                            float *ring = reinterpret_cast<float *>(smem);
+                            for (int k0 = c_lo; k0 <= c_hi && ok;) {
+                                const int first = k0 == c_lo ? 0 : 1;
+                                const int room = per_round - first;
+                                const int cnt = (c_hi - k0 + 1 < room) ? c_hi - k0 + 1 : room;
+                                if (leader) {
+                                    fence_proxy_async_global();
+                                    mbar_arrive_expect_tx(fix_bar, static_cast<uint32_t>(cnt) * part_bytes);
+                                    for (int q = 0; q < cnt; ++q)
+                                        bulk_copy_g2s(sbase + static_cast<uint32_t>(first + q) * part_bytes,
+                                                      args.partials +
+                                                          static_cast<size_t>(2 * (k0 + q) +
+                                                                              sched.sk_slot(k0 + q, u.sk)) *
+                                                              slot_floats,
+                                                      part_bytes, fix_bar);
+                                }
+                                ok = epilogue_all(mbar_wait(fix_bar, fix_phase, abort_flag));
+                                fix_phase ^= 1u;
+                                if (!ok) break;
+                                if (rows_live) {
+                                    // k order: slot 0 (the partials so far), then the new
+                                    // ones; 32 columns at a time, each slot's 32 values
+                                    // loaded before they are added (shared-memory latency
+                                    // overlapped, not one dependent load per add)
+#pragma unroll 1
+                                    for (int c = 0; c < 64; c += 32) {
+                                        float *cell = ring + static_cast<size_t>(c) * args.slot_rows + row_in_tile;
+                                        float x[32];
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i) x[i] = cell[static_cast<size_t>(i) * args.slot_rows];
+#pragma unroll 1
+                                        for (int q = 1; q < first + cnt; ++q) {
+                                            const float *src = cell + static_cast<size_t>(q) * 64 * args.slot_rows;
+                                            float v[32];
+#pragma unroll
+                                            for (int i = 0; i < 32; ++i) v[i] = src[static_cast<size_t>(i) * args.slot_rows];
+#pragma unroll
+                                            for (int i = 0; i < 32; ++i) x[i] += v[i];
+                                        }
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i) cell[static_cast<size_t>(i) * args.slot_rows] = x[i];
+                                    }
+                                }
+                                k0 += cnt;
+                                epilogue_bar();   // the ring is read before the next round lands
+                            }
+                            if (ok && rows_live) {
+                                const float *sum = reinterpret_cast<const float *>(smem);
+#pragma unroll 1
+                                for (int c = 0; c < 64; c += 32) {
+                                    float x[32];
+#pragma unroll
+                                    for (int i = 0; i < 32; ++i)
+                                        x[i] = sum[static_cast<size_t>(c + i) * args.slot_rows + row_in_tile];
+                                    store_plain32(row0 + lane, col0 + c, x, args);
+                                }
+                            }
+                        } else if (rows_live) {
+                            // the partials of two contributors are loaded
+                            // before either is added (half as many load round
+                            // trips as one at a time)
 #pragma unroll 1
                             for (int c = 0; c < 64; c += 32) {
                                 float x[32];
 #pragma unroll 1
-                                for (int k0 = c_lo; k0 <= c_hi; k0 += 4) {
-                                    float v[4][32];
+                                for (int k0 = c_lo; k0 <= c_hi; k0 += 2) {
+                                    float v[2][32];
 #pragma unroll
-                                    for (int q = 0; q < 4; ++q) {
+                                    for (int q = 0; q < 2; ++q) {
                                         if (k0 + q > c_hi) break;
                                         const int k = k0 + q;
                                         const float *src = args.partials +
@@ -427,7 +505,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
                                                                        args.slot_rows + row_in_tile);
                                     }
 #pragma unroll
-                                    for (int q = 0; q < 4; ++q) {
+                                    for (int q = 0; q < 2; ++q) {
                                         if (k0 + q > c_hi) break;
 #pragma unroll
                                         for (int i = 0; i < 32; ++i)

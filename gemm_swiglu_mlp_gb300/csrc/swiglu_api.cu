@@ -279,25 +279,40 @@ WorkSched plan_down(int64_t M, int64_t N, int64_t K, int workers) {
 }
 
 // Schedule of the plain product on the 1-SM kernel (tiles of 128 rows x 64
-// output columns, k-blocks over N): whole tiles when they fill at least 90%
-// of their last wave, else stream-K over the tiles past the last full wave,
-// or over all tiles when there are fewer tiles than SMs (the usual case: a
-// decode-sized down-projection has K/64 tiles, e.g. 56 for 7B). A split
-// tile's partials are 64 columns wide, summed by the last contributor.
+// output columns, k-blocks over N). A decode-sized product streams W3 from
+// HBM, and the four 64-column tiles of one packed 256-column weight tile read
+// the four 8 KB quarters of each 32 KB block: they should do so at the same
+// time. So with fewer tiles than SMs every tile is cut into j = floor(SMs /
+// tiles) equal K ranges, one per CTA (each CTA one unit; the j CTAs of a
+// range index r of the four sibling tiles run in step), as long as a range
+// keeps kMinStreamKIters k-blocks; with j = 1, whole tiles. Stream-K over all
+// tiles on all SMs had the siblings at unrelated k offsets (7B, M=16: the
+// weights arrived at ~4.4 TB/s). With at least as many tiles as SMs: whole
+// tiles when they fill 90% of the last wave, else stream-K over the tail.
 WorkSched plan_down_slim(int64_t M, int64_t N, int64_t K, int sms) {
     const int m_tiles = static_cast<int>((M + FusedC::BM - 1) / FusedC::BM);
     const int n_tiles = static_cast<int>((K + 63) / 64);
     const int k_blocks = static_cast<int>((N + ElemBF16::kBK - 1) / ElemBF16::kBK);
-    int mode = schedule_mode_fused();
-    if (mode == kSchedColumnSplit) mode = kSchedAuto;
-    if (mode == kSchedAuto) {
-        const long long T = static_cast<long long>(m_tiles) * n_tiles;
-        const long long waves = (T + sms - 1) / sms;
-        const double eff = static_cast<double>(T) / (static_cast<double>(waves) * sms);
-        mode = eff >= 0.9 ? kSchedDataParallel : (T >= sms ? kSchedStreamKTail : kSchedStreamK);
-    }
     const int grows = group_rows_override();
     const int group_m = grows ? std::max(1, grows / FusedC::BM) : kGroupM;
+    int mode = schedule_mode_fused();
+    if (mode == kSchedColumnSplit) mode = kSchedAuto;
+    const long long T = static_cast<long long>(m_tiles) * n_tiles;
+    if (mode == kSchedAuto && T < sms) {
+        const int j = std::min(static_cast<int>(sms / T), k_blocks / kMinStreamKIters);
+        if (j >= 2) {
+            const WorkSched s = plan_schedule(m_tiles, n_tiles, k_blocks, static_cast<int>(j * T),
+                                              group_m, kMinStreamKIters, false, kSchedStreamK);
+            if (s.grid == j * T && s.dp_tiles == 0) return s;
+        }
+        return plan_schedule(m_tiles, n_tiles, k_blocks, sms, group_m, kMinStreamKIters, false,
+                             kSchedDataParallel);
+    }
+    if (mode == kSchedAuto) {
+        const long long waves = (T + sms - 1) / sms;
+        const double eff = static_cast<double>(T) / (static_cast<double>(waves) * sms);
+        mode = eff >= 0.9 ? kSchedDataParallel : kSchedStreamKTail;
+    }
     return plan_schedule(m_tiles, n_tiles, k_blocks, sms, group_m, kMinStreamKIters, false, mode);
 }
 

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "down_decode_kernel.cuh"
 #include "down_wide_kernel.cuh"
 #include "fused_up_kernel.cuh"
 #include "fused_up_pair_kernel.cuh"
@@ -33,6 +34,7 @@ constexpr int64_t kWideMinM = 256;   // from this many rows on, the wide down-pr
 constexpr int64_t kSlimMaxM = 128;   // up to this many rows, and
 constexpr int kSlimMaxPairTiles = 8; // fewer 256-column tiles: the 1-SM plain kernel (64 columns)
 constexpr int64_t kPairMinM = 256;   // from this many tokens on, the 2-SM kernel
+constexpr int64_t kDecodeMaxM = 128; // up to this many rows: the decode down-projection kernel
 using FusedC = FusedCfg<kFusedStages>;
 using Narrow64C = FusedCfg<kNarrow64Stages, 128>;
 using Narrow32C = FusedCfg<kNarrow32Stages, 64>;
@@ -58,6 +60,9 @@ struct DeviceState {
     int status = SWIGLU_OK;  // result of the one-time setup
     int sm_count = 0;
     int pair_clusters = 0;   // CTA pairs of the 2-SM kernel that can run at once
+    // clusters of j CTAs of the decode down-projection kernel that can run at
+    // once, j = 1..kDecodeMaxSplits (0: that size cannot be launched)
+    int decode_clusters[kDecodeMaxSplits + 1] = {};
 };
 
 DeviceState g_devices[kMaxDevices];
@@ -149,7 +154,21 @@ int device_setup(int *dev_out, DeviceState **st_out) {
             // plain product on the 1-SM kernel (decode-sized down-projection)
             cudaFuncSetAttribute(fused_up_kernel<kNarrow32Stages, 64, ElemBF16, false, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Narrow32C::SMEM_BYTES) != cudaSuccess) {
+                                 Narrow32C::SMEM_BYTES) != cudaSuccess ||
+            // the decode down-projection kernel (swapped operands), per token block
+            cudaFuncSetAttribute(down_decode_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 DecodeCfg<32>::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(down_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 DecodeCfg<64>::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(down_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 DecodeCfg<128>::SMEM_BYTES) != cudaSuccess ||
+            // its clusters of up to 16 CTAs (more than the portable 8)
+            cudaFuncSetAttribute(down_decode_kernel<32>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+            cudaFuncSetAttribute(down_decode_kernel<64>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+            cudaFuncSetAttribute(down_decode_kernel<128>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
             cudaGetLastError();
             st.status = SWIGLU_ERR_CUDA;
             return;
@@ -177,6 +196,28 @@ int device_setup(int *dev_out, DeviceState **st_out) {
         };
         const int pairs = max_clusters(2, fused_up_pair_kernel<kPairStages, ElemBF16>);
         st.pair_clusters = pairs >= 1 ? pairs : sms / 2;
+        // the decode kernel's clusters (a cluster sits inside one GPC: how
+        // many of j CTAs fit depends on the GPCs' SM counts, not only on sms / j)
+        for (int j = 1; j <= kDecodeMaxSplits; ++j) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(j);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(j * std::max(1, sms / j)));
+            cfg.blockDim = dim3(DecodeCfg<128>::THREADS);
+            cfg.dynamicSmemBytes = DecodeCfg<128>::SMEM_BYTES;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, down_decode_kernel<128>, &cfg) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                clusters = 0;
+            }
+            st.decode_clusters[j] = std::min(clusters, sms / j);
+        }
         st.sm_count = sms;
         st.status = SWIGLU_OK;
     });
@@ -316,8 +357,52 @@ WorkSched plan_down_slim(int64_t M, int64_t N, int64_t K, int sms) {
     return plan_schedule(m_tiles, n_tiles, k_blocks, sms, group_m, kMinStreamKIters, false, mode);
 }
 
-// The down-projection's kernel and schedule. Three kernels serve it, on the
+// Split of the decode down-projection kernel (down_decode_kernel.cuh): its
+// T = ceil(K / 128) tiles of 128 output columns (all token rows at once) are
+// each cut into j equal K ranges, one per CTA, the j CTAs of a tile forming a
+// cluster. The automatic j is the smallest that puts at least two thirds of
+// the SMs to work in one wave (T clusters of j fitting at once: `clusters[j]`,
+// from the occupancy query), with at least kDecodeMinKb k-blocks per range;
+// failing that, the j with the most CTAs in one wave; j = 1 (whole tiles, no
+// cluster) when T is the SM count or more. Measured on GB300 (graph-replayed
+// calls, us): 7B M=16 (28 tiles) j=3 30.0, j=4 24.5, j=5 25.4; 32B M=64 (40
+// tiles) j=2 61.6, j=3 46.1; 72B M=32 (64 tiles) j=2 76.3; the 0.5B shape
+// (7 tiles) j=8 8.6, j=16 8.3. The extra SMs of the larger j add no weight
+// bandwidth once about two thirds stream, while idle SMs let the next
+// launch's CTAs start their prologue early. SWIGLU_SCHEDULE=dp forces j = 1,
+// SWIGLU_DECODE_SPLITS=<j> any j (clamped to 1..16 and the k-blocks; more
+// clusters than fit at once then run in waves); both are read on every call.
+constexpr int kDecodeMinKb = 4;
+int plan_down_decode(int64_t N, int64_t K, int sms, const int *clusters) {
+    const int64_t T = (K + 127) / 128;
+    const int k_blocks = static_cast<int>((N + ElemBF16::kBK - 1) / ElemBF16::kBK);
+    const int jmax = std::min(kDecodeMaxSplits, k_blocks);
+    if (const char *v = std::getenv("SWIGLU_DECODE_SPLITS")) {
+        const int j = std::atoi(v);
+        if (j >= 1) return std::min(j, jmax);
+    }
+    if (schedule_mode() == kSchedDataParallel || T >= sms) return 1;
+    const int64_t target = (2 * static_cast<int64_t>(sms) + 2) / 3;
+    int best = 1;
+    int64_t best_ctas = T;
+    for (int j = 2; j <= jmax; ++j) {
+        if (k_blocks / j < kDecodeMinKb) break;
+        const int fit = clusters ? clusters[j] : sms / j;
+        if (fit < T || T * j > sms) continue;
+        if (T * j >= target) return j;
+        if (T * j > best_ctas) {
+            best = j;
+            best_ctas = T * j;
+        }
+    }
+    return best;
+}
+
+// The down-projection's kernel and schedule. Four kernels serve it, on the
 // same packed W3:
+//   * kDownDecode (down_decode_kernel.cuh, swapped operands: tiles of 128
+//     output columns x all token rows, split K ranges summed inside a
+//     cluster, plan_down_decode): every product of up to kDecodeMaxM rows;
 //   * kDownWide (down_wide_kernel.cuh, CTA pairs, tiles of 256 x 512): a
 //     third fewer operand bytes per flop than 256-column tiles, which shows
 //     at the power cap as a higher SM clock (7B, M=8192: 631 against 666 us;
@@ -338,12 +423,17 @@ WorkSched plan_down_slim(int64_t M, int64_t N, int64_t K, int sms) {
 // SWIGLU_DOWN_TILE=64|256|512, read on every call, forces one of them
 // (ablations and tests); with the wide kernel forced, SWIGLU_SCHEDULE picks
 // its form (dp, sk, sk-tail, sk-aligned; whole tiles otherwise).
-enum DownKind { kDownPair = 0, kDownWide = 1, kDownSlim = 2 };
+enum DownKind { kDownPair = 0, kDownWide = 1, kDownSlim = 2, kDownDecode = 3 };
 struct DownPlan {
     int kind;
     WorkSched sched;
+    int splits;   // kDownDecode: K ranges per tile (cluster size)
 };
-DownPlan plan_down_any(int64_t M, int64_t N, int64_t K, int workers, int sms) {
+// `decode_clusters`: DeviceState::decode_clusters, or null (no device: the
+// decode split is then planned as if clusters of any size filled the GPU,
+// which changes nothing the caller sees, as that kernel needs no workspace).
+DownPlan plan_down_any(int64_t M, int64_t N, int64_t K, int workers, int sms,
+                       const int *decode_clusters) {
     const int rows = WideCfg::UMMA_M;
     const int m_tiles = static_cast<int>((M + rows - 1) / rows);
     const int n_tiles = static_cast<int>((K + WideCfg::TILE_N - 1) / WideCfg::TILE_N);
@@ -353,19 +443,25 @@ DownPlan plan_down_any(int64_t M, int64_t N, int64_t K, int workers, int sms) {
     const double eff = static_cast<double>(T) / (static_cast<double>(waves) * workers);
     // the CTA-pair kernel's tiles for this product (256 x 256)
     const long long pair_tiles = ((M + 255) / 256) * ((K + kDownTileCols - 1) / kDownTileCols);
-    int kind = (M <= kSlimMaxM && pair_tiles < kSlimMaxPairTiles)
+    int kind = M <= kDecodeMaxM ? kDownDecode
+               : (M <= kSlimMaxM && pair_tiles < kSlimMaxPairTiles)
                    ? kDownSlim
                    : (M >= kWideMinM && eff >= 0.9 ? kDownWide : kDownPair);
     const char *v = std::getenv("SWIGLU_DOWN_TILE");
     if (v && std::strcmp(v, "64") == 0) kind = kDownSlim;
+    if (v && std::strcmp(v, "128") == 0 && M <= kDecodeMaxM) kind = kDownDecode;
     if (v && std::strcmp(v, "256") == 0) kind = kDownPair;
     if (v && std::strcmp(v, "512") == 0) kind = kDownWide;
-    if (kind == kDownPair) return {kDownPair, plan_down(M, N, K, workers)};
-    if (kind == kDownSlim) return {kDownSlim, plan_down_slim(M, N, K, sms)};
+    if (kind == kDownDecode)
+        return {kDownDecode, WorkSched{}, plan_down_decode(N, K, sms, decode_clusters)};
+    if (kind == kDownPair) return {kDownPair, plan_down(M, N, K, workers), 1};
+    if (kind == kDownSlim) return {kDownSlim, plan_down_slim(M, N, K, sms), 1};
     const int grows = group_rows_override();
     const int group_m = grows ? std::max(1, grows / rows) : kGroupM / 2;
-    return {kDownWide, plan_down_wide(m_tiles, n_tiles, k_blocks, workers, group_m,
-                                      kMinStreamKIters, schedule_mode())};
+    return {kDownWide,
+            plan_down_wide(m_tiles, n_tiles, k_blocks, workers, group_m, kMinStreamKIters,
+                           schedule_mode()),
+            1};
 }
 
 // Which kernel serves a call, and its schedule: the 1-SM kernel below 256
@@ -424,6 +520,7 @@ size_t workspace_bytes_for(const WorkSched &s, int64_t M, bool pair, int sm_coun
 // The down-projection's: the wide kernel keeps 2 slots per worker and CTA
 // half of a whole FP32 partial tile half (128 rows x 512 columns).
 size_t down_workspace_bytes_for(const DownPlan &p, int64_t M, int sm_count) {
+    if (p.kind == kDownDecode) return 0;   // split tiles are summed inside their cluster
     if (p.kind != kDownWide) return workspace_bytes_for(p.sched, M, p.kind == kDownPair, sm_count);
     if (p.sched.sk_iters == 0) return 0;
     return counter_region_bytes(sm_count) + static_cast<size_t>(2) * p.sched.grid * 2 *
@@ -832,10 +929,11 @@ size_t down_workspace_bytes_impl(int64_t M, int64_t N, int64_t K) {
     int dev;
     DeviceState *st;
     if (device_setup(&dev, &st) == SWIGLU_OK)
-        return down_workspace_bytes_for(plan_down_any(M, N, K, st->pair_clusters, st->sm_count),
-                                        M, st->sm_count);
+        return down_workspace_bytes_for(
+            plan_down_any(M, N, K, st->pair_clusters, st->sm_count, st->decode_clusters), M,
+            st->sm_count);
     const int sms = current_sm_count();
-    return down_workspace_bytes_for(plan_down_any(M, N, K, sms / 2, sms), M, sms);
+    return down_workspace_bytes_for(plan_down_any(M, N, K, sms / 2, sms, nullptr), M, sms);
 }
 
 // Argument checks of the plain product out [M, K] = Y [M, N] x W3 [N, K].
@@ -892,6 +990,66 @@ int down_wide_launch(const WorkSched &sched, const void *Y, const void *W3packed
     cfg.blockDim = dim3(WideCfg::THREADS);
     cfg.dynamicSmemBytes = WideCfg::SMEM_BYTES;
     const cudaError_t err = cudaLaunchKernelEx(&cfg, down_wide_kernel, tmA, tmB, tmOut, args);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SWIGLU_ERR_CUDA;
+    }
+    return SWIGLU_OK;
+}
+
+// The decode kernel's launch (plan from plan_down_any, checks done; M <= 128):
+// ceil(K / 128) * splits CTAs in clusters of `splits`; `clusters` as in
+// DeviceState (a size of which none fits is refused).
+int down_decode_launch(int splits, const int *clusters, const void *Y, const void *W3packed,
+                       void *out, int64_t M, int64_t N, int64_t K, void *stream) {
+    const int kt = static_cast<int>((K + kDownTileCols - 1) / kDownTileCols);
+    const int k_blocks = static_cast<int>((N + ElemBF16::kBK - 1) / ElemBF16::kBK);
+    const int64_t tiles = (K + 127) / 128;
+    if (splits < 1 || splits > kDecodeMaxSplits || splits > k_blocks ||
+        tiles * splits > int64_t(1) << 30 || (splits > 1 && clusters[splits] < 1))
+        return SWIGLU_ERR_UNSUPPORTED;
+    const uint64_t weight_tiles = static_cast<uint64_t>(kt) * static_cast<uint64_t>(k_blocks);
+    const int mt = static_cast<int>(round_up(M, 16));
+    CUtensorMap tmY, tmW;
+    if (!encode_2d(&tmY, Y, N, M, ElemBF16::kBK, static_cast<uint32_t>(mt)) ||
+        !encode_packed_weights(&tmW, W3packed, weight_tiles, 128u, false))
+        return SWIGLU_ERR_CUDA;
+    DecodeArgs args{};
+    args.M = static_cast<int>(M);
+    args.N = static_cast<int>(K);   // output columns
+    args.mt = mt;
+    args.k_blocks = k_blocks;
+    args.splits = splits;
+    args.out = static_cast<uint16_t *>(out);
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+    args.skip_first_fill = g_test_skip_first_fill;
+#endif
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(splits);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = splits > 1 ? 2 : 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles * splits));
+    cudaError_t err;
+    if (mt <= 32) {
+        cfg.blockDim = dim3(DecodeCfg<32>::THREADS);
+        cfg.dynamicSmemBytes = DecodeCfg<32>::SMEM_BYTES;
+        err = cudaLaunchKernelEx(&cfg, down_decode_kernel<32>, tmY, tmW, args);
+    } else if (mt <= 64) {
+        cfg.blockDim = dim3(DecodeCfg<64>::THREADS);
+        cfg.dynamicSmemBytes = DecodeCfg<64>::SMEM_BYTES;
+        err = cudaLaunchKernelEx(&cfg, down_decode_kernel<64>, tmY, tmW, args);
+    } else {
+        cfg.blockDim = dim3(DecodeCfg<128>::THREADS);
+        cfg.dynamicSmemBytes = DecodeCfg<128>::SMEM_BYTES;
+        err = cudaLaunchKernelEx(&cfg, down_decode_kernel<128>, tmY, tmW, args);
+    }
     if (err != cudaSuccess) {
         cudaGetLastError();
         return SWIGLU_ERR_CUDA;
@@ -965,7 +1123,8 @@ int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M,
     DeviceState *st;
     const int s = device_setup(&dev, &st);
     if (s != SWIGLU_OK) return s;
-    const DownPlan plan = plan_down_any(M, N, K, st->pair_clusters, st->sm_count);
+    const DownPlan plan =
+        plan_down_any(M, N, K, st->pair_clusters, st->sm_count, st->decode_clusters);
     const WorkSched &sched = plan.sched;
     const size_t ws_need = down_workspace_bytes_for(plan, M, st->sm_count);
     if (ws_need > 0) {
@@ -979,6 +1138,9 @@ int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M,
     if (plan.kind == kDownWide)
         return down_wide_launch(sched, Y, W3packed, out, M, N, K, workspace, ws_need > 0,
                                 st->sm_count, stream);
+    if (plan.kind == kDownDecode)
+        return down_decode_launch(plan.splits, st->decode_clusters, Y, W3packed, out, M, N, K,
+                                  stream);
     if (plan.kind == kDownSlim)
         return down_slim_launch(sched, Y, W3packed, out, M, N, K, workspace, ws_need > 0,
                                 st->sm_count, stream);

@@ -281,15 +281,21 @@ int swiglu_up_forward_fp8(const void *A8, const void *Wpacked8, void *Y,
  * the hidden size) is the usual completion of that MLP, and these entry
  * points are this library's extension. The down-projection is a plain
  * product: BF16 Y and W3, FP32 accumulation in tensor memory, each output
- * rounded once to BF16 (round to nearest even). Three kernels serve it, on
- * the same packed W3: a wide one (tiles of 256 rows x 512 output columns, one
- * accumulator stage; a third fewer operand bytes per flop) when whole wide
- * tiles fill at least 90% of their last wave and M >= 256; the 1-SM kernel in
- * a plain mode (tiles of 128 rows x 64 output columns, stream-K with small
- * partials) for M <= 128 when K has fewer than eight 256-column tiles; and
- * otherwise the CTA-pair kernel in a plain mode (tiles of 256 rows x 256
- * output columns; stream-K over N when whole tiles would leave the last wave
- * less than 90% full). SWIGLU_DOWN_TILE=64|256|512 forces one of them. The wide kernel also
+ * rounded once to BF16 (round to nearest even). Four kernels serve it, on
+ * the same packed W3: for M <= 128 a decode kernel with the operands' roles
+ * swapped (128 output columns of W3 on the tensor cores' 128-row side, all
+ * token rows on the N side), each 128-column tile cut into j equal K ranges
+ * on one cluster of j CTAs (j up to 16) whose partials are summed through
+ * distributed shared memory (no workspace); a wide one (tiles of 256 rows x
+ * 512 output columns, one accumulator stage; a third fewer operand bytes per
+ * flop) when whole wide tiles fill at least 90% of their last wave and
+ * M >= 256; otherwise the CTA-pair kernel in a plain mode (tiles of 256 rows
+ * x 256 output columns; stream-K over N when whole tiles would leave the
+ * last wave less than 90% full); and, forced only, the 1-SM kernel in a
+ * plain mode (tiles of 128 rows x 64 output columns, stream-K).
+ * SWIGLU_DOWN_TILE=64|128|256|512 forces one of them (128: the decode kernel,
+ * only for M <= 128); SWIGLU_DECODE_SPLITS=<j> forces the decode kernel's K
+ * ranges per tile. The wide kernel also
  * has split forms (forced by SWIGLU_SCHEDULE=sk|sk-tail|sk-aligned): a split
  * tile is finished, 128 columns at a time, by whichever participant counts
  * in last on them, so no CTA waits for another and the sums are added in k
@@ -330,9 +336,11 @@ size_t swiglu_down_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * workspace. SWIGLU_SCHEDULE=dp|sk|sk-tail forces a work split as for
  * swiglu_up_forward (split is not offered here and means the automatic
  * choice; sk-aligned, every tile cut into equal K ranges on as many pairs,
- * applies to the wide kernel only); SWIGLU_DOWN_TILE=64|256|512 forces the
- * kernel (see above); SWIGLU_FUSED_VARIANT does not apply. Errors as
- * swiglu_up_forward.
+ * applies to the wide kernel only; the decode kernel takes dp as one K
+ * range per tile and its own SWIGLU_DECODE_SPLITS); SWIGLU_DOWN_TILE=
+ * 64|128|256|512 forces the kernel (see above); SWIGLU_FUSED_VARIANT does not
+ * apply. Errors as swiglu_up_forward; SWIGLU_ERR_UNSUPPORTED also for a
+ * forced decode split whose clusters cannot be launched on this device.
  */
 int swiglu_down_forward(const void *Y, const void *W3packed, void *out,
                         int64_t M, int64_t N, int64_t K,

@@ -94,14 +94,17 @@ def test_wait_timeout_is_reported_and_context_survives(fi_lib, monkeypatch, vari
     assert r["mismatches"] == 0 and r["over_bound"] == 0, r
 
 
-@pytest.mark.parametrize("tile", ["64", "256", "512"])
-@pytest.mark.parametrize("mode,M,N,K", [("auto", 512, 2048, 512), ("dp", 512, 512, 512)])
+@pytest.mark.parametrize("tile,mode,M,N,K", [
+    (t, mode, M, N, K) for t in ("64", "256", "512")
+    for mode, M, N, K in (("auto", 512, 2048, 512), ("dp", 512, 512, 512))
+] + [("128", "auto", 16, 2048, 512), ("128", "dp", 64, 512, 512)])
 def test_down_projection_wait_timeout(fi_lib, monkeypatch, tile, mode, M, N, K):
     """The same for the down-projection, on each of its kernels (the 1-SM
     kernel's plain mode, tile 64, the CTA-pair kernel's plain mode, tile 256,
-    and the wide kernel, tile 512),
-    with stream-K split tiles (auto: 4 or 2 output tiles on many pairs) and
-    with whole tiles: the timeout is reported and the next call is correct."""
+    the wide kernel, tile 512, and the decode kernel, tile 128), with
+    stream-K split tiles (auto: 4 or 2 output tiles on many pairs; the decode
+    kernel: 4 tiles of 128 columns, each in 8 K ranges on a cluster) and with
+    whole tiles: the timeout is reported and the next call is correct."""
     monkeypatch.setenv("SWIGLU_DOWN_TILE", tile)
     if mode != "auto":
         monkeypatch.setenv("SWIGLU_SCHEDULE", mode)
@@ -169,13 +172,15 @@ def _busy_and_run(lib, op, n_busy=120, busy_ns=300_000_000):
     return out, status, raw.value, still_busy
 
 
-@pytest.mark.parametrize("kind", ["down", "down-wide", "up"])
+@pytest.mark.parametrize("kind", ["down", "down-wide", "down-decode", "up"])
 def test_split_tiles_finish_while_other_work_holds_sms(fi_lib, monkeypatch, kind):
     """A K-split launch while a kernel on another stream holds 120 of the
     SMs for 300 ms: only some of its pairs can run at first. In the CTA-pair
     kernel a split tile's owner waits only for pairs that started before it
     (worker numbers follow the start order); in the wide down-projection
-    kernel nobody waits (the last to count in on a part finishes it). Either
+    kernel nobody waits (the last to count in on a part finishes it); in the
+    decode kernel a CTA waits only for the CTAs of its own cluster, which are
+    scheduled together. Either
     way the call completes on the free SMs, well within this build's ~10 ms
     wait limit, and is correct. (Were owners to wait for pairs not yet
     started, they would hold their SMs until the limit and report
@@ -186,11 +191,16 @@ def test_split_tiles_finish_while_other_work_holds_sms(fi_lib, monkeypatch, kind
     if kind.startswith("down"):
         # CTA-pair kernel: 8 output tiles of 256 x 256, 64 k-blocks each,
         # stream-K over 64 pairs; wide kernel: 4 tiles of 256 x 512,
-        # stream-K forced, on 32 pairs
-        monkeypatch.setenv("SWIGLU_DOWN_TILE", "512" if kind == "down-wide" else "256")
+        # stream-K forced, on 32 pairs; decode kernel (16 rows): 8 tiles of
+        # 128 columns, each in two K ranges on a cluster of 2 (a cluster
+        # needs its CTAs' SMs free at once: pairs fit beside the busy kernel)
+        tile = {"down-wide": "512", "down-decode": "128"}.get(kind, "256")
+        monkeypatch.setenv("SWIGLU_DOWN_TILE", tile)
         if kind == "down-wide":
             monkeypatch.setenv("SWIGLU_SCHEDULE", "sk")
-        M, N, K = 512, 4096, 1024
+        if kind == "down-decode":
+            monkeypatch.setenv("SWIGLU_DECODE_SPLITS", "2")
+        M, N, K = (16 if kind == "down-decode" else 512), 4096, 1024
         lib.swiglu_pack_down_weights.argtypes = [vp, i64, i64, vp, vp]
         lib.swiglu_down_packed_weight_bytes.argtypes = [i64, i64]
         lib.swiglu_down_packed_weight_bytes.restype = sz
@@ -207,14 +217,16 @@ def test_split_tiles_finish_while_other_work_holds_sms(fi_lib, monkeypatch, kind
         st0 = torch.cuda.current_stream().cuda_stream
         assert lib.swiglu_pack_down_weights(W3d.data_ptr(), N, K, W3p.data_ptr(), st0) == 0
         ws_bytes = lib.swiglu_down_workspace_bytes(M, N, K)
-        assert ws_bytes > 0                                  # the K split is planned
-        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+        # the K split is planned (the decode kernel sums inside its clusters)
+        assert (ws_bytes == 0) if kind == "down-decode" else (ws_bytes > 0)
+        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
         torch.cuda.synchronize()
 
         def op(stream):
             out = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
             assert lib.swiglu_down_forward(Yd.data_ptr(), W3p.data_ptr(), out.data_ptr(), M, N,
-                                           K, ws.data_ptr(), ws_bytes, stream) == 0
+                                           K, ws.data_ptr() if ws_bytes else None, ws_bytes,
+                                           stream) == 0
             return out
 
         out, status, raw, still_busy = _busy_and_run(lib, op)

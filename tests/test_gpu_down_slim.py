@@ -2,9 +2,9 @@
 columns), the down-projection of decode-sized MLPs, against the oracle,
 through the C ABI.
 
-It is the automatic choice up to 128 rows when the output has fewer than
-eight 256-column tiles (the 0.5B shape); SWIGLU_DOWN_TILE=64 forces it at any
-M, SWIGLU_SCHEDULE a work split. The shapes cover M tails inside a
+SWIGLU_DOWN_TILE=64 forces it at any M (the decode kernel took its place as
+the automatic choice for decode-sized products), SWIGLU_SCHEDULE a work
+split. The shapes cover M tails inside a
 128-row tile, output widths that end inside a 64-column tile and inside a
 256-column packed weight tile, ragged reductions, stream-K tiles split over
 up to ~50 CTAs (the last contributor sums every partial), and the decode
@@ -99,12 +99,10 @@ def test_slim_every_schedule_form(sg, orc, monkeypatch, mode):
 
 @pytest.mark.parametrize("label", ["0", "2", "3", "4", "8", "10"])
 def test_slim_down_at_decode_workload_shapes(sg, orc, monkeypatch, label):
-    """This kernel at the decode workloads' down-projection shapes, every
-    element compared: the 0.5B shape (M=128, 896 output columns: its
-    automatic choice) and, forced, M = 1, 16, 128 for 7B, 64 for 32B and 32
-    for 72B (where the CTA-pair kernel is the automatic choice)."""
-    if label != "0":
-        monkeypatch.setenv("SWIGLU_DOWN_TILE", "64")
+    """This kernel, forced, at the decode workloads' down-projection shapes,
+    every element compared: the 0.5B shape (M=128, 896 output columns), and
+    M = 1, 16, 128 for 7B, 64 for 32B and 32 for 72B."""
+    monkeypatch.setenv("SWIGLU_DOWN_TILE", "64")
     w = workloads.BY_LABEL[label]
     M, N, K = w.M, w.N, w.K
     Yb, W3b = _case(M, N, K, 400 + int(label))

@@ -110,3 +110,4 @@ def test_stream_k_grid_search(checker):
     assert r.returncode == 0, r.stdout[-3000:]
     last = r.stdout.strip().splitlines()[-1]
     assert "grid=72 " in last and "max_contrib=2" in last, last
+

@@ -310,4 +310,38 @@ inline WorkSched plan_down_wide(int m_tiles, int n_tiles, int k_blocks, int work
                          kSchedDataParallel);
 }
 
+// K ranges per tile of the decode down-projection kernel (down_decode_kernel
+// .cuh), whose T tiles each run on one cluster of j CTAs. Candidates: the j
+// whose T clusters fit at once (clusters[j] >= T, from the occupancy query;
+// null: sms / j) with at least kDecodeMinKb k-blocks per range. A long weight
+// stream (ranges of kDecodeStreamKb k-blocks or more) takes the smallest j
+// that puts two thirds of the `sms` SMs to work: more SMs add no bandwidth
+// there, and SMs left idle let the next launch's CTAs start their prologue
+// early (7B, M=16, 28 tiles: j=4 24.5 us, j=5 25.4 us). Anything else takes
+// the j with the most CTAs: short ranges are latency-bound (0.5B, 7 tiles
+// of 76 k-blocks: j=15 8.7 us, j=16 8.3 us). 1 when T is the SM count or
+// more. j <= max_splits (clusters[] has max_splits + 1 entries).
+constexpr int kDecodeMinKb = 4;
+constexpr int kDecodeStreamKb = 32;
+
+inline int plan_decode_splits(long long T, int k_blocks, int sms, const int *clusters,
+                              int max_splits) {
+    if (T >= sms) return 1;
+    const int jmax = max_splits < k_blocks ? max_splits : k_blocks;
+    const long long target = (2LL * sms + 2) / 3;
+    int best = 1;
+    long long best_ctas = T;
+    for (int j = 2; j <= jmax; ++j) {
+        if (k_blocks / j < kDecodeMinKb) break;
+        const int fit = clusters ? clusters[j] : sms / j;
+        if (fit < T || T * j > sms) continue;
+        if (T * j >= target && k_blocks / j >= kDecodeStreamKb) return j;
+        if (T * j > best_ctas) {
+            best = j;
+            best_ctas = T * j;
+        }
+    }
+    return best;
+}
+
 }  // namespace swiglu

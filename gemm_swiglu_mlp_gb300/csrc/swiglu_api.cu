@@ -360,42 +360,22 @@ WorkSched plan_down_slim(int64_t M, int64_t N, int64_t K, int sms) {
 // Split of the decode down-projection kernel (down_decode_kernel.cuh): its
 // T = ceil(K / 128) tiles of 128 output columns (all token rows at once) are
 // each cut into j equal K ranges, one per CTA, the j CTAs of a tile forming a
-// cluster. The automatic j is the smallest that puts at least two thirds of
-// the SMs to work in one wave (T clusters of j fitting at once: `clusters[j]`,
-// from the occupancy query), with at least kDecodeMinKb k-blocks per range;
-// failing that, the j with the most CTAs in one wave; j = 1 (whole tiles, no
-// cluster) when T is the SM count or more. Measured on GB300 (graph-replayed
-// calls, us): 7B M=16 (28 tiles) j=3 30.0, j=4 24.5, j=5 25.4; 32B M=64 (40
-// tiles) j=2 61.6, j=3 46.1; 72B M=32 (64 tiles) j=2 76.3; the 0.5B shape
-// (7 tiles) j=8 8.6, j=16 8.3. The extra SMs of the larger j add no weight
-// bandwidth once about two thirds stream, while idle SMs let the next
-// launch's CTAs start their prologue early. SWIGLU_SCHEDULE=dp forces j = 1,
-// SWIGLU_DECODE_SPLITS=<j> any j (clamped to 1..16 and the k-blocks; more
-// clusters than fit at once then run in waves); both are read on every call.
-constexpr int kDecodeMinKb = 4;
+// cluster; j from plan_decode_splits (schedule.cuh). Measured on GB300
+// (graph-replayed calls, us): 7B M=16 (28 tiles) j=3 30.0, j=4 24.5, j=5
+// 25.4; 32B M=64 (40 tiles) j=2 61.6, j=3 46.1; 72B M=32 (64 tiles) j=2
+// 76.3; the 0.5B shape (7 tiles) j=8 8.6, j=16 8.3; 1.5B M=16 (12 tiles)
+// j=8 9.4, j=10 9.0. SWIGLU_SCHEDULE=dp forces j = 1, SWIGLU_DECODE_SPLITS=<j>
+// any j (clamped to 1..16 and the k-blocks; more clusters than fit at once
+// then run in waves); both are read on every call.
 int plan_down_decode(int64_t N, int64_t K, int sms, const int *clusters) {
     const int64_t T = (K + 127) / 128;
     const int k_blocks = static_cast<int>((N + ElemBF16::kBK - 1) / ElemBF16::kBK);
-    const int jmax = std::min(kDecodeMaxSplits, k_blocks);
     if (const char *v = std::getenv("SWIGLU_DECODE_SPLITS")) {
         const int j = std::atoi(v);
-        if (j >= 1) return std::min(j, jmax);
+        if (j >= 1) return std::min(j, std::min(kDecodeMaxSplits, k_blocks));
     }
-    if (schedule_mode() == kSchedDataParallel || T >= sms) return 1;
-    const int64_t target = (2 * static_cast<int64_t>(sms) + 2) / 3;
-    int best = 1;
-    int64_t best_ctas = T;
-    for (int j = 2; j <= jmax; ++j) {
-        if (k_blocks / j < kDecodeMinKb) break;
-        const int fit = clusters ? clusters[j] : sms / j;
-        if (fit < T || T * j > sms) continue;
-        if (T * j >= target) return j;
-        if (T * j > best_ctas) {
-            best = j;
-            best_ctas = T * j;
-        }
-    }
-    return best;
+    if (schedule_mode() == kSchedDataParallel) return 1;
+    return plan_decode_splits(T, k_blocks, sms, clusters, kDecodeMaxSplits);
 }
 
 // The down-projection's kernel and schedule. Four kernels serve it, on the

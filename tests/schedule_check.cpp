@@ -37,6 +37,25 @@ int main() {
         // with mode - 10, `sms` CTA pairs
         // mode 20: stream-K over all tiles with the grid searched for the
         // finishing cost (plan_stream_k_grid)
+        // mode 30: the decode kernel's K ranges per tile (plan_decode_splits)
+        // for nt tiles of kb k-blocks; wbound selects the cluster capacities:
+        // 0 none (sms / j), 1 the ones measured on a 152-SM GB300 with ~225 KB
+        // of shared memory per CTA. Checks: 1 <= j <= 16, j <= kb, at least
+        // kDecodeMinKb k-blocks per range when split, a split's clusters fit
+        // in one wave; prints "splits=j".
+        if (mode == 30) {
+            static const int gb300[17] = {0, 152, 76, 46, 36, 28, 23, 15, 15, 15, 13, 8, 8, 7, 7, 7, 7};
+            int cap[17];
+            for (int j = 0; j <= 16; ++j) cap[j] = wbound ? gb300[j] : (j ? sms / j : 0);
+            const int j = plan_decode_splits(nt, kb, sms, cap, 16);
+            if (j < 1 || j > 16 || j > kb) { bad |= fail("decode splits range", j, kb); continue; }
+            if (j > 1 && (kb / j < kDecodeMinKb || cap[j] < nt || (long long)nt * j > sms)) {
+                bad |= fail("decode split does not fit", j, nt);
+                continue;
+            }
+            std::printf("nt=%d kb=%d sms=%d splits=%d\n", nt, kb, sms, j);
+            continue;
+        }
         const bool grid_search = mode == 20;
         const bool wide = mode >= 10 && !grid_search;
         if (wide) mode -= 10;

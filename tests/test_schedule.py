@@ -111,3 +111,32 @@ def test_stream_k_grid_search(checker):
     last = r.stdout.strip().splitlines()[-1]
     assert "grid=72 " in last and "max_contrib=2" in last, last
 
+
+def test_decode_splits(checker):
+    """The decode down-projection kernel's K ranges per tile: range checks on
+    random shapes, and with the cluster capacities measured on GB300 the
+    choices at the workloads' decode shapes (tiles of 128 output columns,
+    k-blocks over the intermediate size): for long weight streams the
+    smallest split that puts two thirds of the 152 SMs to work in one wave
+    (7B: 28 tiles in 4, 112 CTAs; 72B: 64 in 2; 32B: 40 in 3), for short
+    ranges the most CTAs in one wave (1.5B M=16: 12 tiles in 10; 0.5B: 7 in
+    16), whole tiles for 152 tiles or more."""
+    rng = np.random.Generator(np.random.PCG64(7))
+    cases = [(1, int(rng.integers(1, 400)), int(rng.integers(1, 600)), 152, 8,
+              int(rng.integers(0, 2)), 30) for _ in range(500)]
+    inp = "\n".join(" ".join(map(str, c)) for c in cases) + "\n"
+    r = subprocess.run([checker], input=inp, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout[-3000:]
+    assert r.stdout.count("\n") == len(cases)
+    want = {"3": 4, "10": 2, "8": 3, "0": 16}
+    for label, j in want.items():
+        w = workloads.BY_LABEL[label]
+        case = (1, -(-w.K // 128), -(-w.N // 64), 152, 8, 1, 30)
+        r = subprocess.run([checker], input=" ".join(map(str, case)) + "\n", capture_output=True,
+                           text=True)
+        assert r.returncode == 0 and "splits=%d\n" % j in r.stdout, (label, r.stdout)
+    for case, j in [((1, 12, 140, 152, 8, 1, 30), 10), ((1, 152, 296, 152, 8, 1, 30), 1),
+                    ((1, 7, 3, 152, 8, 1, 30), 1)]:
+        r = subprocess.run([checker], input=" ".join(map(str, case)) + "\n", capture_output=True,
+                           text=True)
+        assert r.returncode == 0 and "splits=%d\n" % j in r.stdout, (case, r.stdout)

@@ -317,7 +317,8 @@ def swiglu_up_forward_noalloc(A: torch.Tensor, Wpacked: torch.Tensor, N: int,
 
 
 _PLAN_SWITCHES = ("SWIGLU_FUSED_VARIANT", "SWIGLU_SCHEDULE", "SWIGLU_DYNAMIC_TILES",
-                  "SWIGLU_GROUP_M", "SWIGLU_DOWN_TILE", "SWIGLU_DECODE_SPLITS")
+                  "SWIGLU_GROUP_M", "SWIGLU_DOWN_TILE", "SWIGLU_DECODE_SPLITS",
+                  "SWIGLU_SK_PAIRS")
 
 
 def _plan_key(*head):

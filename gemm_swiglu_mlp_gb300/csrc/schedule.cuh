@@ -242,13 +242,16 @@ inline WorkSched plan_schedule(int m_tiles, int n_tiles, int k_blocks, int sm_co
 // Stream-K over all T tiles (fewer than `workers`) with the grid chosen for
 // its finishing cost: on g CTAs each takes about T*k/g k-blocks, and a tile
 // whose k-blocks span n CTAs' ranges is summed through the workspace, which
-// costs its finisher about kSplitFixKb per partial to read (and an owner
-// waits for partials written at the same time). Among g in [ceil(W/2), W],
-// the grid minimising ceil(T*k/g) + kSplitFixKb * (n_max(g) - 1) wins; e.g.
-// 48 tiles of 140 k-blocks on 76 pairs: g = 76 gives 88.4 k-blocks each but
-// tiles among three pairs, g = 72 gives 93.3 each and every tile between
-// exactly two (two tiles per three pairs).
-constexpr int kSplitFixKb = 14;
+// costs about kSplitFixKb k-blocks of time per extra participant (partial
+// writes, an owner waiting for a partner that finishes at the same time,
+// the reads back). Among g in [ceil(W/2), W], the grid minimising
+// ceil(T*k/g) + kSplitFixKb * (n_max(g) - 1) wins. Measured on GB300 (the
+// CTA-pair plain product, graph-replayed calls, us): 7B M=512, 28 tiles of
+// 296 k-blocks: 28 pairs (no split) 85.9, 42 pairs 70.0, 56 (two per tile)
+// 56.2, 64 65.6, 70 61.7, 76 64.5 -- about 12 us (~40 k-blocks) per extra
+// participant; 1.5B, 48 tiles of 140 k-blocks: 48 pairs 45.0, 56 47.7, 64
+// 45.2, 72 (every tile between exactly two) 42.0, 76 45.5.
+constexpr int kSplitFixKb = 40;
 
 inline WorkSched plan_stream_k_grid(int m_tiles, int n_tiles, int k_blocks, int workers,
                                     int group_m, int min_sk_iters) {

@@ -298,6 +298,8 @@ WorkSched plan_for(int64_t M, int64_t N, int64_t K, int workers, int ctas, int k
 // tiles). With fewer tiles than pairs the grid is picked for the split's
 // finishing cost (schedule.cuh, plan_stream_k_grid: 1.5B, 48 tiles, on 72 of
 // the 76 pairs, two per tile). Column sub-tiles do not apply.
+// SWIGLU_SK_PAIRS=<g> (ablation, read on every call) runs that stream-K over
+// all tiles on g pairs instead (clamped to 1..workers).
 WorkSched plan_down(int64_t M, int64_t N, int64_t K, int workers) {
     const int rows = FusedC::BM * 2;
     const int m_tiles = static_cast<int>((M + rows - 1) / rows);
@@ -313,6 +315,14 @@ WorkSched plan_down(int64_t M, int64_t N, int64_t K, int workers) {
     }
     const int grows = group_rows_override();
     const int group_m = grows ? std::max(1, grows / rows) : kGroupM / 2;
+    if (mode == kSchedStreamK) {
+        if (const char *v = std::getenv("SWIGLU_SK_PAIRS")) {
+            const int g = std::atoi(v);
+            if (g >= 1)
+                return plan_schedule(m_tiles, n_tiles, k_blocks, std::min(g, workers), group_m,
+                                     kMinStreamKIters, false, kSchedStreamK);
+        }
+    }
     if (mode == kSchedStreamK && schedule_mode_fused() == kSchedAuto)
         return plan_stream_k_grid(m_tiles, n_tiles, k_blocks, workers, group_m, kMinStreamKIters);
     return plan_schedule(m_tiles, n_tiles, k_blocks, workers, group_m, kMinStreamKIters, false,

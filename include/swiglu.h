@@ -295,7 +295,8 @@ int swiglu_up_forward_fp8(const void *A8, const void *Wpacked8, void *Y,
  * plain mode (tiles of 128 rows x 64 output columns, stream-K).
  * SWIGLU_DOWN_TILE=64|128|256|512 forces one of them (128: the decode kernel,
  * only for M <= 128); SWIGLU_DECODE_SPLITS=<j> forces the decode kernel's K
- * ranges per tile. The wide kernel also
+ * ranges per tile, SWIGLU_SK_PAIRS=<g> the number of pairs of the CTA-pair
+ * kernel's stream-K over all tiles (ablations). The wide kernel also
  * has split forms (forced by SWIGLU_SCHEDULE=sk|sk-tail|sk-aligned): a split
  * tile is finished, 128 columns at a time, by whichever participant counts
  * in last on them, so no CTA waits for another and the sums are added in k

@@ -84,6 +84,53 @@ struct DecodeArgs {
 #endif
 };
 
+// The cluster's sum of one tile slice: this thread's chunks first, first +
+// STRIDE, .. (< c_hi), U of them per step. Chunk c is the float4 at byte 16c
+// of every CTA's partial ([token][128 columns] FP32 at shared offset 0): all
+// `splits` (<= 16 / U) CTAs' values of the step's chunks are loaded before
+// any is added, then each chunk is summed in rank order and stored as BF16.
+template <int U, int STRIDE>
+__device__ __forceinline__ void decode_finish(const DecodeArgs &args, uint32_t sbase, int tile,
+                                              int splits, int first, int c_hi) {
+    constexpr int QMAX = kDecodeMaxSplits / U;
+    for (int c0 = first; c0 < c_hi; c0 += STRIDE * U) {
+        float4 v[U][QMAX];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + STRIDE * u;
+            if (c < c_hi) {
+                const uint32_t local = sbase + 16u * static_cast<uint32_t>(c);
+#pragma unroll
+                for (int q = 0; q < QMAX; ++q)
+                    if (q < splits)
+                        v[u][q] = ld_cluster_f32x4(mapa_shared(local, static_cast<uint32_t>(q)));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + STRIDE * u;
+            const int col = tile * 128 + 4 * (c & 31);
+            // N % 8 == 0: a chunk is all in or all out
+            if (c >= c_hi || col >= args.N) continue;
+            float4 s = v[u][0];
+#pragma unroll
+            for (int q = 1; q < QMAX; ++q) {
+                if (q < splits) {
+                    s.x += v[u][q].x;
+                    s.y += v[u][q].y;
+                    s.z += v[u][q].z;
+                    s.w += v[u][q].w;
+                }
+            }
+            uint2 packed;
+            packed.x = pack_bf16x2(s.x, s.y);
+            packed.y = pack_bf16x2(s.z, s.w);
+            *reinterpret_cast<uint2 *>(args.out + static_cast<size_t>(c >> 5) * args.N + col) =
+                packed;
+        }
+    }
+}
+
 template <int MTB>
 __global__ void __launch_bounds__(DecodeCfg<MTB>::THREADS, 1)
     down_decode_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmW,
@@ -286,34 +333,21 @@ __global__ void __launch_bounds__(DecodeCfg<MTB>::THREADS, 1)
         if (warp >= 2 && !*abort_flag) {
             // slice `rank` of the tile's M x 128 outputs, in 4-column chunks
             // (chunk c: token c / 32, columns 4 * (c % 32) ..), summed over
-            // the cluster's partials in rank order
+            // the cluster's partials in rank order; U chunks per step, so
+            // that U * splits (<= 16) loads from the cluster's shared
+            // memories are in flight at once
             const int chunks = args.M * (C::COLS / 4);
             const int c_lo = static_cast<int>(static_cast<long long>(chunks) * rank / splits);
             const int c_hi = static_cast<int>(static_cast<long long>(chunks) * (rank + 1) / splits);
-            for (int c = c_lo + static_cast<int>(threadIdx.x) - 64; c < c_hi; c += C::EPI_THREADS) {
-                const int t = c >> 5;
-                const int col = tile * C::COLS + 4 * (c & 31);
-                if (col >= args.N) continue;   // N % 8 == 0: a chunk is all in or all out
-                const uint32_t local = sbase + 16u * static_cast<uint32_t>(c);
-                float4 v[kDecodeMaxSplits];
-#pragma unroll
-                for (int q = 0; q < kDecodeMaxSplits; ++q)
-                    if (q < splits) v[q] = ld_cluster_f32x4(mapa_shared(local, static_cast<uint32_t>(q)));
-                float4 s = v[0];
-#pragma unroll
-                for (int q = 1; q < kDecodeMaxSplits; ++q) {
-                    if (q < splits) {
-                        s.x += v[q].x;
-                        s.y += v[q].y;
-                        s.z += v[q].z;
-                        s.w += v[q].w;
-                    }
-                }
-                uint2 packed;
-                packed.x = pack_bf16x2(s.x, s.y);
-                packed.y = pack_bf16x2(s.z, s.w);
-                *reinterpret_cast<uint2 *>(args.out + static_cast<size_t>(t) * args.N + col) = packed;
-            }
+            const int first = c_lo + static_cast<int>(threadIdx.x) - 64;
+            if (splits <= 2)
+                decode_finish<8, C::EPI_THREADS>(args, sbase, tile, splits, first, c_hi);
+            else if (splits <= 4)
+                decode_finish<4, C::EPI_THREADS>(args, sbase, tile, splits, first, c_hi);
+            else if (splits <= 8)
+                decode_finish<2, C::EPI_THREADS>(args, sbase, tile, splits, first, c_hi);
+            else
+                decode_finish<1, C::EPI_THREADS>(args, sbase, tile, splits, first, c_hi);
         }
         // every partial has been read before any CTA of the cluster exits
         cluster_sync();

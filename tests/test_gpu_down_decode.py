@@ -155,3 +155,29 @@ def test_decode_and_slim_agree_with_the_oracle_on_one_input(sg, orc, monkeypatch
         monkeypatch.setenv("SWIGLU_DOWN_TILE", tile)
         got = _run(sg, Yb, W3b)[0]
         _check(got, want, Yb, W3b, tile)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 18944, 3584), (128, 4864, 896), (32, 4600, 1032)])
+def test_decode_in_a_cuda_graph(sg, monkeypatch, M, N, K):
+    """The decode kernel captured in a CUDA graph (clusters of 4, 16 and 2 at
+    these shapes) replays to the bytes of direct calls: nothing carries over
+    between launches."""
+    Yb, W3b = _case(M, N, K, 71)
+    Wd = sg.swiglu_pack_down_weights(to_device_bf16(W3b, "cuda"))
+    Yd = to_device_bf16(Yb, "cuda")
+    direct = sg.swiglu_down_forward(Yd, Wd, K)
+    torch.cuda.synchronize()
+    outs = [torch.zeros((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        for o in outs:
+            sg.swiglu_down_forward(Yd, Wd, K, out=o, stream=cs)
+    for _ in range(2):
+        for o in outs:
+            o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert sg.swiglu_check_device_status() == 0
+        for o in outs:
+            assert torch.equal(o.view(torch.int16), direct.view(torch.int16))

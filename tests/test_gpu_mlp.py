@@ -185,12 +185,15 @@ def test_mlp_small_full_compare(sg, orc, M, N, K):
     _check_mlp(orc, A, W1, W2, W3, Yg, outg, np.arange(M, dtype=np.int64), (M, N, K))
 
 
-def test_mlp_in_a_cuda_graph(sg, orc):
-    M, N, K = 600, 1032, 520
-    A, W1, W2 = workloads.random_case(M, N, K, seed=31)
-    W3 = _rand_bf16(32, (N, K), N ** -0.5)
+@pytest.mark.parametrize("M,N,K", [(600, 1032, 520), (16, 4600, 1032)])
+def test_mlp_in_a_cuda_graph(sg, orc, M, N, K):
+    """The whole MLP captured in a CUDA graph: a prefill-sized shape (the
+    CTA-pair kernels) and a decode-sized one (the down-projection on the
+    decode kernel's clusters)."""
+    A, W1, W2 = workloads.random_case(M, N, K, seed=31 + M)
+    W3 = _rand_bf16(32 + M, (N, K), N ** -0.5)
     Yg, outg = _run_mlp(sg, A, W1, W2, W3, graph=True)
-    _check_mlp(orc, A, W1, W2, W3, Yg, outg, np.arange(M, dtype=np.int64), "graph")
+    _check_mlp(orc, A, W1, W2, W3, Yg, outg, np.arange(M, dtype=np.int64), ("graph", M))
 
 
 @pytest.mark.parametrize("label,full", [("0", True), ("1", False), ("6", False), ("10", False)])

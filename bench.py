@@ -574,6 +574,103 @@ def down_sweep(sg, dev, stream, sampler, window_s: float, labels=DOWN_SWEEP_LABE
     return out
 
 
+def mlp_decode_context(sg, peaks, dev, stream, sampler, window_s: float, label: str = "3"):
+    """The whole gated MLP at a decode shape (default the 7B workload with 16
+    tokens): out = (SiLU(A W1) * (A W2)) W3, a stream of the three weight
+    matrices. This library's whole-MLP call (the fused up-projection, then
+    the decode down-projection kernel), the fused up-projection followed by
+    torch.matmul (cuBLAS), and eager PyTorch (three cuBLAS GEMMs and
+    silu * mul), each as a CUDA graph of launches over rotating inputs
+    (seeded, drawn on the GPU: A ~ N(0, 1), W1 and W2 ~ N(0, 1/K), W3 ~
+    N(0, 1/N)) replayed for `window_s` seconds, in two alternating rounds,
+    the faster window of each with its SM clock; plus the HBM roofline of
+    the weight stream (3 K N BF16 values) at the measured copy rate. BF16."""
+    import torch
+    import torch.nn.functional as F
+
+    import workloads
+    w = workloads.BY_LABEL[label]
+    M, K, N = w.M, w.K, w.N
+    per = 2 * (M * K + 3 * K * N + 2 * M * N + M * K)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(2, min(8, int(2.5 * l2 // per) + 1))   # the sets exceed twice the L2
+    g = torch.Generator(device=dev)
+    g.manual_seed(9000 + w.seed_index)
+
+    def rnd(rows, cols, scale):
+        return (torch.randn(rows, cols, generator=g, device=dev) * scale).to(torch.bfloat16)
+
+    As = [rnd(M, K, 1.0) for _ in range(R)]
+    W1s = [rnd(K, N, K ** -0.5) for _ in range(R)]
+    W2s = [rnd(K, N, K ** -0.5) for _ in range(R)]
+    W3s = [rnd(N, K, N ** -0.5) for _ in range(R)]
+    Wps = [sg.swiglu_pack_weights(W1s[j], W2s[j]) for j in range(R)]
+    W3ps = [sg.swiglu_pack_down_weights(W3s[j]) for j in range(R)]
+    Gs = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    Us = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    Ys = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    Os = [torch.empty(M, K, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    mws = sg.swiglu_mlp_workspace_bytes(M, N, K)
+    uws = sg.swiglu_workspace_bytes(M, N, K)
+    MWs = [torch.zeros(max(mws, 256), dtype=torch.uint8, device=dev) for _ in range(R)]
+    UWs = [torch.zeros(max(uws, 256), dtype=torch.uint8, device=dev) for _ in range(R)]
+
+    def fused(i, st):
+        j = i % R
+        sg.swiglu_mlp_forward(As[j], Wps[j], W3ps[j], N, Y=Ys[j], out=Os[j],
+                              workspace=MWs[j] if mws else None, stream=st)
+
+    def fused_cublas_down(i, st):
+        j = i % R
+        sg.swiglu_up_forward(As[j], Wps[j], N, Y=Ys[j], workspace=UWs[j] if uws else None,
+                             stream=st)
+        torch.matmul(Ys[j], W3s[j], out=Os[j])
+
+    def eager(i, st):
+        j = i % R
+        torch.matmul(As[j], W1s[j], out=Gs[j])
+        torch.matmul(As[j], W2s[j], out=Us[j])
+        torch.mul(F.silu(Gs[j]), Us[j], out=Ys[j])
+        torch.matmul(Ys[j], W3s[j], out=Os[j])
+
+    variants = (("fused", fused), ("fused_up_cublas_down", fused_cublas_down), ("eager", eager))
+    weight_bytes = 3 * K * N * 2
+    roof_us = weight_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+    graphs = {}
+    for name, fn in variants:
+        with torch.cuda.stream(stream):
+            for i in range(R):
+                fn(i, stream)
+        torch.cuda.synchronize(dev)
+        n = graph_launches(R, roof_us * 1e-6)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            cs = torch.cuda.current_stream(dev)
+            for i in range(n):
+                fn(i, cs)
+        graphs[name] = (gr, n)
+    best = {}
+    for _ in range(2):
+        for name, _fn in variants:
+            gr, n = graphs[name]
+            el, rounds, t0, t1 = replay_window([gr], stream, dev, window_s)
+            us = el / (n * rounds) * 1e6
+            if name not in best or us < best[name][0]:
+                best[name] = (us, sampler.summary(t0, t1, min_samples=2))
+    sg.swiglu_check_device_status(stream)
+    e = {"workload": label, "name": w.name, "M": M, "K": K, "N": N,
+         "weight_bytes": weight_bytes, "hbm_roofline_us": roof_us}
+    for name, _fn in variants:
+        us, clk = best[name]
+        e[name] = {"us": us, "frac_of_hbm_roofline": roof_us / us, "clocks": clk}
+    e["mlp_speedup_over_eager"] = best["eager"][0] / best["fused"][0]
+    e["what"] = ("whole gated MLP at a decode shape, CUDA graphs over rotating inputs; fused = "
+                 "swiglu_mlp_forward (fused up-projection + decode down-projection kernel)")
+    del graphs, As, W1s, W2s, W3s, Wps, W3ps, Gs, Us, Ys, Os, MWs, UWs
+    torch.cuda.empty_cache()
+    return e
+
+
 ABLATION_FORMS = (
     # (packed layout, kernel variant, schedule form); "auto" = the library's choice
     [(layout, "auto", mode) for layout in ("blocked", "interleaved")
@@ -1072,9 +1169,11 @@ def run_gb300(args, w):
         import workloads
         labels = [x.c for x in workloads.WORKLOADS]
         sweep_out = sweep(sg, peaks, args.dtype, dev, stream, sampler, args.sweep_window_s, labels)
-    down_out = None
+    down_out = mlp_decode = None
     if world == 1 and not args.no_context and not args.no_sweep and not fp8:
         down_out = down_sweep(sg, dev, stream, sampler, min(args.sweep_window_s, 0.15))
+        mlp_decode = mlp_decode_context(sg, peaks, dev, stream, sampler,
+                                        min(args.sweep_window_s, 0.15))
     sampler.stop()
 
     if rank != 0:
@@ -1134,6 +1233,8 @@ def run_gb300(args, w):
         line["context_mlp"] = mlp
     if down_out is not None:
         line["context_down"] = down_out
+    if mlp_decode is not None:
+        line["context_mlp_decode"] = mlp_decode
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inputs)
     print(json.dumps(line), flush=True)

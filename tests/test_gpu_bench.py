@@ -64,9 +64,10 @@ def test_bench_prints_one_contract_line(dtype):
 
 
 def test_bench_context_down_projection():
-    """With the context on: the whole MLP at the bench workload and the
+    """With the context on: the whole MLP at the bench workload, the
     down-projection sweep (this library against cuBLAS at the workloads'
-    down-projection shapes, alternating windows, clocks per window)."""
+    down-projection shapes, alternating windows, clocks per window) and the
+    whole MLP at a decode shape (graph-replayed, against eager cuBLAS)."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "0", "--steps", "20",
@@ -88,6 +89,13 @@ def test_bench_context_down_projection():
             assert e[side]["us"] > 0 and e[side]["tflops"] > 0, e
             assert "sm_mhz" in e[side]["clocks"], e
         assert e["ours_over_cublas_time"] == pytest.approx(e["ours"]["us"] / e["cublas"]["us"])
+    md = r["context_mlp_decode"]
+    w = workloads.BY_LABEL[md["workload"]]
+    assert (md["M"], md["K"], md["N"]) == (w.M, w.K, w.N) and md["weight_bytes"] == 6 * w.K * w.N
+    for side in ("fused", "fused_up_cublas_down", "eager"):
+        assert md[side]["us"] > 0 and 0 < md[side]["frac_of_hbm_roofline"] < 1.5, md
+        assert "sm_mhz" in md[side]["clocks"], md
+    assert md["mlp_speedup_over_eager"] == pytest.approx(md["eager"]["us"] / md["fused"]["us"])
 
 
 @pytest.mark.parametrize("world", [2, 3])

@@ -19,14 +19,15 @@
 // Work split: the T = ceil(N / 128) tiles of a decode shape are far fewer
 // than the SMs (7B: 28, 72B: 64), so each tile is cut into j equal K ranges
 // and its j CTAs form one thread-block cluster (j = 1..16, chosen on the host
-// so that the T clusters fill the GPU in one wave; plan_down_decode in
-// swiglu_api.cu). Each CTA accumulates its K range in TMEM, then writes the
+// so that the T clusters fit the GPU in one wave: plan_decode_splits in
+// schedule.cuh). Each CTA accumulates its K range in TMEM, then writes the
 // FP32 partial [mt tokens x 128 columns] into its own shared memory (the
 // operand ring, idle by then); after a cluster barrier, CTA r sums the r-th
 // slice of the tile from all j partials through distributed shared memory,
-// in rank order (= K order, so results are bit-reproducible), and stores it
-// as BF16; a second cluster barrier keeps every partial alive until it has
-// been read. The reduction needs no global workspace, no atomics and no L2
+// in rank order (= K order, so results are bit-reproducible), loading every
+// rank's values of up to 16 / j chunks before adding any (decode_finish),
+// and stores it as BF16; a second cluster barrier keeps every partial alive
+// until it has been read. The reduction needs no global workspace, no atomics and no L2
 // round trip, and no CTA waits for one outside its cluster, whose CTAs the
 // hardware schedules together.
 //

@@ -31,8 +31,6 @@ constexpr int kAssumedMaxSms = 256;  // workspace sizing when no device answers
 constexpr int kPairStages = 6;
 constexpr int kDownTileCols = 256;   // output columns of a plain-product (down) tile
 constexpr int64_t kWideMinM = 256;   // from this many rows on, the wide down-projection kernel
-constexpr int64_t kSlimMaxM = 128;   // up to this many rows, and
-constexpr int kSlimMaxPairTiles = 8; // fewer 256-column tiles: the 1-SM plain kernel (64 columns)
 constexpr int64_t kPairMinM = 256;   // from this many tokens on, the 2-SM kernel
 constexpr int64_t kDecodeMaxM = 128; // up to this many rows: the decode down-projection kernel
 using FusedC = FusedCfg<kFusedStages>;
@@ -392,7 +390,9 @@ int plan_down_decode(int64_t N, int64_t K, int sms, const int *clusters) {
 // same packed W3:
 //   * kDownDecode (down_decode_kernel.cuh, swapped operands: tiles of 128
 //     output columns x all token rows, split K ranges summed inside a
-//     cluster, plan_down_decode): every product of up to kDecodeMaxM rows;
+//     cluster, plan_down_decode): every product of up to kDecodeMaxM rows
+//     (0.5B, M=128: 8.0 us; the 1-SM plain mode below took 14.4 us and
+//     the CTA-pair kernel 41 us);
 //   * kDownWide (down_wide_kernel.cuh, CTA pairs, tiles of 256 x 512): a
 //     third fewer operand bytes per flop than 256-column tiles, which shows
 //     at the power cap as a higher SM clock (7B, M=8192: 631 against 666 us;
@@ -400,19 +400,15 @@ int plan_down_decode(int64_t N, int64_t K, int sms, const int *clusters) {
 //     512-column FP32 partials for split tiles; it takes a call when whole
 //     wide tiles fill at least 90% of their last wave (from kWideMinM rows
 //     on), as whole tiles;
-//   * kDownSlim (the 1-SM kernel's plain mode, tiles of 128 x 64): decode-
-//     sized products (up to kSlimMaxM rows) with a handful of 256-column
-//     tiles, where the CTA-pair kernel's K split would put ten or more pairs
-//     on each tile (0.5B, M=128: 21.8 against 41.1 us); with more output
-//     columns its 64-column tiles re-read A once per tile, which costs more
-//     than the pairs' larger partials (72B, M=32: 110 against 82 us), so the
-//     pairs keep those;
 //   * kDownPair (the CTA-pair kernel's plain mode, 256 x 256, plan_down):
 //     the rest (few output tiles for the pairs, e.g. the 1.5B and 7B M=2048
-//     shapes).
-// SWIGLU_DOWN_TILE=64|256|512, read on every call, forces one of them
-// (ablations and tests); with the wide kernel forced, SWIGLU_SCHEDULE picks
-// its form (dp, sk, sk-tail, sk-aligned; whole tiles otherwise).
+//     shapes);
+//   * kDownSlim (the 1-SM kernel's plain mode, tiles of 128 x 64,
+//     plan_down_slim): forced only (ablations and tests).
+// SWIGLU_DOWN_TILE=64|128|256|512, read on every call, forces one of them
+// (128 only up to kDecodeMaxM rows); with the wide kernel forced,
+// SWIGLU_SCHEDULE picks its form (dp, sk, sk-tail, sk-aligned; whole tiles
+// otherwise).
 enum DownKind { kDownPair = 0, kDownWide = 1, kDownSlim = 2, kDownDecode = 3 };
 struct DownPlan {
     int kind;
@@ -431,12 +427,8 @@ DownPlan plan_down_any(int64_t M, int64_t N, int64_t K, int workers, int sms,
     const long long T = static_cast<long long>(m_tiles) * n_tiles;
     const long long waves = (T + workers - 1) / workers;
     const double eff = static_cast<double>(T) / (static_cast<double>(waves) * workers);
-    // the CTA-pair kernel's tiles for this product (256 x 256)
-    const long long pair_tiles = ((M + 255) / 256) * ((K + kDownTileCols - 1) / kDownTileCols);
     int kind = M <= kDecodeMaxM ? kDownDecode
-               : (M <= kSlimMaxM && pair_tiles < kSlimMaxPairTiles)
-                   ? kDownSlim
-                   : (M >= kWideMinM && eff >= 0.9 ? kDownWide : kDownPair);
+                                : (M >= kWideMinM && eff >= 0.9 ? kDownWide : kDownPair);
     const char *v = std::getenv("SWIGLU_DOWN_TILE");
     if (v && std::strcmp(v, "64") == 0) kind = kDownSlim;
     if (v && std::strcmp(v, "128") == 0 && M <= kDecodeMaxM) kind = kDownDecode;

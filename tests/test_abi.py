@@ -212,6 +212,12 @@ def test_down_sizes_and_host_validation(lib):
     assert sg.swiglu_down_packed_weight_bytes(72, 8) == 256 * 128 * 2         # N -> 128
     assert sg.swiglu_down_packed_weight_bytes(0, 8) == 0
     assert sg.swiglu_down_workspace_bytes(2048, 8960, 1536) >= 0
+    # up to 128 rows the decode kernel serves the call and sums its split
+    # tiles inside a cluster: no workspace (7B M=16, the 0.5B shape); from
+    # 129 rows on the CTA-pair kernel's stream-K needs one
+    assert sg.swiglu_down_workspace_bytes(16, 18944, 3584) == 0
+    assert sg.swiglu_down_workspace_bytes(128, 4864, 896) == 0
+    assert sg.swiglu_down_workspace_bytes(129, 4864, 896) > 0
     assert sg.swiglu_mlp_workspace_bytes(2048, 8960, 1536) >= max(
         sg.swiglu_workspace_bytes(2048, 8960, 1536), sg.swiglu_down_workspace_bytes(2048, 8960, 1536))
     d = lib.swiglu_down_forward

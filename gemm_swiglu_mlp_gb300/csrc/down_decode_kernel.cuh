@@ -79,6 +79,7 @@ struct DecodeArgs {
     int mt;                    // M rounded up to 16: UMMA N and the Y box's rows
     int k_blocks;
     int splits;                // K ranges per tile = cluster size, 1..16, <= k_blocks
+    int weights_early;         // 1: no launch still in flight writes W3 (see the prologue)
     uint16_t *out;             // [M, N] row-major BF16
 #ifdef SWIGLU_TEST_FAULT_INJECTION
     int skip_first_fill;       // test build only: never fill the first pipeline stage
@@ -179,28 +180,55 @@ __global__ void __launch_bounds__(DecodeCfg<MTB>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    // The prologue touched no global memory: let the next launch begin, ask
-    // L2 for the first weight stages (the weights do not depend on the
-    // previous launch), then wait for the previous launch's results (Y).
+    // The prologue touched no global memory: let the next launch begin, then
+    // wait for the previous launch's results (Y). Meanwhile the producer asks
+    // L2 for the first weight stages, or, when the caller guarantees that no
+    // launch still in flight writes W3 (weights_early), already loads the
+    // weights of the first ring pass into shared memory.
     const int wrow = 128 * (tile & 1);
     const int wtile0 = (tile >> 1) * args.k_blocks;
+    const uint32_t tx = static_cast<uint32_t>(C::W_BYTES + mt * kRowBytes);
+    // producer bookkeeping for the drain after an abort
+    uint32_t issued_mask = 0, last_parity = 0;
+    int pre = 0;   // stages whose weights were loaded before the wait
     griddep_launch_dependents();
     if (warp == 0 && lane == 0) {
-        const int kend = (kb1 - kb0 < kPrefetchStages) ? kb1 : kb0 + kPrefetchStages;
-        for (int kb = kb0; kb < kend; ++kb) tma_prefetch_3d(&tmW, 0, wrow, wtile0 + kb);
+        bool early = args.weights_early != 0;
+#ifdef SWIGLU_TEST_FAULT_INJECTION
+        early = early && !args.skip_first_fill;
+#endif
+        if (early) {
+            // the ring's first pass: every stage is free (phase 0)
+            pre = (kb1 - kb0 < C::STAGES) ? kb1 - kb0 : C::STAGES;
+            for (int st = 0; st < pre; ++st) {
+                mbar_arrive_expect_tx(full_bar(st), tx);
+                tma_load_3d(sbase + C::OFF_W + st * C::W_BYTES, &tmW, full_bar(st), 0, wrow,
+                            wtile0 + kb0 + st);
+                issued_mask |= 1u << st;
+            }
+        } else {
+            const int kend = (kb1 - kb0 < kPrefetchStages) ? kb1 : kb0 + kPrefetchStages;
+            for (int kb = kb0; kb < kend; ++kb) tma_prefetch_3d(&tmW, 0, wrow, wtile0 + kb);
+        }
     }
     griddep_wait();
 
-    // producer bookkeeping for the drain after an abort
-    uint32_t issued_mask = 0, last_parity = 0;
-
     if (warp == 0) {
         if (lane == 0) {
-            const uint32_t tx = static_cast<uint32_t>(C::W_BYTES + mt * kRowBytes);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             for (int kb = kb0; kb < kb1; ++kb) {
+                if (kb - kb0 < pre) {
+                    // this stage's weights are in flight already: its Y block
+                    tma_load_2d(sbase + C::OFF_Y + stage * C::Y_BYTES, &tmY, full_bar(stage),
+                                kb * ElemBF16::kBK, 0);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    continue;
+                }
                 if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                     ok = false;
                     break;

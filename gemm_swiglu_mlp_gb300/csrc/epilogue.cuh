@@ -80,6 +80,8 @@ struct FusedArgs {
     int ticket_index;         // counters[ticket_index]: start-order tickets of a K-split pair launch
     int dyn_tiles;            // 1: tiles past the first wave are handed out at run time (pair kernel)
     int tile_counter_index;   // counters[i]: next dynamic tile; counters[i + 1]: pairs finished
+    int late_trigger;         // 1: let the next launch start only after this one's dependency
+                              // wait (so that every launch before this one has completed)
 #ifdef SWIGLU_TEST_FAULT_INJECTION
     int skip_first_fill;      // test build only: never fill the first pipeline stage
 #endif

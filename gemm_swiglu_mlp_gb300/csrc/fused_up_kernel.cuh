@@ -159,8 +159,9 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
     // it waits, the producer asks L2 for this CTA's first pipeline stages (a
     // prefetch only moves device memory into L2, where every SM's writes
     // land, so what the previous launch writes afterwards is still what the
-    // loads below see).
-    griddep_launch_dependents();
+    // loads below see). With late_trigger the next launch may start only
+    // after the wait below.
+    if (!args.late_trigger) griddep_launch_dependents();
     if (warp == 0 && lane == 0) {
         UnitIter it;
         it.init(sched, cta);
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
         }
     }
     griddep_wait();
+    if (args.late_trigger) griddep_launch_dependents();
 
     // Producer bookkeeping kept for the drain after an abort: which stages
     // received a load, and the parity of the phase of the last one.

@@ -217,8 +217,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
     // it waits (the previous launch's last tiles), the producer asks L2 for
     // this CTA's first pipeline stages: a prefetch reads device memory into
     // L2 only, and L2 is where every SM's writes land, so data the previous
-    // launch writes afterwards is still what the loads below see.
-    griddep_launch_dependents();
+    // launch writes afterwards is still what the loads below see. With
+    // late_trigger the next launch may start only after the wait below.
+    if (!args.late_trigger) griddep_launch_dependents();
     if (warp == 0 && lane == 0) {
         UnitIter it;
         it.init(sched, pair);
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
         }
     }
     griddep_wait();
+    if (args.late_trigger) griddep_launch_dependents();
     if (sched.sk_iters > 0) {
         // worker number by start order (see the header comment); the peer
         // CTA gets it through distributed shared memory

@@ -687,7 +687,7 @@ size_t workspace_bytes_impl(int64_t M, int64_t N, int64_t K) {
 template <typename E, bool IL = false>
 int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t N, int64_t K,
                  float gate_scale, float up_scale, void *workspace, size_t workspace_bytes,
-                 void *stream, size_t packed_bytes) {
+                 void *stream, size_t packed_bytes, bool late_trigger = false) {
     const size_t esize = E::kFp8 ? 1 : 2;
     const int64_t kmul = E::kFp8 ? 16 : 8;   // 16-byte rows of A
     if (!A || !Wpacked || !Y) return SWIGLU_ERR_INVALID_ARG;
@@ -762,6 +762,7 @@ int forward_impl(const void *A, const void *Wpacked, void *Y, int64_t M, int64_t
     args.ticket_index = ticket_index(st->sm_count);
     args.tile_counter_index = tile_counter_index(st->sm_count);
     args.dyn_tiles = dynamic_tiles(sched, pair) ? 1 : 0;
+    args.late_trigger = late_trigger ? 1 : 0;
 
     // Both kernels are launched with programmatic stream serialization: a
     // launch may begin while the previous kernel in the stream finishes; the
@@ -983,7 +984,8 @@ int down_wide_launch(const WorkSched &sched, const void *Y, const void *W3packed
 // ceil(K / 128) * splits CTAs in clusters of `splits`; `clusters` as in
 // DeviceState (a size of which none fits is refused).
 int down_decode_launch(int splits, const int *clusters, const void *Y, const void *W3packed,
-                       void *out, int64_t M, int64_t N, int64_t K, void *stream) {
+                       void *out, int64_t M, int64_t N, int64_t K, void *stream,
+                       bool weights_early) {
     const int kt = static_cast<int>((K + kDownTileCols - 1) / kDownTileCols);
     const int k_blocks = static_cast<int>((N + ElemBF16::kBK - 1) / ElemBF16::kBK);
     const int64_t tiles = (K + 127) / 128;
@@ -1002,6 +1004,7 @@ int down_decode_launch(int splits, const int *clusters, const void *Y, const voi
     args.mt = mt;
     args.k_blocks = k_blocks;
     args.splits = splits;
+    args.weights_early = weights_early ? 1 : 0;
     args.out = static_cast<uint16_t *>(out);
 #ifdef SWIGLU_TEST_FAULT_INJECTION
     args.skip_first_fill = g_test_skip_first_fill;
@@ -1093,8 +1096,13 @@ int down_slim_launch(const WorkSched &sched, const void *Y, const void *W3packed
 
 // out [M, K] = Y [M, N] x W3 [N, K] (W3 packed by swiglu_pack_down_weights),
 // BF16 in and out, FP32 accumulation, on the kernel plan_down_any picks.
+// weights_early: no launch still in flight on `stream` writes W3packed (the
+// whole-MLP call, whose up-projection lets this launch start only after its
+// own dependency wait), so the decode kernel may load W3 before waiting for
+// the previous launch.
 int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M, int64_t N,
-                      int64_t K, void *workspace, size_t workspace_bytes, void *stream) {
+                      int64_t K, void *workspace, size_t workspace_bytes, void *stream,
+                      bool weights_early = false) {
     const int c = down_checks(Y, W3packed, out, M, N, K);
     if (c != SWIGLU_OK) return c;
     const size_t obytes = static_cast<size_t>(M) * K * 2;
@@ -1122,7 +1130,7 @@ int down_forward_impl(const void *Y, const void *W3packed, void *out, int64_t M,
                                 st->sm_count, stream);
     if (plan.kind == kDownDecode)
         return down_decode_launch(plan.splits, st->decode_clusters, Y, W3packed, out, M, N, K,
-                                  stream);
+                                  stream, weights_early);
     if (plan.kind == kDownSlim)
         return down_slim_launch(sched, Y, W3packed, out, M, N, K, workspace, ws_need > 0,
                                 st->sm_count, stream);
@@ -1272,9 +1280,16 @@ int swiglu_mlp_forward(const void *A, const void *Wpacked, const void *W3packed,
         if (overlaps(workspace, need, out, obytes) || overlaps(workspace, need, W3packed, p3bytes))
             return SWIGLU_ERR_INVALID_ARG;
     }
-    int s = swiglu_up_forward(A, Wpacked, Y, M, N, K, workspace, workspace_bytes, stream);
+    // The up-projection lets the down-projection start only after its own
+    // dependency wait: every launch before this call has then completed,
+    // and the up-projection writes Y and the workspace only, so the
+    // down-projection may read W3packed before its own wait.
+    int s = forward_impl<ElemBF16>(A, Wpacked, Y, M, N, K, 1.0f, 1.0f, workspace,
+                                   workspace_bytes, stream, swiglu_packed_weight_bytes(N, K),
+                                   true);
     if (s != SWIGLU_OK) return s;
-    return down_forward_impl(Y, W3packed, out, M, N, K, workspace, workspace_bytes, stream);
+    return down_forward_impl(Y, W3packed, out, M, N, K, workspace, workspace_bytes, stream,
+                             true);
 }
 
 int swiglu_check_device_status(void *stream, uint32_t *raw_word) {

@@ -354,6 +354,11 @@ size_t swiglu_mlp_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * out = (SiLU(A x W1) (.) (A x W2)) x W3: swiglu_up_forward into Y, then
  * swiglu_down_forward from Y, two launches on `stream` (the second starts
  * while the first finishes and waits for its results before reading Y).
+ * The first lets the second start only after every earlier work on
+ * `stream` has completed, so the second (the decode kernel, up to 128 rows)
+ * may already load W3packed while the first finishes; as with any stream
+ * order, W3packed must not be written by work still running on another
+ * stream.
  *   A, Wpacked  as swiglu_up_forward; W3packed as swiglu_down_forward
  *   Y           device, BF16, [M, N]: the intermediate, caller-owned,
  *               overwritten (it holds the up-projection's output afterwards)

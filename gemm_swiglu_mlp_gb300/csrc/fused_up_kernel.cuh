@@ -424,9 +424,10 @@ __global__ void __launch_bounds__(FusedCfg<STAGES, BROWS>::THREADS, 1)
                         constexpr uint32_t kRingBytes = STAGES * (C::A_BYTES + C::B_BYTES);
                         const int per_round = static_cast<int>(kRingBytes / part_bytes);
                         if (last_unit && per_round >= 2) {
-                            // round 1 brings the first per_round partials to
-                            // slots 0..; later rounds bring the next ones to
-                            // slots 1.. and add to the running sum in slot 0
+                            // the first batch of copies brings the first
+                            // per_round partials to slots 0..; each later
+                            // batch brings the next ones to slots 1.. and
+                            // adds to the running sum in slot 0
                             float *ring = reinterpret_cast<float *>(smem);
                             for (int k0 = c_lo; k0 <= c_hi && ok;) {
                                 const int first = k0 == c_lo ? 0 : 1;
